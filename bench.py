@@ -1,0 +1,511 @@
+#!/usr/bin/env python
+"""Benchmark of the paged GQA attention hot path on one GB300 (or N replicas).
+
+Metric: decode KV GB/s (algorithmic bytes / time) on the bf16 GQA decode workload
+(batch 64, 24 q / 4 kv heads, head_dim 512, page_size 64, kv_len uniform in [1024, 8192],
+shuffled pages, split-K), with the causal bf16 prefill workload (lengths 2048 / 3000 /
+4096 / 6272, 24 / 4 heads, head_dim 512) reported beside it in TFLOP/s.  Each figure is
+also given as a fraction of the measured GB300 roofline (MEASURED_PEAKS.json).
+
+A step is one call of the C ABI (all kernels of the phase) on inputs already resident in
+HBM; "e2e" repeats the metric with host buffers (pinned host -> device copies of every
+input and the device -> host read of the output inside the timed region).
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference] [--all]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+MAIN = "gqa_decode_bf16"
+PREFILL = "causal_prefill_bf16"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DECODE_SOURCES = ("decode_impl.cuh", "common.cuh", "decode_inst.cuh", "kernel_params.h")
+PREFILL_SOURCES = ("prefill_impl.cuh", "common.cuh", "kernel_params.h")
+
+
+# ------------------------------------------------------------------------- work counts
+def _beta_x2(kv_dtype):
+    return {synth.KV_BF16: 4, synth.KV_FP8: 2, synth.KV_NVFP4: 1}[kv_dtype]
+
+
+def decode_bytes(c) -> int:
+    """Algorithmic bytes of one decode call: visible (in-window) K and V of every kv head,
+    NVFP4 block scales, q, out and lse."""
+    tokens = 0
+    for L in c.kv_lens:
+        tokens += min(L, c.window_left + 1) if c.window_left >= 0 else L
+    per_tok = c.Hkv * (c.d_qk + c.d_vo) * _beta_x2(c.kv_dtype) // 2
+    if c.kv_dtype == synth.KV_NVFP4:
+        per_tok += c.Hkv * (c.d_qk + c.d_vo) // 16
+    rows = c.total_q * c.Hq
+    return tokens * per_tok + rows * (c.d_qk * 2 + c.d_vo * 2 + 4)
+
+
+def prefill_flops(c) -> float:
+    """Unmasked (query, key) pairs x (2 d_qk + 2 d_vo) x query heads."""
+    pairs = 0
+    for L, Q in zip(c.kv_lens, c.qo_lens):
+        for i in range(Q):
+            pos = L - Q + i
+            hi = pos if c.causal else L - 1
+            lo = max(0, pos - c.window_left) if c.window_left >= 0 else 0
+            pairs += max(0, hi - lo + 1)
+    return float(pairs) * c.Hq * (2 * c.d_qk + 2 * c.d_vo)
+
+
+def prefill_kv_bytes(c) -> int:
+    return sum(c.kv_lens) * c.Hkv * (c.d_qk + c.d_vo) * _beta_x2(c.kv_dtype) // 2
+
+
+# ------------------------------------------------------------------------- environment
+def peaks():
+    p = dict(FALLBACK_PEAKS)
+    src = "fallback"
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            m = json.load(f)
+        for k in FALLBACK_PEAKS:
+            if k in m:
+                p[k] = float(m[k])
+        src = "measured"
+    return p, src
+
+
+def sources_digest(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        path = os.path.join(ROOT, "paged_gqa_attention_hd512_gb300", "csrc", n)
+        if os.path.exists(path):
+            h.update(open(path, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel: str, workload: str, digest: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current
+    kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path)).get(f"{kernel}:{workload}")
+    except (OSError, ValueError):
+        return None
+    if not rec or rec.get("source_digest") != digest:
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------- timing
+def time_region(fn, steps, warmup, barrier=None):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s)
+    for _ in range(steps):
+        fn()
+    e1.record(s)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return e0.elapsed_time(e1)
+
+
+def oracle_sample_rate(host_case, budget_s: float, kind: str):
+    """Time the fp64 oracle on a bounded sample of (sequence, kv head) units of the
+    workload; returns (rate in the metric's unit, seconds, description, threads)."""
+    import numpy as np
+
+    import oracle
+
+    threads = oracle.default_threads()
+    c = host_case
+    g = c.group
+    qo = c.qo_indptr.tolist()
+    units = [(b, k) for b in range(c.batch) for k in range(c.Hkv)]
+    stride = max(1, len(units) // 64)
+    units = units[::stride]
+
+    def run(n):
+        sel = units[:n]
+        tok, head = [], []
+        for b, k in sel:
+            for t in range(qo[b], qo[b + 1]):
+                for h in range(k * g, (k + 1) * g):
+                    tok.append(t)
+                    head.append(h)
+        t0 = time.perf_counter()
+        oracle.rows(c, np.array(tok), np.array(head), threads=threads)
+        return time.perf_counter() - t0, sel
+
+    n = min(len(units), threads)
+    dt, sel = run(n)
+    while dt < budget_s * 0.4 and n < len(units):
+        n = min(len(units), max(n + 1, int(n * budget_s * 0.8 / max(dt, 1e-3))))
+        dt, sel = run(n)
+    seqs = sorted({b for b, _ in sel})
+    if kind == "decode":
+        tok = 0
+        for b, _ in sel:
+            L = c.kv_lens[b]
+            tok += min(L, c.window_left + 1) if c.window_left >= 0 else L
+        work = tok * (c.d_qk + c.d_vo) * _beta_x2(c.kv_dtype) // 2 + len(sel) * g * (2 * c.d_qk + 2 * c.d_vo + 4)
+        rate = work / dt / 1e9
+    else:
+        sub = synth.Case(**{f: getattr(c, f) for f in c.__dataclass_fields__})
+        pairs = 0
+        for b, _ in sel:
+            L, Q = c.kv_lens[b], c.qo_lens[b]
+            for i in range(Q):
+                pos = L - Q + i
+                lo = max(0, pos - c.window_left) if c.window_left >= 0 else 0
+                pairs += max(0, (pos if c.causal else L - 1) - lo + 1)
+        work = pairs * g * (2 * c.d_qk + 2 * c.d_vo)
+        rate = work / dt / 1e12
+        del sub
+    desc = f"{len(sel)} (sequence, kv head) units of {len(seqs)} sequences, all {g} query heads each"
+    return rate, dt, desc, threads
+
+
+# ------------------------------------------------------------------------- our arm
+def bench_decode(name, steps, warmup, barrier, gpu_index, pk, with_e2e=True, with_cpu=True):
+    import paged_gqa_attention_hd512_gb300 as pa
+
+    c = synth.workload(name, device="cuda")
+    kw = pa.case_args(c)
+    out = torch.empty(c.batch, c.Hq, c.d_vo, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(c.batch, c.Hq, dtype=torch.float32, device="cuda")
+
+    def step():
+        pa.paged_attn_decode(c.q, c.kv_cache, c.kv_indptr, c.kv_indices, c.kv_last_page_len, out=out, lse=lse,
+                             **kw)
+
+    step()
+    torch.cuda.synchronize()
+    if pa.paged_attn_check_device_error() != 0:
+        raise RuntimeError("device error word set after the first decode call")
+    nbytes = decode_bytes(c)
+    with ClockSampler(gpu_index) as clk:
+        pa.paged_attn_profile_begin(steps)
+        ms = time_region(step, steps, warmup, barrier)
+        n_k, k_ms = pa.paged_attn_profile_end()
+    clocks = clk.summary()
+    variant = pa.paged_attn_last_variant()
+    res = {"workload": name, "ms_per_step": ms / steps, "value": nbytes / (ms / steps * 1e-3) / 1e9,
+           "unit": "GB/s", "bytes_per_step": nbytes, "clocks": clocks, "variant": variant,
+           "gpu_launches": 3 * steps}
+    kern_ms = k_ms / max(1, n_k)
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    digest = sources_digest(DECODE_SOURCES)
+    res["roofline"] = {"bound": "hbm", "achieved": achieved, "peak": pk[0]["hbm_gbs"], "unit": "GB/s",
+                       "frac": achieved / pk[0]["hbm_gbs"], "traffic": traffic_record("decode_kernel", name, digest),
+                       "kernel": "decode_kernel", "kernel_ms": kern_ms, "launches_timed": n_k,
+                       "peak_source": f"{pk[1]} hbm_gbs", "source_digest": digest}
+    if with_e2e:
+        res["e2e"] = decode_e2e(c, kw, max(3, min(steps, 10)), nbytes)
+    if with_cpu:
+        host = c.to("cpu")
+        rate, dt, desc, threads = oracle_sample_rate(host, 12.0, "decode")
+        res["cpu_baseline"] = {"value": rate, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                               "sample": desc, "seconds": dt}
+    del c
+    torch.cuda.empty_cache()
+    return res
+
+
+def decode_e2e(c, kw, steps, nbytes):
+    """Same metric through the C ABI from pinned host buffers, copies in the timed region."""
+    import paged_gqa_attention_hd512_gb300 as pa
+
+    names = ("q", "kv_cache", "kv_indptr", "kv_indices", "kv_last_page_len")
+    host = {n: getattr(c, n).cpu().pin_memory() for n in names}
+    dev = {n: torch.empty_like(getattr(c, n)) for n in names}
+    out_h = torch.empty(c.batch, c.Hq, c.d_vo, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(c.batch, c.Hq, dtype=torch.float32).pin_memory()
+    out = torch.empty(c.batch, c.Hq, c.d_vo, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(c.batch, c.Hq, dtype=torch.float32, device="cuda")
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+    def step():
+        for n in names:
+            dev[n].copy_(host[n], non_blocking=True)
+        pa.paged_attn_decode(dev["q"], dev["kv_cache"], dev["kv_indptr"], dev["kv_indices"],
+                             dev["kv_last_page_len"], out=out, lse=lse, **kw)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    ms = time_region(step, steps, 2)
+    res = {"value": nbytes / (ms / steps * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
+    del dev, host
+    return res
+
+
+def bench_prefill(name, steps, warmup, gpu_index, pk, with_cpu=False):
+    import paged_gqa_attention_hd512_gb300 as pa
+
+    c = synth.workload(name, device="cuda")
+    kw = pa.case_args(c)
+    out = torch.empty(c.total_q, c.Hq, c.d_vo, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(c.total_q, c.Hq, dtype=torch.float32, device="cuda")
+
+    def step():
+        pa.paged_attn_prefill(c.q, c.qo_indptr, c.kv_cache, c.kv_indptr, c.kv_indices, c.kv_last_page_len,
+                              causal=bool(c.causal), out=out, lse=lse, **kw)
+
+    try:
+        step()
+    except pa.PagedAttnError as e:
+        return {"workload": name, "unavailable": str(e)}
+    torch.cuda.synchronize()
+    if pa.paged_attn_check_device_error() != 0:
+        raise RuntimeError("device error word set after the first prefill call")
+    flops = prefill_flops(c)
+    # the KV of this workload (~126 MB) is about the size of L2: flush L2 between steps
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    with ClockSampler(gpu_index) as clk:
+        for _ in range(warmup):
+            step()
+        torch.cuda.synchronize()
+        pa.paged_attn_profile_begin(steps)
+        tot = 0.0
+        for _ in range(steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(s)
+            step()
+            e1.record(s)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1)
+        n_k, k_ms = pa.paged_attn_profile_end()
+    ms = tot / steps
+    kern_ms = k_ms / max(1, n_k)
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+    digest = sources_digest(PREFILL_SOURCES)
+    res = {"workload": name, "ms_per_step": ms, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "flops_per_step": flops, "variant": pa.paged_attn_last_variant(), "clocks": clk.summary(),
+           "l2": "flushed between steps (256 MiB write)", "gpu_launches": 2 * steps,
+           "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk[0]["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": achieved / pk[0]["bf16_tflops"],
+                        "traffic": traffic_record("prefill_kernel", name, digest), "kernel": "prefill_kernel",
+                        "kernel_ms": kern_ms, "launches_timed": n_k, "peak_source": f"{pk[1]} bf16_tflops (burst)",
+                        "source_digest": digest}}
+    if with_cpu:
+        rate, dt, desc, threads = oracle_sample_rate(c.to("cpu"), 12.0, "prefill")
+        res["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                               "sample": desc, "seconds": dt}
+    del c, flush
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--all", action="store_true", help="also time every other workload")
+    ap.add_argument("--no-prefill", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference" and rank != 0:
+            return 0
+        if args.impl == "ours":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+            barrier = dist.barrier
+
+    if args.impl == "reference":
+        return reference_arm(args, world)
+
+    from paged_gqa_attention_hd512_gb300 import build as pa_build
+    if rank == 0 or world == 1:
+        pa_build.build()
+    if barrier:
+        barrier()
+    torch.cuda.set_device(local)
+    pk = peaks()
+    main_res = bench_decode(MAIN, args.steps, args.warmup, barrier, local, pk, with_cpu=(rank == 0))
+    ms = main_res["ms_per_step"]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = main_res["bytes_per_step"] * world / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "decode KV GB/s and prefill TFLOPS at hd512, % of GB300 roofline",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded Irwin-Hall(4) standard-normal draws; seeded random page order)",
+        "config": {"workload": "bf16 GQA decode: batch 64, 24 q / 4 kv heads, head_dim 512, page_size 64, "
+                               "kv_len uniform in [1024, 8192], shuffled pages, split-K",
+                   "name": MAIN, "l2": "inputs (2.4 GB of KV) larger than L2, no flush",
+                   "parallelism": f"{world} independent replica(s), no collective"},
+        "e2e": main_res.get("e2e"), "roofline": main_res["roofline"], "cpu_baseline": main_res.get("cpu_baseline"),
+        "clocks": main_res["clocks"], "gpu_launches": main_res["gpu_launches"], "variant": main_res["variant"],
+    }
+    if not args.no_prefill:
+        line["prefill"] = bench_prefill(PREFILL, max(3, min(50, args.steps // 40)), 3, local, pk,
+                                        with_cpu=(rank == 0 and args.all))
+    if args.all:
+        extra = []
+        for name in ("tiny_mqa_decode", "fp8_decode", "sliding_decode_d256"):
+            extra.append(bench_decode(name, max(3, args.steps // 10), args.warmup, barrier, local, pk,
+                                      with_e2e=False, with_cpu=False))
+        extra.append(bench_prefill("nvfp4_asym_prefill", max(3, min(50, args.steps // 40)), 3, local, pk))
+        line["secondary"] = extra
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def reference_arm(args, world):
+    """The oracle (fp64, host cores) as the reference arm: each step is a bounded sample of
+    the same workload, sized so the whole run ends within a few minutes."""
+    import numpy as np
+
+    import oracle
+
+    oracle.build()
+    c = synth.workload(MAIN, device="cuda" if torch.cuda.is_available() else "cpu").to("cpu")
+    threads = oracle.default_threads()
+    g = c.group
+    budget = 120.0 / (args.steps + args.warmup)
+    # calibrate: one (sequence, kv head) unit per thread
+    units = [(b, k) for b in range(c.batch) for k in range(c.Hkv)]
+
+    def rows_of(sel):
+        tok, head = [], []
+        for b, k in sel:
+            tok += [b] * g
+            head += list(range(k * g, (k + 1) * g))
+        return np.array(tok), np.array(head)
+
+    def unit_bytes(sel):
+        return sum(c.kv_lens[b] for b, _ in sel) * (c.d_qk + c.d_vo) * 2 + len(sel) * g * (2 * c.d_qk + 2 * c.d_vo + 4)
+
+    t0 = time.perf_counter()
+    oracle.rows(c, *rows_of(units[:1]), threads=1)
+    per_unit = time.perf_counter() - t0
+    n = max(1, min(len(units), int(budget / max(per_unit, 1e-6) * min(threads, 8))))
+    cursor = [0]
+
+    def one_step():
+        sel = [units[(cursor[0] + i) % len(units)] for i in range(n)]
+        cursor[0] += n
+        t = time.perf_counter()
+        oracle.rows(c, *rows_of(sel), threads=threads)
+        return time.perf_counter() - t, unit_bytes(sel)
+
+    for _ in range(args.warmup):
+        one_step()
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, nb = one_step()
+        tot_t += dt
+        tot_b += nb
+    value = tot_b / tot_t / 1e9
+    sample = f"{n} (sequence, kv head) unit(s) per step, all {g} query heads each, cycling through the batch"
+    line = {"impl": "reference", "metric": "decode KV GB/s and prefill TFLOPS at hd512, % of GB300 roofline",
+            "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "bf16 GQA decode: batch 64, 24 q / 4 kv heads, head_dim 512, page_size 64, "
+                                   "kv_len uniform in [1024, 8192], shuffled pages", "name": MAIN},
+            "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": sample, "value": value, "unit": "GB/s"},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,178 @@
+/*
+ * paged_attn.h -- C ABI of the GB300 (sm_103a) paged grouped-query attention library.
+ *
+ * Two calls, one per phase, over one paged KV cache:
+ *   paged_attn_decode   split-K flash-decoding of one query token per sequence
+ *   paged_attn_prefill  causal (or full) attention of the new tokens of each sequence
+ *
+ * The operation (defined by the pages this library follows; each source is a page title
+ * and the section on it):
+ *  - "[None][feat] Run Gemma4 head_dim 512 attention on Triton" (TensorRT-LLM PR #17772),
+ *    Approach: both phases read the combined HND cache
+ *    [num_pages, 2, num_kv_heads, page_size, head_dim] through kv_indptr / kv_indices /
+ *    kv_last_page_len (the same slicing as the FlashInfer decode plan); prefill is causal
+ *    when no custom mask is given; FP8 KV is dequantised in the kernel ("cast on load").
+ *    Test Coverage: head_dim up to 512, GQA ratios with non-power-of-two groups (12/4,
+ *    24/4) padded inside the kernel, page sizes 1..64 with partial and exact last pages,
+ *    split-K, sliding windows.  Not covered: unsupported inputs fail loudly instead of
+ *    returning wrong results.
+ *  - "feat(attention): asymmetric VO-split NVFP4 paged prefill (qk=512/vo=256) for
+ *    Gemma-4 on SM120/121" (FlashInfer PR #3684), Summary: head_dim_qk = 512 with
+ *    head_dim_vo = 256, independent K/V strides, NVFP4 KV with explicit scale strides in a
+ *    contiguous [all-data | all-SF] layout; NVFP4 split-KV correctness: packed e2m1 with
+ *    one FP8 scale per 16 consecutive head-dim elements of one token.
+ *
+ * Per sequence b and query head h (kv head h / (Hq/Hkv)), a query at position
+ * pos = kv_len - qo_len + i (decode: pos = kv_len - 1) sees key j < kv_len when
+ * (causal ? j <= pos : 1) and (window_left >= 0 ? j >= pos - window_left : 1):
+ *   out = softmax_j(sm_scale * q . K[j]) V[j],   lse = m + ln(sum_j exp(s_j - m))
+ * (natural log of the scaled scores).  A row with no visible key gets out = 0,
+ * lse = -inf.
+ *
+ * ---------------------------------------------------------------------------------
+ * Memory layout (all device memory, caller-owned; the library keeps no pointer after a
+ * call returns):
+ *  q          bf16, [batch, Hq, head_dim_qk] (decode) or [total_q, Hq, head_dim_qk]
+ *             (prefill), rows contiguous.  16-byte aligned.
+ *  kv_cache   page p (0 <= p < num_pages) is one contiguous block: the K block
+ *             [Hkv][page_size][head_dim_qk] followed by the V block
+ *             [Hkv][page_size][head_dim_vo], elements of kv_dtype.  With
+ *             head_dim_qk == head_dim_vo this is exactly
+ *             [num_pages, 2, Hkv, page_size, head_dim].  NVFP4 elements are packed two
+ *             per byte, element 2i in the low nibble of byte i.  16-byte aligned.
+ *  kv_indptr  int32 [batch+1]; sequence b owns logical pages
+ *             kv_indices[kv_indptr[b] .. kv_indptr[b+1]).
+ *  kv_indices int32 physical page ids, each in [0, num_pages).
+ *  kv_last_page_len int32 [batch], in [1, page_size] for a sequence with pages;
+ *             kv_len = (npages - 1) * page_size + kv_last_page_len.
+ *  qo_indptr  int32 [batch+1] (prefill): the new tokens of sequence b are q rows
+ *             qo_indptr[b] .. qo_indptr[b+1]; they are the last qo_len of its kv_len
+ *             tokens (the cache already holds them).  Requires kv_len >= qo_len.
+ *  out        bf16, [rows, Hq, head_dim_vo]; lse fp32 [rows, Hq] or NULL.
+ *  scales     see pa_kv_scales.
+ * Values inside the device arrays (page ids, lengths) are the caller's contract; they
+ * are not read on the host (no host-device synchronisation happens in a call).
+ *
+ * Streams and workspace: work is enqueued on `stream` (a cudaStream_t, NULL = legacy
+ * default stream) and the call returns without waiting.  The library owns a grow-only
+ * device workspace (work lists, split-K partials, an error word); it grows with
+ * cudaMalloc only when a call needs more than it has, so once warmed up a call
+ * allocates nothing.  Calls that overlap on the GPU (different streams) share that
+ * workspace and must not run concurrently.
+ *
+ * Errors: every entry point returns 0 (PA_OK) or a negative pa_status, and launches
+ * nothing when it rejects its arguments.
+ */
+#ifndef PAGED_ATTN_H_
+#define PAGED_ATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = -1, /* a null required pointer, a bad size, Hq % Hkv != 0, ... */
+  PA_ERR_UNSUPPORTED = -2, /* valid but not built (see the lists on each call) */
+  PA_ERR_ALIGNMENT = -3,   /* a pointer that is not 16-byte aligned */
+  PA_ERR_SMEM = -4,        /* the kernel's shared memory exceeds the device opt-in limit */
+  PA_ERR_CUDA = -5,        /* a CUDA runtime / driver call failed */
+  PA_ERR_DEVICE = -6       /* a kernel gave up on a bounded wait (see the error query) */
+} pa_status;
+
+typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1, PA_KV_NVFP4 = 2 } pa_kv_dtype;
+
+/* Dequantisation scales of the KV cache (all device pointers).
+ *  PA_KV_BF16:      all fields ignored (may be NULL).
+ *  PA_KV_FP8_E4M3:  k_scale, v_scale: one fp32 each, K^ = e4m3(code) * k_scale,
+ *                   V^ = e4m3(code) * v_scale (e4m3 "fn": bias 7, max 448, no inf).
+ *  PA_KV_NVFP4:     k_scale, v_scale: one fp32 global scale each; sf: the block-scale
+ *                   pool, page p holding [Hkv][page_size][head_dim_qk/16] K scales
+ *                   then [Hkv][page_size][head_dim_vo/16] V scales (e4m3 bytes), i.e.
+ *                   the contiguous [all-data | all-SF] arrangement;
+ *                   K^ = e2m1(nibble) * e4m3(sf) * k_scale (likewise V).
+ *                   16-byte aligned. */
+typedef struct {
+  const float* k_scale;
+  const float* v_scale;
+  const uint8_t* sf;
+} pa_kv_scales;
+
+/*
+ * paged_attn_decode -- one query token per sequence, split-K over the KV length.
+ *
+ * q [batch, num_qo_heads, head_dim_qk] bf16; out [batch, num_qo_heads, head_dim_vo]
+ * bf16; lse [batch, num_qo_heads] fp32 or NULL.  Every query head of one kv head is
+ * served by the same CTA (groups up to 16, padded inside the kernel).  The KV length of
+ * each sequence is cut into page-aligned chunks on the device; chunks of one sequence
+ * write partial (O, m, l) that a merge kernel combines.
+ *
+ * Supported: (head_dim_qk, head_dim_vo) in {(512,512), (512,256), (256,256)};
+ * num_qo_heads / num_kv_heads in [1, 16]; page_size in {1,2,4,8,16,32,64};
+ * kv_dtype any pa_kv_dtype.  window_left = -1 disables the sliding window.
+ * Returns PA_OK, or PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED / PA_ERR_ALIGNMENT /
+ * PA_ERR_SMEM / PA_ERR_CUDA; nothing is launched on error.
+ */
+int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_indptr,
+                      const int32_t* kv_indices, const int32_t* kv_last_page_len, int batch,
+                      int num_pages, int num_qo_heads, int num_kv_heads, int head_dim_qk,
+                      int head_dim_vo, int page_size, float sm_scale, int window_left,
+                      int kv_dtype, const pa_kv_scales* kv_scales, void* out, float* lse,
+                      void* stream);
+
+/*
+ * paged_attn_prefill -- attention of the new tokens (q rows qo_indptr[b]..[b+1]) of each
+ * sequence over its paged KV, causal when `causal` != 0 (bottom-right aligned: the new
+ * tokens are the last qo_len of kv_len).
+ *
+ * q [total_q, num_qo_heads, head_dim_qk] bf16; out [total_q, num_qo_heads, head_dim_vo]
+ * bf16; lse [total_q, num_qo_heads] fp32 or NULL.  QK^T and PV run as tcgen05 MMAs with
+ * TMEM accumulators; for head_dim_vo = 512 the VO dimension is processed in two halves.
+ * Supported shapes, page sizes and dtypes as for decode; group size up to 16.
+ * Returns as paged_attn_decode.
+ */
+int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q,
+                       const void* kv_cache, const int32_t* kv_indptr,
+                       const int32_t* kv_indices, const int32_t* kv_last_page_len, int batch,
+                       int num_pages, int num_qo_heads, int num_kv_heads, int head_dim_qk,
+                       int head_dim_vo, int page_size, float sm_scale, int window_left,
+                       int causal, int kv_dtype, const pa_kv_scales* kv_scales, void* out,
+                       float* lse, void* stream);
+
+/* Human-readable text of a pa_status value (static storage, never NULL). */
+const char* paged_attn_status_string(int status);
+
+/* Frees the library-owned workspace of the current device (blocking).  Returns PA_OK or
+ * PA_ERR_CUDA.  The next call allocates it again. */
+int paged_attn_release_workspace(void);
+
+/* Synchronises the current device, then reports and clears the device error word that
+ * kernels set when a bounded wait gives up: *code = 0 (none) or the wait site id.
+ * Returns PA_OK, PA_ERR_DEVICE when a wait gave up, PA_ERR_CUDA on a CUDA error. */
+int paged_attn_check_device_error(int* code);
+
+/* Test hook for split-K: force every decode chunk to `pages` pages (0 = automatic).
+ * The device still widens chunks when the workspace bound requires it.  Process-wide. */
+int paged_attn_set_decode_chunk_pages(int pages);
+
+/* Name of the kernel variant the last successful call on this host thread launched
+ * (for tests that must know which path ran).  Returns PA_OK; the text is truncated to
+ * len-1 characters. */
+int paged_attn_last_variant(char* buf, int len);
+
+/* Measurement hook.  After paged_attn_profile_begin(n), the next n calls record a pair of
+ * CUDA events on their stream around their main attention kernel (decode_kernel or
+ * prefill_kernel; not the planning or merge kernels).  paged_attn_profile_end waits for
+ * the last recorded event, returns the number of recorded launches and their summed
+ * device time in milliseconds, and stops recording.  Process-wide, not thread-safe.
+ * Returns PA_OK, PA_ERR_INVALID_ARG or PA_ERR_CUDA. */
+int paged_attn_profile_begin(int max_launches);
+int paged_attn_profile_end(int* launches, float* total_ms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_ATTN_H_ */

@@ -1,0 +1,375 @@
+// api.cu -- the C ABI (include/paged_attn.h): argument validation, the library-owned
+// workspace, TMA tensor maps over the paged cache, and the kernel launches.
+//
+// Every rejection happens on the host before anything is launched ("Run Gemma4 head_dim
+// 512 attention on Triton", Not covered: unsupported inputs fail loudly rather than
+// returning incorrect results; "feat(attention): asymmetric VO-split NVFP4 paged prefill
+// (qk=512/vo=256) for Gemma-4 on SM120/121", commit "support-or-reject-explicitly" and
+// the shared-memory validation guards).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "launch.h"
+#include "paged_attn.h"
+
+namespace pa {
+namespace {
+
+thread_local char g_variant[64] = "none";
+
+// measurement hook state: event pairs recorded around the main kernel of each call
+struct Profile {
+  std::vector<cudaEvent_t> start, stop;
+  int used = 0;
+  bool on = false;
+};
+Profile g_prof;
+std::mutex g_prof_mutex;
+
+void prof_mark(cudaStream_t s, bool begin) {
+  std::lock_guard<std::mutex> lock(g_prof_mutex);
+  if (!g_prof.on || g_prof.used >= (int)g_prof.start.size()) return;
+  if (begin) {
+    cudaEventRecord(g_prof.start[g_prof.used], s);
+  } else {
+    cudaEventRecord(g_prof.stop[g_prof.used], s);
+    ++g_prof.used;
+  }
+}
+int g_forced_chunk_pages = 0;
+std::mutex g_ws_mutex;
+
+constexpr int kMaxDevices = 64;
+struct Workspace {
+  void* base = nullptr;
+  size_t bytes = 0;
+};
+Workspace g_ws[kMaxDevices];
+constexpr size_t kErrOffset = 0;      // int error word
+constexpr size_t kFixedBytes = 256;   // error word region
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Make sure the current device's workspace holds at least `need` bytes; returns its
+// base or nullptr.  Growth frees the old buffer (cudaFree waits for the device).
+void* workspace(size_t need, int* status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *status = PA_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  Workspace& w = g_ws[dev];
+  if (w.bytes >= need) return w.base;
+  if (w.base) cudaFree(w.base);
+  w.base = nullptr;
+  w.bytes = 0;
+  size_t bytes = align_up(need + need / 4, 1 << 20);
+  if (cudaMalloc(&w.base, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    *status = PA_ERR_CUDA;
+    return nullptr;
+  }
+  if (cudaMemset(w.base, 0, kFixedBytes) != cudaSuccess) {
+    *status = PA_ERR_CUDA;
+    return nullptr;
+  }
+  w.bytes = bytes;
+  return w.base;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 3-D byte tensor [pages][rows][row_bytes] with the given page stride; boxes of
+// [1][box_rows][box_inner] bytes.
+bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t pages,
+              uint64_t page_stride, uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {row_bytes, rows, pages};
+  cuuint64_t strides[2] = {row_bytes, page_stride};
+  cuuint32_t box[3] = {box_inner, box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+int x2_of(int kvt) { return kvt == KV_BF16 ? 4 : (kvt == KV_FP8 ? 2 : 1); }
+
+// Checks shared by both phases.  Returns PA_OK or an error status.
+int check_common(const void* q, const void* kv_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
+                 const int32_t* kv_last_page_len, int batch, int num_pages, int Hq, int Hkv, int dqk, int dvo,
+                 int page_size, float sm_scale, int window_left, int kv_dtype, const pa_kv_scales* sc,
+                 const void* out, const float* lse) {
+  if (batch < 0 || num_pages < 1 || Hq < 1 || Hkv < 1) return PA_ERR_INVALID_ARG;
+  if (!q || !kv_cache || !kv_indptr || !kv_indices || !kv_last_page_len || !out) return PA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return PA_ERR_INVALID_ARG;
+  if (Hq / Hkv > 16) return PA_ERR_UNSUPPORTED;
+  if (!((dqk == 512 && dvo == 512) || (dqk == 512 && dvo == 256) || (dqk == 256 && dvo == 256)))
+    return PA_ERR_UNSUPPORTED;
+  if (page_size < 1 || page_size > 64 || (page_size & (page_size - 1))) return PA_ERR_UNSUPPORTED;
+  if (!std::isfinite(sm_scale) || window_left < -1) return PA_ERR_INVALID_ARG;
+  if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3 && kv_dtype != PA_KV_NVFP4) return PA_ERR_INVALID_ARG;
+  if (kv_dtype != PA_KV_BF16) {
+    if (!sc || !sc->k_scale || !sc->v_scale) return PA_ERR_INVALID_ARG;
+    if (!aligned(sc->k_scale, 4) || !aligned(sc->v_scale, 4)) return PA_ERR_ALIGNMENT;
+  }
+  if (kv_dtype == PA_KV_NVFP4) {
+    if (!sc->sf) return PA_ERR_INVALID_ARG;
+    if (!aligned(sc->sf, 16)) return PA_ERR_ALIGNMENT;
+  }
+  if (!aligned(q, 16) || !aligned(kv_cache, 16) || !aligned(out, 16)) return PA_ERR_ALIGNMENT;
+  if (!aligned(kv_indptr, 4) || !aligned(kv_indices, 4) || !aligned(kv_last_page_len, 4)) return PA_ERR_ALIGNMENT;
+  if (lse && !aligned(lse, 4)) return PA_ERR_ALIGNMENT;
+  const uint64_t page_bytes = (uint64_t)Hkv * page_size * (dqk + dvo) * x2_of(kv_dtype) / 2;
+  if ((uint64_t)num_pages * page_bytes >= (1ull << 46)) return PA_ERR_INVALID_ARG;
+  return PA_OK;
+}
+
+int device_sms(int* smem_optin) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaDeviceGetAttribute(smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  return sms;
+}
+
+// K, V (and NVFP4 scale) maps over the cache; box_rows rows per box.
+bool make_kv_maps(CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tsfk, CUtensorMap* tsfv, const void* kv_cache,
+                  const uint8_t* sf, int num_pages, int Hkv, int dqk, int dvo, int ps, int kvt, int box_rows,
+                  bool swz) {
+  const int x2 = x2_of(kvt);
+  const uint64_t k_row = (uint64_t)dqk * x2 / 2, v_row = (uint64_t)dvo * x2 / 2;
+  const uint64_t rows = (uint64_t)Hkv * ps;
+  const uint64_t page_bytes = rows * (k_row + v_row);
+  const uint8_t* base = static_cast<const uint8_t*>(kv_cache);
+  if (!make_map(tk, base, k_row, rows, num_pages, page_bytes, 128, box_rows, swz)) return false;
+  if (!make_map(tv, base + rows * k_row, v_row, rows, num_pages, page_bytes, 128, box_rows, swz)) return false;
+  if (kvt == KV_NVFP4) {
+    const uint64_t sk = dqk / 16, sv = dvo / 16, sf_page = rows * (sk + sv);
+    if (!make_map(tsfk, sf, sk, rows, num_pages, sf_page, (uint32_t)sk, box_rows, false)) return false;
+    if (!make_map(tsfv, sf + rows * sk, sv, rows, num_pages, sf_page, (uint32_t)sv, box_rows, false)) return false;
+  } else {
+    *tsfk = *tk;
+    *tsfv = *tv;
+  }
+  return true;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* paged_attn_status_string(int status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported configuration (shape, group size, page size or dtype not built)";
+    case PA_ERR_ALIGNMENT: return "pointer not aligned (device arrays need 16-byte alignment, int32 arrays 4)";
+    case PA_ERR_SMEM: return "kernel shared memory exceeds the device opt-in limit";
+    case PA_ERR_CUDA: return "CUDA runtime or driver call failed";
+    case PA_ERR_DEVICE: return "a kernel gave up on a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+int paged_attn_last_variant(char* buf, int len) {
+  if (!buf || len <= 0) return PA_ERR_INVALID_ARG;
+  std::snprintf(buf, (size_t)len, "%s", g_variant);
+  return PA_OK;
+}
+
+int paged_attn_set_decode_chunk_pages(int pages) {
+  if (pages < 0) return PA_ERR_INVALID_ARG;
+  g_forced_chunk_pages = pages;
+  return PA_OK;
+}
+
+int paged_attn_release_workspace(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  if (g_ws[dev].base && cudaFree(g_ws[dev].base) != cudaSuccess) return PA_ERR_CUDA;
+  g_ws[dev].base = nullptr;
+  g_ws[dev].bytes = 0;
+  return PA_OK;
+}
+
+int paged_attn_profile_begin(int max_launches) {
+  if (max_launches < 1 || max_launches > (1 << 20)) return PA_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_prof_mutex);
+  for (size_t i = 0; i < g_prof.start.size(); ++i) {
+    cudaEventDestroy(g_prof.start[i]);
+    cudaEventDestroy(g_prof.stop[i]);
+  }
+  g_prof.start.assign(max_launches, nullptr);
+  g_prof.stop.assign(max_launches, nullptr);
+  for (int i = 0; i < max_launches; ++i)
+    if (cudaEventCreate(&g_prof.start[i]) != cudaSuccess || cudaEventCreate(&g_prof.stop[i]) != cudaSuccess)
+      return PA_ERR_CUDA;
+  g_prof.used = 0;
+  g_prof.on = true;
+  return PA_OK;
+}
+
+int paged_attn_profile_end(int* launches, float* total_ms) {
+  std::lock_guard<std::mutex> lock(g_prof_mutex);
+  g_prof.on = false;
+  double sum = 0.0;
+  for (int i = 0; i < g_prof.used; ++i) {
+    if (cudaEventSynchronize(g_prof.stop[i]) != cudaSuccess) return PA_ERR_CUDA;
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, g_prof.start[i], g_prof.stop[i]) != cudaSuccess) return PA_ERR_CUDA;
+    sum += ms;
+  }
+  if (launches) *launches = g_prof.used;
+  if (total_ms) *total_ms = (float)sum;
+  return PA_OK;
+}
+
+int paged_attn_check_device_error(int* code) {
+  if (code) *code = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_ws_mutex);
+  if (!g_ws[dev].base) return PA_OK;
+  int v = 0;
+  char* e = static_cast<char*>(g_ws[dev].base) + kErrOffset;
+  if (cudaMemcpy(&v, e, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
+  if (v != 0 && cudaMemset(e, 0, sizeof v) != cudaSuccess) return PA_ERR_CUDA;
+  if (code) *code = v;
+  return v ? PA_ERR_DEVICE : PA_OK;
+}
+
+int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
+                      const int32_t* kv_last_page_len, int batch, int num_pages, int num_qo_heads,
+                      int num_kv_heads, int head_dim_qk, int head_dim_vo, int page_size, float sm_scale,
+                      int window_left, int kv_dtype, const pa_kv_scales* kv_scales, void* out, float* lse,
+                      void* stream) {
+  int st = check_common(q, kv_cache, kv_indptr, kv_indices, kv_last_page_len, batch, num_pages, num_qo_heads,
+                        num_kv_heads, head_dim_qk, head_dim_vo, page_size, sm_scale, window_left, kv_dtype,
+                        kv_scales, out, lse);
+  if (st != PA_OK) return st;
+  if (batch == 0) return PA_OK;
+  const int group = num_qo_heads / num_kv_heads;
+  const int hp = group <= 8 ? 8 : 16;
+  int smem_optin = 0;
+  const int sms = device_sms(&smem_optin);
+  if (sms <= 0) return PA_ERR_CUDA;
+  const int smem = decode_smem_bytes(kv_dtype, head_dim_qk, head_dim_vo, hp);
+  if (smem > smem_optin) return PA_ERR_SMEM;
+
+  DecodeLaunch L;
+  std::memset(&L, 0, sizeof L);
+  const int T = decode_tile_tokens(kv_dtype, head_dim_qk);
+  const int box_rows = page_size < T ? page_size : T;
+  const bool swz = page_size >= 8;
+  if (!make_kv_maps(&L.tk, &L.tv, &L.tsfk, &L.tsfv, kv_cache, kv_scales ? kv_scales->sf : nullptr, num_pages,
+                    num_kv_heads, head_dim_qk, head_dim_vo, page_size, kv_dtype, box_rows, swz))
+    return PA_ERR_CUDA;
+
+  const int grid = sms;
+  const int forced = g_forced_chunk_pages;
+  const int target = forced > 0 ? 2048 : (16 * grid + num_kv_heads - 1) / num_kv_heads;
+  const int max_chunks = target + batch;
+  size_t off = kFixedBytes;
+  const size_t o_hdr = off; off = align_up(off + 64, 256);
+  const size_t o_chunks = off; off = align_up(off + (size_t)max_chunks * sizeof(DecodeChunk), 256);
+  const size_t o_seq = off; off = align_up(off + (size_t)batch * sizeof(int2), 256);
+  const size_t o_ml = off; off = align_up(off + (size_t)max_chunks * num_qo_heads * sizeof(float2), 256);
+  const size_t o_o = off; off = align_up(off + (size_t)max_chunks * num_qo_heads * head_dim_vo * sizeof(float), 256);
+  char* ws = static_cast<char*>(workspace(off, &st));
+  if (!ws) return st;
+
+  DecodeParams& p = L.p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.kv_indptr = kv_indptr;
+  p.kv_indices = kv_indices;
+  p.kv_last_page_len = kv_last_page_len;
+  p.k_scale = kv_dtype != PA_KV_BF16 ? kv_scales->k_scale : nullptr;
+  p.v_scale = kv_dtype != PA_KV_BF16 ? kv_scales->v_scale : nullptr;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.err = reinterpret_cast<int*>(ws + kErrOffset);
+  p.hdr = reinterpret_cast<int*>(ws + o_hdr);
+  p.chunks = reinterpret_cast<DecodeChunk*>(ws + o_chunks);
+  p.seq_info = reinterpret_cast<int2*>(ws + o_seq);
+  p.ws_ml = reinterpret_cast<float2*>(ws + o_ml);
+  p.ws_o = reinterpret_cast<float*>(ws + o_o);
+  p.batch = batch;
+  p.Hq = num_qo_heads;
+  p.Hkv = num_kv_heads;
+  p.group = group;
+  p.page_size = page_size;
+  p.window_left = window_left;
+  p.max_chunks = max_chunks;
+  p.target_chunks = target;
+  p.forced_chunk_pages = forced;
+  p.box_rows = box_rows;
+  p.swz = swz ? 7 : 0;
+  p.sm_scale = sm_scale;
+  L.grid = grid;
+  L.stream = static_cast<cudaStream_t>(stream);
+
+  if (launch_decode_plan(p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  const char* name = "?";
+  cudaError_t e;
+  prof_mark(L.stream, true);
+  if (kv_dtype == PA_KV_BF16) e = launch_decode_bf16(head_dim_qk, head_dim_vo, hp, L, &name);
+  else if (kv_dtype == PA_KV_FP8_E4M3) e = launch_decode_fp8(head_dim_qk, head_dim_vo, hp, L, &name);
+  else e = launch_decode_nvfp4(head_dim_qk, head_dim_vo, hp, L, &name);
+  prof_mark(L.stream, false);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_decode_merge(head_dim_vo, p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};
+  std::snprintf(g_variant, sizeof g_variant, "%s_%s", name, kv_names[kv_dtype]);
+  return PA_OK;
+}
+
+int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, const void* kv_cache,
+                       const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                       int batch, int num_pages, int num_qo_heads, int num_kv_heads, int head_dim_qk,
+                       int head_dim_vo, int page_size, float sm_scale, int window_left, int causal, int kv_dtype,
+                       const pa_kv_scales* kv_scales, void* out, float* lse, void* stream) {
+  int st = check_common(q, kv_cache, kv_indptr, kv_indices, kv_last_page_len, batch, num_pages, num_qo_heads,
+                        num_kv_heads, head_dim_qk, head_dim_vo, page_size, sm_scale, window_left, kv_dtype,
+                        kv_scales, out, lse);
+  if (st != PA_OK) return st;
+  if (!qo_indptr || total_q < 0) return PA_ERR_INVALID_ARG;
+  (void)causal;
+  (void)stream;
+  return PA_ERR_UNSUPPORTED;
+}
+
+}  // extern "C"

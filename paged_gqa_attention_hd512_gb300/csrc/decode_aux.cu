@@ -1,0 +1,31 @@
+// decode_aux.cu -- the decode work planner, the split-K merge and shape queries.
+#define PA_DECODE_AUX 1
+#include "decode_inst.cuh"
+
+namespace pa {
+
+cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t s) {
+  decode_plan_kernel<<<1, 1024, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode_merge(int dvo, const DecodeParams& p, cudaStream_t s) {
+  const long rows = (long)p.batch * p.Hq;
+  const int blocks = (int)((rows * 32 + 255) / 256);
+  if (blocks == 0) return cudaSuccess;
+  if (dvo == 512) decode_merge_kernel<512><<<blocks, 256, 0, s>>>(p);
+  else decode_merge_kernel<256><<<blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+int decode_smem_bytes(int kvt, int dqk, int dvo, int hp) {
+  if (kvt == KV_BF16) return smem_of<KV_BF16>(dqk, dvo, hp);
+  if (kvt == KV_FP8) return smem_of<KV_FP8>(dqk, dvo, hp);
+  return smem_of<KV_NVFP4>(dqk, dvo, hp);
+}
+
+int decode_tile_tokens(int kvt, int dqk) {
+  return (kvt == KV_BF16 && dqk == 512) ? 32 : 64;
+}
+
+}  // namespace pa

@@ -1,0 +1,86 @@
+// kernel_params.h -- plain structs passed from the host launchers to the kernels.
+#pragma once
+
+#include <stdint.h>
+
+namespace pa {
+
+enum { KV_BF16 = 0, KV_FP8 = 1, KV_NVFP4 = 2 };
+
+// Wait-site ids recorded in the error word when a bounded wait gives up.
+enum {
+  SITE_DEC_EMPTY = 101,
+  SITE_DEC_FULL = 102,
+  SITE_PRE_Q = 201,
+  SITE_PRE_KV_EMPTY = 202,
+  SITE_PRE_KV_FULL = 203,
+  SITE_PRE_S_FULL = 204,
+  SITE_PRE_S_FREE = 205,
+  SITE_PRE_P_FULL = 206,
+  SITE_PRE_O_DONE = 207,
+  SITE_PRE_DEQ = 208,
+};
+
+// Decode work list entry: one page-aligned chunk of one sequence.
+struct DecodeChunk {
+  int b;           // sequence
+  int page_begin;  // first logical page (index into the sequence's page list)
+  int page_end;    // one past the last logical page
+  int split;       // index of this chunk among the sequence's chunks
+};
+
+struct DecodeParams {
+  const uint16_t* q;  // bf16 [batch, Hq, d_qk]
+  const int32_t* kv_indptr;
+  const int32_t* kv_indices;
+  const int32_t* kv_last_page_len;
+  const float* k_scale;  // device scalar or nullptr (bf16)
+  const float* v_scale;
+  uint16_t* out;  // bf16 [batch, Hq, d_vo]
+  float* lse;     // [batch, Hq] or nullptr
+  // workspace
+  int* err;           // error word
+  int* hdr;           // [0] number of chunks, [1] chunk pages
+  DecodeChunk* chunks;
+  int2* seq_info;     // per sequence: {first chunk row, number of chunks}
+  float* ws_o;        // [max_chunks][Hq][d_vo] unnormalised partial outputs
+  float2* ws_ml;      // [max_chunks][Hq] {running max (log2 units), running sum}
+  int batch, Hq, Hkv, group, page_size, window_left;
+  int max_chunks, target_chunks, forced_chunk_pages;
+  int box_rows;  // rows per TMA box: min(page_size, tile tokens)
+  int swz;       // 7 when the K/V smem tiles are 128B-swizzled, 0 when not
+  float sm_scale;
+};
+
+// Prefill work item: one tile of query rows (positions x heads of one kv head).
+struct PrefillItem {
+  int b;
+  int q_begin;  // first new-token index (within the sequence) of the tile
+  int kvh;
+  int cost;     // keys visited (for ordering)
+};
+
+struct PrefillParams {
+  const uint16_t* q;  // bf16 [total_q, Hq, d_qk]
+  const int32_t* qo_indptr;
+  const int32_t* kv_indptr;
+  const int32_t* kv_indices;
+  const int32_t* kv_last_page_len;
+  const float* k_scale;
+  const float* v_scale;
+  const uint8_t* kv_cache;  // for the plain-load (dequantising) producer
+  const uint8_t* sf;
+  uint16_t* out;  // bf16 [total_q, Hq, d_vo]
+  float* lse;
+  int* err;
+  int* hdr;  // [0] number of items
+  PrefillItem* items;
+  int batch, total_q, Hq, Hkv, group, page_size, window_left, causal, num_pages;
+  int rows_per_tile;  // query positions per 128-row tile (128 / group)
+  int max_items;
+  int box_rows;
+  int swz;
+  float sm_scale;
+};
+
+}  // namespace pa

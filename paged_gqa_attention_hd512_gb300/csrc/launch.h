@@ -1,0 +1,42 @@
+// launch.h -- host-side launch descriptors passed from api.cu to the per-dtype
+// translation units that instantiate the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kernel_params.h"
+
+namespace pa {
+
+struct DecodeLaunch {
+  CUtensorMap tk, tv, tsfk, tsfv;
+  DecodeParams p;
+  int grid;
+  cudaStream_t stream;
+};
+
+struct PrefillLaunch {
+  CUtensorMap tq, tk, tv, tsfk, tsfv;
+  PrefillParams p;
+  int grid;
+  cudaStream_t stream;
+};
+
+// Each returns cudaSuccess or the launch error; `variant` receives a static name.
+// Returns cudaErrorInvalidValue for a shape that has no instantiation.
+cudaError_t launch_decode_bf16(int dqk, int dvo, int hp, const DecodeLaunch& L, const char** variant);
+cudaError_t launch_decode_fp8(int dqk, int dvo, int hp, const DecodeLaunch& L, const char** variant);
+cudaError_t launch_decode_nvfp4(int dqk, int dvo, int hp, const DecodeLaunch& L, const char** variant);
+cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_merge(int dvo, const DecodeParams& p, cudaStream_t s);
+// Shared memory (bytes) the decode kernel of this shape needs.
+int decode_smem_bytes(int kvt, int dqk, int dvo, int hp);
+// Tokens per decode tile of this shape.
+int decode_tile_tokens(int kvt, int dqk);
+
+cudaError_t launch_prefill(int kvt, int dqk, int dvo, const PrefillLaunch& L, const char** variant);
+cudaError_t launch_prefill_plan(const PrefillParams& p, cudaStream_t s);
+int prefill_smem_bytes(int kvt, int dqk, int dvo);
+
+}  // namespace pa
