@@ -383,6 +383,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--all", action="store_true", help="also time every other workload")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
+    ap.add_argument("--workload", default=MAIN, help="decode workload of the main line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -410,7 +413,8 @@ def main():
         barrier()
     torch.cuda.set_device(local)
     pk = peaks()
-    main_res = bench_decode(MAIN, args.steps, args.warmup, barrier, local, pk, with_cpu=(rank == 0))
+    main_res = bench_decode(args.workload, args.steps, args.warmup, barrier, local, pk,
+                            with_e2e=not args.no_e2e, with_cpu=(rank == 0 and not args.no_cpu))
     ms = main_res["ms_per_step"]
     if world > 1:
         import torch.distributed as dist
@@ -425,7 +429,7 @@ def main():
         "data": "synthetic (seeded Irwin-Hall(4) standard-normal draws; seeded random page order)",
         "config": {"workload": "bf16 GQA decode: batch 64, 24 q / 4 kv heads, head_dim 512, page_size 64, "
                                "kv_len uniform in [1024, 8192], shuffled pages, split-K",
-                   "name": MAIN, "l2": "inputs (2.4 GB of KV) larger than L2, no flush",
+                   "name": args.workload, "l2": "inputs (2.4 GB of KV) larger than L2, no flush",
                    "parallelism": f"{world} independent replica(s), no collective"},
         "e2e": main_res.get("e2e"), "roofline": main_res["roofline"], "cpu_baseline": main_res.get("cpu_baseline"),
         "clocks": main_res["clocks"], "gpu_launches": main_res["gpu_launches"], "variant": main_res["variant"],

@@ -368,8 +368,8 @@ def make_case(phase: str, *, batch: int, Hq: int, Hkv: int, d_qk: int, d_vo: int
 # --------------------------------------------------------------------------------------
 # the workloads the pages' Gemma-4 layer shapes give (seed = 1000 + workload number)
 # --------------------------------------------------------------------------------------
-def _cfg2_lens():
-    return [randint(1002, TID_LEN, b, 1024, 8192) for b in range(64)]
+def _cfg2_lens(batch=64):
+    return [randint(1002, TID_LEN, b, 1024, 8192) for b in range(batch)]
 
 
 WORKLOADS = {
@@ -378,6 +378,10 @@ WORKLOADS = {
         kv_lens=[37, 64], kv_dtype=KV_BF16, seed=1001),
     "gqa_decode_bf16": dict(
         phase="decode", batch=64, Hq=24, Hkv=4, d_qk=512, d_vo=512, page_size=64,
+        kv_lens=None, kv_dtype=KV_BF16, seed=1002),
+    # a quarter of the bf16 GQA decode workload (~0.6 GB of KV, above L2): profiling captures
+    "gqa_decode_bf16_quarter": dict(
+        phase="decode", batch=16, Hq=24, Hkv=4, d_qk=512, d_vo=512, page_size=64,
         kv_lens=None, kv_dtype=KV_BF16, seed=1002),
     "fp8_decode": dict(
         phase="decode", batch=128, Hq=12, Hkv=4, d_qk=512, d_vo=512, page_size=16,
@@ -398,10 +402,10 @@ WORKLOADS = {
 def workload(name: str, device="cpu", poison: bool = True) -> Case:
     w = dict(WORKLOADS[name])
     if w["kv_lens"] is None:
-        w["kv_lens"] = _cfg2_lens()
+        w["kv_lens"] = _cfg2_lens(w["batch"])
     return make_case(device=device, poison=poison, **w)
 
 
 def workload_kv_lens(name: str) -> List[int]:
     w = WORKLOADS[name]
-    return list(w["kv_lens"]) if w["kv_lens"] is not None else _cfg2_lens()
+    return list(w["kv_lens"]) if w["kv_lens"] is not None else _cfg2_lens(w["batch"])
