@@ -79,7 +79,8 @@ typedef enum {
   PA_ERR_ALIGNMENT = -3,   /* a pointer that is not 16-byte aligned */
   PA_ERR_SMEM = -4,        /* the kernel's shared memory exceeds the device opt-in limit */
   PA_ERR_CUDA = -5,        /* a CUDA runtime / driver call failed */
-  PA_ERR_DEVICE = -6       /* a kernel gave up on a bounded wait (see the error query) */
+  PA_ERR_DEVICE = -6,      /* a kernel gave up on a bounded wait (see the error query) */
+  PA_ERR_SCRATCH = -7      /* the problem needs more scratch than paged_attn_decode_noalloc holds */
 } pa_status;
 
 typedef enum { PA_KV_BF16 = 0, PA_KV_FP8_E4M3 = 1, PA_KV_NVFP4 = 2 } pa_kv_dtype;
@@ -161,6 +162,43 @@ int paged_attn_set_decode_chunk_pages(int pages);
  * (for tests that must know which path ran).  Returns PA_OK; the text is truncated to
  * len-1 characters. */
 int paged_attn_last_variant(char* buf, int len);
+
+/*
+ * paged_attn_decode_noalloc -- paged_attn_decode for callers that cannot allocate device
+ * memory.  (No counterpart in the pages: it is a deployment variant of the decode call.)
+ *
+ * Who needs it: code that runs inside a host framework that owns every byte of device
+ * memory (an inference-engine plugin handed a fixed pool, a service with a hard memory
+ * budget), and code that must not trigger cudaMalloc's implicit device-wide
+ * synchronisation in the middle of a step.  paged_attn_decode may grow its workspace
+ * with cudaMalloc; this entry point never does.  It calls no cudaMalloc, cudaFree or
+ * other allocating routine.
+ *
+ * Its scratch (work list, split-K partials, error word) is one statically sized device
+ * array of PA_NOALLOC_SCRATCH_BYTES (32 MiB) inside the library; every GPU that loads the
+ * library holds that array until the process exits.  The caller still passes every input
+ * and output.  A problem whose scratch does not fit returns PA_ERR_SCRATCH before
+ * anything is launched; the scratch needed grows with batch * num_qo_heads *
+ * head_dim_vo (the split-K partials), and the call first uses fewer KV splits when that
+ * keeps it inside the array.
+ *
+ * The first call on a device resolves the array's device address (with that device
+ * current) and caches it; make that first call before any stream capture.  Every call
+ * shares the one array and it keeps the last call's contents (the call clears the
+ * part that must start at zero), so calls that overlap on the GPU -- on different
+ * streams, or from different threads -- race; serialise them.  A bounded wait that
+ * gives up is recorded in the array's first word and is not reported by
+ * paged_attn_check_device_error.
+ *
+ * Arguments, layouts and the supported set are those of paged_attn_decode.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int paged_attn_decode_noalloc(const void* q, const void* kv_cache, const int32_t* kv_indptr,
+                              const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                              int batch, int num_pages, int num_qo_heads, int num_kv_heads,
+                              int head_dim_qk, int head_dim_vo, int page_size, float sm_scale,
+                              int window_left, int kv_dtype, const pa_kv_scales* kv_scales,
+                              void* out, float* lse, void* stream);
 
 /* Measurement hook.  After paged_attn_profile_begin(n), the next n calls record a pair of
  * CUDA events on their stream around their main attention kernel (decode_kernel or

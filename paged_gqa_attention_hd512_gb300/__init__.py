@@ -23,13 +23,14 @@ LIB_PATH = os.path.join(HERE, "_build", "libpaged_attn.so")
 
 PA_KV_BF16, PA_KV_FP8_E4M3, PA_KV_NVFP4 = 0, 1, 2
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_ALIGNMENT = 0, -1, -2, -3
-PA_ERR_SMEM, PA_ERR_CUDA, PA_ERR_DEVICE = -4, -5, -6
+PA_ERR_SMEM, PA_ERR_CUDA, PA_ERR_DEVICE, PA_ERR_SCRATCH = -4, -5, -6, -7
+PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # every symbol include/paged_attn.h declares
 EXPORTED = ("paged_attn_decode", "paged_attn_prefill", "paged_attn_status_string",
             "paged_attn_release_workspace", "paged_attn_check_device_error",
             "paged_attn_set_decode_chunk_pages", "paged_attn_last_variant",
-            "paged_attn_profile_begin", "paged_attn_profile_end")
+            "paged_attn_profile_begin", "paged_attn_profile_end", "paged_attn_decode_noalloc")
 
 _lib = None
 
@@ -57,6 +58,8 @@ def load(path: Optional[str] = None):
     lib.paged_attn_decode.restype = i32
     lib.paged_attn_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32,
                                       i32, ctypes.POINTER(_Scales), vp, vp, vp]
+    lib.paged_attn_decode_noalloc.restype = i32
+    lib.paged_attn_decode_noalloc.argtypes = list(lib.paged_attn_decode.argtypes)
     lib.paged_attn_prefill.restype = i32
     lib.paged_attn_prefill.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                        f32, i32, i32, i32, ctypes.POINTER(_Scales), vp, vp, vp]
@@ -138,6 +141,29 @@ def paged_attn_decode(q: torch.Tensor, kv_cache: torch.Tensor, kv_indptr: torch.
                                   ctypes.byref(sc), _ptr(out), _ptr(lse), _stream(stream))
     if st != PA_OK:
         raise PagedAttnError(st, "paged_attn_decode")
+    return out, lse
+
+
+def paged_attn_decode_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, kv_indptr: torch.Tensor,
+                              kv_indices: torch.Tensor, kv_last_page_len: torch.Tensor, *, out: torch.Tensor,
+                              lse: Optional[torch.Tensor], num_kv_heads: int, head_dim_vo: int, page_size: int,
+                              sm_scale: float, window_left: int = -1, kv_dtype: int = PA_KV_BF16,
+                              k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                              sf: Optional[torch.Tensor] = None, num_pages: Optional[int] = None,
+                              stream=None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Decode for callers that cannot allocate device memory: the library uses only its
+    fixed scratch array, and the caller passes ``out`` (and ``lse``) already allocated.
+    Overlapping calls race on that array; serialise them."""
+    batch, hq, dqk = q.shape
+    if num_pages is None:
+        num_pages = _num_pages(kv_cache, num_kv_heads, dqk, head_dim_vo, page_size, kv_dtype)
+    sc = _scales(kv_dtype, k_scale, v_scale, sf)
+    st = load().paged_attn_decode_noalloc(_ptr(q), _ptr(kv_cache), _ptr(kv_indptr), _ptr(kv_indices),
+                                          _ptr(kv_last_page_len), batch, num_pages, hq, num_kv_heads, dqk,
+                                          head_dim_vo, page_size, float(sm_scale), window_left, kv_dtype,
+                                          ctypes.byref(sc), _ptr(out), _ptr(lse), _stream(stream))
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_decode_noalloc")
     return out, lse
 
 

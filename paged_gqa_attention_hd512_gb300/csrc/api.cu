@@ -199,6 +199,7 @@ const char* paged_attn_status_string(int status) {
     case PA_ERR_SMEM: return "kernel shared memory exceeds the device opt-in limit";
     case PA_ERR_CUDA: return "CUDA runtime or driver call failed";
     case PA_ERR_DEVICE: return "a kernel gave up on a bounded wait";
+    case PA_ERR_SCRATCH: return "problem needs more scratch than paged_attn_decode_noalloc's fixed array holds";
     default: return "unknown status";
   }
 }
@@ -373,3 +374,141 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------------
+// paged_attn_decode_noalloc: the decode call for callers that cannot allocate device
+// memory (an engine plugin handed a fixed pool, a memory-budgeted service, code that must
+// not trigger cudaMalloc's implicit device synchronisation mid-step).  Its scratch is the
+// statically sized device array below instead of the grow-only workspace; it calls no
+// cudaMalloc, cudaFree or other allocating routine.
+//
+// In host code `g_pa_noalloc_scratch` names only a host-side stand-in of the device
+// array: handing it to a kernel would fault or, where the GPU can reach host memory,
+// silently use the wrong memory.  Its device address comes from cudaGetSymbolAddress,
+// resolved once per device (with that device current) by the first call on that device,
+// which should therefore come before any stream capture.
+static __device__ __align__(256) uint8_t g_pa_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+namespace pa {
+namespace {
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mutex;
+
+void* noalloc_scratch(int* status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *status = PA_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_pa_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      *status = PA_ERR_CUDA;
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+}  // namespace
+}  // namespace pa
+
+extern "C" int paged_attn_decode_noalloc(const void* q, const void* kv_cache, const int32_t* kv_indptr,
+                                         const int32_t* kv_indices, const int32_t* kv_last_page_len, int batch,
+                                         int num_pages, int num_qo_heads, int num_kv_heads, int head_dim_qk,
+                                         int head_dim_vo, int page_size, float sm_scale, int window_left,
+                                         int kv_dtype, const pa_kv_scales* kv_scales, void* out, float* lse,
+                                         void* stream) {
+  int st = check_common(q, kv_cache, kv_indptr, kv_indices, kv_last_page_len, batch, num_pages, num_qo_heads,
+                        num_kv_heads, head_dim_qk, head_dim_vo, page_size, sm_scale, window_left, kv_dtype,
+                        kv_scales, out, lse);
+  if (st != PA_OK) return st;
+  if (batch == 0) return PA_OK;
+  const int group = num_qo_heads / num_kv_heads;
+  const int hp = group <= 8 ? 8 : 16;
+  int smem_optin = 0;
+  const int sms = device_sms(&smem_optin);
+  if (sms <= 0) return PA_ERR_CUDA;
+  if (decode_smem_bytes(kv_dtype, head_dim_qk, head_dim_vo, hp) > smem_optin) return PA_ERR_SMEM;
+
+  // Size the work list to the fixed array: fewer KV splits when the usual number does
+  // not fit, PA_ERR_SCRATCH when not even one split per sequence fits.
+  const size_t cap = PA_NOALLOC_SCRATCH_BYTES;
+  const size_t per_chunk =
+      sizeof(DecodeChunk) + (size_t)num_qo_heads * sizeof(float2) + (size_t)num_qo_heads * head_dim_vo * 4;
+  const size_t fixed = kFixedBytes + 256 + align_up((size_t)batch * sizeof(int2), 256) + 4 * 256;
+  if (fixed >= cap) return PA_ERR_SCRATCH;
+  const long fit = (long)((cap - fixed) / per_chunk) - batch;
+  const int forced = g_forced_chunk_pages;
+  const int grid = sms;
+  const long usual = forced > 0 ? 2048 : (16 * grid + num_kv_heads - 1) / num_kv_heads;
+  const long target = fit < usual ? fit : usual;
+  if (target < 1) return PA_ERR_SCRATCH;
+  const int max_chunks = (int)target + batch;
+  size_t off = kFixedBytes;
+  const size_t o_hdr = off; off = align_up(off + 64, 256);
+  const size_t o_chunks = off; off = align_up(off + (size_t)max_chunks * sizeof(DecodeChunk), 256);
+  const size_t o_seq = off; off = align_up(off + (size_t)batch * sizeof(int2), 256);
+  const size_t o_ml = off; off = align_up(off + (size_t)max_chunks * num_qo_heads * sizeof(float2), 256);
+  const size_t o_o = off; off = align_up(off + (size_t)max_chunks * num_qo_heads * head_dim_vo * sizeof(float), 256);
+  if (off > cap) return PA_ERR_SCRATCH;
+  char* ws = static_cast<char*>(noalloc_scratch(&st));
+  if (!ws) return st;
+
+  DecodeLaunch L;
+  std::memset(&L, 0, sizeof L);
+  const int T = decode_tile_tokens(kv_dtype, head_dim_qk);
+  const int box_rows = page_size < T ? page_size : T;
+  const bool swz = page_size >= 8;
+  if (!make_kv_maps(&L.tk, &L.tv, &L.tsfk, &L.tsfv, kv_cache, kv_scales ? kv_scales->sf : nullptr, num_pages,
+                    num_kv_heads, head_dim_qk, head_dim_vo, page_size, kv_dtype, box_rows, swz))
+    return PA_ERR_CUDA;
+  L.grid = grid;
+  L.stream = static_cast<cudaStream_t>(stream);
+  // the error word is the only scratch that must start at zero (the planner rewrites
+  // the work list and every partial is written before it is read)
+  if (cudaMemsetAsync(ws + kErrOffset, 0, sizeof(int), L.stream) != cudaSuccess) return PA_ERR_CUDA;
+
+  DecodeParams& p = L.p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.kv_indptr = kv_indptr;
+  p.kv_indices = kv_indices;
+  p.kv_last_page_len = kv_last_page_len;
+  p.k_scale = kv_dtype != PA_KV_BF16 ? kv_scales->k_scale : nullptr;
+  p.v_scale = kv_dtype != PA_KV_BF16 ? kv_scales->v_scale : nullptr;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.err = reinterpret_cast<int*>(ws + kErrOffset);
+  p.hdr = reinterpret_cast<int*>(ws + o_hdr);
+  p.chunks = reinterpret_cast<DecodeChunk*>(ws + o_chunks);
+  p.seq_info = reinterpret_cast<int2*>(ws + o_seq);
+  p.ws_ml = reinterpret_cast<float2*>(ws + o_ml);
+  p.ws_o = reinterpret_cast<float*>(ws + o_o);
+  p.batch = batch;
+  p.Hq = num_qo_heads;
+  p.Hkv = num_kv_heads;
+  p.group = group;
+  p.page_size = page_size;
+  p.window_left = window_left;
+  p.max_chunks = max_chunks;
+  p.target_chunks = (int)target;
+  p.forced_chunk_pages = forced;
+  p.box_rows = box_rows;
+  p.swz = swz ? 7 : 0;
+  p.sm_scale = sm_scale;
+
+  if (launch_decode_plan(p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  const char* name = "?";
+  cudaError_t e;
+  if (kv_dtype == PA_KV_BF16) e = launch_decode_bf16(head_dim_qk, head_dim_vo, hp, L, &name);
+  else if (kv_dtype == PA_KV_FP8_E4M3) e = launch_decode_fp8(head_dim_qk, head_dim_vo, hp, L, &name);
+  else e = launch_decode_nvfp4(head_dim_qk, head_dim_vo, hp, L, &name);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_decode_merge(head_dim_vo, p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};
+  std::snprintf(g_variant, sizeof g_variant, "%s_%s_noalloc", name, kv_names[kv_dtype]);
+  return PA_OK;
+}
