@@ -368,9 +368,86 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
                         kv_scales, out, lse);
   if (st != PA_OK) return st;
   if (!qo_indptr || total_q < 0) return PA_ERR_INVALID_ARG;
-  (void)causal;
-  (void)stream;
-  return PA_ERR_UNSUPPORTED;
+  if (!aligned(qo_indptr, 4)) return PA_ERR_ALIGNMENT;
+  if (batch == 0 || total_q == 0) return PA_OK;
+  // K/V tiles are 128B-swizzled TMA boxes of page_size rows: they need whole 8-row atoms
+  if (page_size < 8) return PA_ERR_UNSUPPORTED;
+  if (kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
+  const int group = num_qo_heads / num_kv_heads;
+  const int rows_per_tile = 128 / group;
+  int smem_optin = 0;
+  const int sms = device_sms(&smem_optin);
+  if (sms <= 0) return PA_ERR_CUDA;
+  if (prefill_smem_bytes(kv_dtype, head_dim_qk, head_dim_vo) > smem_optin) return PA_ERR_SMEM;
+
+  const long max_items = ((long)total_q / rows_per_tile + batch) * num_kv_heads;
+  if (max_items > (1l << 30)) return PA_ERR_INVALID_ARG;
+  size_t off = kFixedBytes;
+  const size_t o_hdr = off; off = align_up(off + 64, 256);
+  const size_t o_items = off; off = align_up(off + (size_t)max_items * sizeof(PrefillItem), 256);
+  char* ws = static_cast<char*>(workspace(off, &st));
+  if (!ws) return st;
+
+  PrefillLaunch L;
+  std::memset(&L, 0, sizeof L);
+  CUtensorMap dummy_sf[2];
+  if (!make_kv_maps(&L.tk, &L.tv, &dummy_sf[0], &dummy_sf[1], kv_cache, nullptr, num_pages, num_kv_heads,
+                    head_dim_qk, head_dim_vo, page_size, kv_dtype, page_size, true))
+    return PA_ERR_CUDA;
+  // Q as [total_q][Hq][d_qk] bf16 bytes: boxes of [rows_per_tile][group][128 B]
+  {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return PA_ERR_CUDA;
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim_qk * 2, (cuuint64_t)num_qo_heads, (cuuint64_t)total_q};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim_qk * 2, (cuuint64_t)num_qo_heads * head_dim_qk * 2};
+    cuuint32_t box[3] = {128, (cuuint32_t)group, (cuuint32_t)rows_per_tile};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (fn(&L.tq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(q), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PA_ERR_CUDA;
+  }
+  PrefillParams& p = L.p;
+  p.q = static_cast<const uint16_t*>(q);
+  p.qo_indptr = qo_indptr;
+  p.kv_indptr = kv_indptr;
+  p.kv_indices = kv_indices;
+  p.kv_last_page_len = kv_last_page_len;
+  p.k_scale = kv_dtype != PA_KV_BF16 ? kv_scales->k_scale : nullptr;
+  p.v_scale = kv_dtype != PA_KV_BF16 ? kv_scales->v_scale : nullptr;
+  p.kv_cache = static_cast<const uint8_t*>(kv_cache);
+  p.sf = kv_scales ? kv_scales->sf : nullptr;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.err = reinterpret_cast<int*>(ws + kErrOffset);
+  p.hdr = reinterpret_cast<int*>(ws + o_hdr);
+  p.items = reinterpret_cast<PrefillItem*>(ws + o_items);
+  p.batch = batch;
+  p.total_q = total_q;
+  p.Hq = num_qo_heads;
+  p.Hkv = num_kv_heads;
+  p.group = group;
+  p.page_size = page_size;
+  p.window_left = window_left;
+  p.causal = causal ? 1 : 0;
+  p.num_pages = num_pages;
+  p.rows_per_tile = rows_per_tile;
+  p.max_items = (int)max_items;
+  p.box_rows = page_size;
+  p.swz = 7;
+  p.sm_scale = sm_scale;
+  L.grid = sms;
+  L.stream = static_cast<cudaStream_t>(stream);
+
+  if (launch_prefill_plan(p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  const char* name = "?";
+  prof_mark(L.stream, true);
+  cudaError_t e = launch_prefill(kv_dtype, head_dim_qk, head_dim_vo, L, &name);
+  prof_mark(L.stream, false);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};
+  std::snprintf(g_variant, sizeof g_variant, "%s_%s", name, kv_names[kv_dtype]);
+  return PA_OK;
 }
 
 }  // extern "C"

@@ -445,6 +445,7 @@ __global__ void __launch_bounds__(288, 1)
       const uint8_t* sfk = kp + C::K_TILE + C::V_TILE;
       const uint8_t* sfv = sfk + C::SFK_TILE;
       mbar_wait(&full[s], (g / NS) & 1, p.err, SITE_DEC_FULL);
+      __syncwarp();  // ldmatrix / mma.sync below are warp-collective
       if (n_valid < T) {
         // rows past the end of the chunk hold stale or unused-slot bytes: zero the V rows
         // (and their scales) so that P = 0 never meets a NaN

@@ -1,0 +1,47 @@
+// prefill.cu -- instantiates the tcgen05 prefill kernel and its planner.
+#define PA_PREFILL_PLAN 1
+#include "launch.h"
+#include "prefill_impl.cuh"
+
+namespace pa {
+
+template <int DQK, int DVO>
+static cudaError_t run_prefill(const PrefillLaunch& L) {
+  using C = PrefillCfg<DQK, DVO>;
+  auto kern = prefill_kernel<DQK, DVO>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC);
+  if (e != cudaSuccess) return e;
+  kern<<<L.grid, 256, C::ALLOC, L.stream>>>(L.tq, L.tk, L.tv, L.p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(int kvt, int dqk, int dvo, const PrefillLaunch& L, const char** variant) {
+  if (kvt != KV_BF16) return cudaErrorInvalidValue;
+  if (dqk == 512 && dvo == 512) {
+    *variant = "prefill_512x512";
+    return run_prefill<512, 512>(L);
+  }
+  if (dqk == 512 && dvo == 256) {
+    *variant = "prefill_512x256";
+    return run_prefill<512, 256>(L);
+  }
+  if (dqk == 256 && dvo == 256) {
+    *variant = "prefill_256x256";
+    return run_prefill<256, 256>(L);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prefill_plan(const PrefillParams& p, cudaStream_t s) {
+  prefill_plan_kernel<<<1, 1024, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+int prefill_smem_bytes(int kvt, int dqk, int dvo) {
+  (void)kvt;
+  if (dqk == 512 && dvo == 512) return PrefillCfg<512, 512>::ALLOC;
+  if (dqk == 512 && dvo == 256) return PrefillCfg<512, 256>::ALLOC;
+  return PrefillCfg<256, 256>::ALLOC;
+}
+
+}  // namespace pa

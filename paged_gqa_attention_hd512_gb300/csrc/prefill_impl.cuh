@@ -1,0 +1,450 @@
+// prefill_impl.cuh -- causal paged prefill at head_dim 512 with tcgen05 MMAs (sm_103a).
+//
+// Attention of the new tokens of each sequence over its paged KV ("Run Gemma4 head_dim 512
+// attention on Triton", Approach: prefill over the HND paged layout, causal when no custom
+// mask is given; "feat(attention): asymmetric VO-split NVFP4 paged prefill (qk=512/vo=256)
+// for Gemma-4 on SM120/121", Summary: head_dim_qk 512 with head_dim_vo 256, VO split).
+//
+// One CTA per SM (persistent).  A work item is 128 query rows = P positions x g heads of
+// one kv head (P = 128 / g), so every K/V tile loaded into shared memory serves all g
+// query heads that read it.  Warp roles:
+//   warp 0     producer: TMA loads of the Q tile (once per item) and of K/V chunks
+//              ([128 keys][64 head-dim] bf16, 128B-swizzled) into a ring of 16 KB slots;
+//              zeroes V rows past the end of the sequence before releasing them
+//   warp 1     MMA issuer (one thread): S = Q K^T into TMEM (M 128, N 128, K 16 steps),
+//              O += P V with P read from TMEM (M 128, N 64 per V chunk)
+//   warps 4-7  softmax + epilogue: thread r owns row r (TMEM lane r): masks, online
+//              softmax in base 2 with lazy rescaling, writes P (bf16) into TMEM, and at the
+//              end normalises O and stores bf16 rows and lse
+// TMEM (512 columns): S [0, 128), P [128, 192), O [256, 512).  A 128 x 512 fp32 O tile
+// would fill all of TMEM, so head_dim_vo 512 is computed in two passes of 256 columns over
+// the same KV range (S is recomputed; the softmax statistics of both passes are identical).
+#pragma once
+
+#include "common.cuh"
+#include "tc_helpers.cuh"
+
+namespace pa {
+
+template <int DQK, int DVO>
+struct PrefillCfg {
+  static constexpr int M = 128;                 // query rows per tile
+  static constexpr int N = 128;                 // keys per KV tile
+  static constexpr int CHUNK = N * 128;         // bytes of one [128 keys][64 dims] bf16 chunk
+  static constexpr int NQC = DQK / 64;          // Q / K chunks (64 head-dim columns each)
+  static constexpr int DVP = DVO > 256 ? 256 : DVO;  // output columns per pass
+  static constexpr int NPASS = DVO / DVP;
+  static constexpr int NVC = DVP / 64;          // V chunks per pass
+  static constexpr int Q_BYTES = NQC * M * 128;
+  static constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
+  static constexpr int NSLOT_RAW = (SMEM_BUDGET - Q_BYTES) / CHUNK;
+  static constexpr int NSLOT = NSLOT_RAW > 8 ? 8 : NSLOT_RAW;
+  static constexpr int OFF_RING = Q_BYTES;
+  static constexpr int OFF_BAR = Q_BYTES + NSLOT * CHUNK;
+  // barriers: q_full, q_empty, s_full, s_free, p_full, o_done, o_free, aux, kv_full[], kv_empty[]
+  static constexpr int NBAR = 8 + 2 * NSLOT;
+  static constexpr int BYTES = OFF_BAR + NBAR * 8 + 16;
+  static constexpr int ALLOC = BYTES + 1024;
+  static constexpr uint32_t TM_S = 0, TM_P = 128, TM_O = 256;
+  static_assert(NSLOT >= 3, "KV ring too shallow");
+};
+
+// ----------------------------------------------------------------------------- plan
+// Items (sequence, first new-token index, kv head) in descending order of the KV tiles
+// they visit, so that a static round-robin over persistent CTAs balances.
+constexpr int kPlanBuckets = 2048;
+
+__device__ __forceinline__ int prefill_tile_cost(const PrefillParams& p, int kv_len, int qo_len, int q_begin) {
+  const int n_pos = min(p.rows_per_tile, qo_len - q_begin);
+  const int pos0 = kv_len - qo_len + q_begin;
+  const int hi = p.causal ? min(kv_len - 1, pos0 + n_pos - 1) : kv_len - 1;
+  const int lo = p.window_left >= 0 ? max(0, pos0 - p.window_left) : 0;
+  if (hi < lo || hi < 0) return 0;
+  return hi / 128 - lo / 128 + 1;
+}
+
+#ifdef PA_PREFILL_PLAN
+__global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p) {
+  __shared__ int hist[kPlanBuckets];
+  __shared__ int s_total;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kPlanBuckets; i += blockDim.x) hist[i] = 0;
+  if (tid == 0) s_total = 0;
+  __syncthreads();
+  const int P = p.rows_per_tile, ps = p.page_size;
+  // histogram of tile costs
+  for (int b = tid; b < p.batch; b += blockDim.x) {
+    const int qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
+    const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
+    const int kv_len = np > 0 ? (np - 1) * ps + p.kv_last_page_len[b] : 0;
+    int cnt = 0;
+    for (int q0 = 0; q0 < qo_len; q0 += P) {
+      const int c = min(kPlanBuckets - 1, prefill_tile_cost(p, kv_len, qo_len, q0));
+      atomicAdd(&hist[c], 1);
+      ++cnt;
+    }
+    atomicAdd(&s_total, cnt);
+  }
+  __syncthreads();
+  // exclusive prefix in descending cost order (bucket kPlanBuckets-1 first), serial: small
+  if (tid == 0) {
+    int run = 0;
+    for (int c = kPlanBuckets - 1; c >= 0; --c) {
+      const int n = hist[c];
+      hist[c] = run;
+      run += n;
+    }
+  }
+  __syncthreads();
+  for (int b = tid; b < p.batch; b += blockDim.x) {
+    const int qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
+    const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
+    const int kv_len = np > 0 ? (np - 1) * ps + p.kv_last_page_len[b] : 0;
+    for (int q0 = 0; q0 < qo_len; q0 += P) {
+      const int cost = prefill_tile_cost(p, kv_len, qo_len, q0);
+      const int slot = atomicAdd(&hist[min(kPlanBuckets - 1, cost)], 1);
+      for (int k = 0; k < p.Hkv; ++k) {
+        if (slot * p.Hkv + k >= p.max_items) break;  // cannot happen within the host bound
+        PrefillItem it;
+        it.b = b;
+        it.q_begin = q0;
+        it.kvh = k;
+        it.cost = cost;
+        p.items[slot * p.Hkv + k] = it;
+      }
+    }
+  }
+  if (tid == 0) p.hdr[0] = min(s_total * p.Hkv, p.max_items);
+}
+#endif  // PA_PREFILL_PLAN
+
+// Everything one role needs to know about a work item.
+struct PrefillItemInfo {
+  int b, kvh, q_begin, n_pos, qo_len, kv_len, q_row0, pos0, jlo, nt, ip0, np;
+};
+
+__device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams& p, int it) {
+  const PrefillItem item = p.items[it];
+  PrefillItemInfo f;
+  f.b = item.b;
+  f.kvh = item.kvh;
+  f.q_begin = item.q_begin;
+  f.qo_len = p.qo_indptr[f.b + 1] - p.qo_indptr[f.b];
+  f.ip0 = p.kv_indptr[f.b];
+  f.np = p.kv_indptr[f.b + 1] - f.ip0;
+  f.kv_len = f.np > 0 ? (f.np - 1) * p.page_size + p.kv_last_page_len[f.b] : 0;
+  f.n_pos = min(p.rows_per_tile, f.qo_len - f.q_begin);
+  f.q_row0 = p.qo_indptr[f.b] + f.q_begin;
+  f.pos0 = f.kv_len - f.qo_len + f.q_begin;
+  int hi = p.causal ? min(f.kv_len - 1, f.pos0 + f.n_pos - 1) : f.kv_len - 1;
+  int lo = p.window_left >= 0 ? max(0, f.pos0 - p.window_left) : 0;
+  hi = max(hi, 0);  // at least one tile: rows without a visible key come out as 0 / -inf
+  lo = min(lo, hi);
+  f.jlo = lo / 128;
+  f.nt = hi / 128 - f.jlo + 1;
+  return f;
+}
+
+// r-th item of this CTA: rounds of gridDim.x items, alternating direction, over a list
+// sorted by descending cost.
+__device__ __forceinline__ int prefill_item_at(int r) {
+  const int off = (r & 1) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
+  return r * (int)gridDim.x + off;
+}
+
+template <int DQK, int DVO>
+__global__ void __launch_bounds__(256, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
+  using C = PrefillCfg<DQK, DVO>;
+  constexpr int NSLOT = C::NSLOT;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t q_s = smem_u32(smem);
+  const uint32_t ring = q_s + C::OFF_RING;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* s_full = bars + 2;
+  uint64_t* s_free = bars + 3;
+  uint64_t* p_full = bars + 4;
+  uint64_t* o_done = bars + 5;
+  uint64_t* o_free = bars + 6;
+  uint64_t* aux = bars + 7;
+  uint64_t* kv_full = bars + 8;
+  uint64_t* kv_empty = bars + 8 + NSLOT;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(s_full, 1);
+    mbar_init(s_free, 4);
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    mbar_init(o_free, 4);
+    mbar_init(aux, 1);
+    for (int s = 0; s < NSLOT; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  const int n_items = min(p.hdr[0], p.max_items);
+  const int ps = p.page_size, g = p.group;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (whole warp)
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+    }
+    uint32_t rc = 0, aux_phase = 0;
+    int it_local = 0;
+    for (int r = 0;; ++r, ++it_local) {
+      const int it = prefill_item_at(r);
+      if (it >= n_items) break;
+      const PrefillItemInfo f = prefill_item_info(p, it);
+      mbar_wait(q_empty, (it_local & 1) ^ 1, p.err, SITE_PRE_Q);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQC * 128 * g * p.rows_per_tile));
+        for (int c = 0; c < C::NQC; ++c)
+          tma_load_3d(q_s + c * (C::M * 128), &tm_q, c * 128, f.kvh * g, f.q_row0, q_full);
+      }
+      const int steps = C::NPASS * f.nt;
+      const int page_tok_cap = f.np * ps;
+      // chunks in the MMA thread's order: K of step 0, then (K of step k+1, V of step k)
+      for (int k = -1; k < steps; ++k) {
+        for (int part = 0; part < 2; ++part) {
+          const bool is_k = (part == 0);
+          const int st = is_k ? k + 1 : k;
+          if (st < 0 || st >= steps) continue;
+          const int pass = st / f.nt, jt = st % f.nt;
+          const int key0 = (f.jlo + jt) * 128;
+          const int valid = max(0, min(128, f.kv_len - key0));
+          const int load_rows = max(0, min(128, page_tok_cap - key0));
+          const int pieces = load_rows / ps;
+          const int my_page = (lane < pieces) ? p.kv_indices[f.ip0 + key0 / ps + lane] : 0;
+          const int nch = is_k ? C::NQC : C::NVC;
+          for (int c = 0; c < nch; ++c, ++rc) {
+            const int slot = rc % NSLOT;
+            mbar_wait(&kv_empty[slot], ((rc / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
+            const uint32_t dst = ring + slot * C::CHUNK;
+            const uint32_t bytes = (uint32_t)(pieces * ps * 128);
+            const bool fix = !is_k && valid < 128;  // V rows past the sequence must be zeroed
+            uint64_t* bar = fix ? aux : &kv_full[slot];
+            if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+            const int col = is_k ? c * 128 : (pass * C::DVP + c * 64) * 2;
+            for (int pc = 0; pc < pieces; ++pc) {
+              const int page = __shfl_sync(0xffffffffu, my_page, pc);
+              if (lane == 0)
+                tma_load_3d(dst + pc * ps * 128, is_k ? &tm_k : &tm_v, col, f.kvh * ps, page, bar);
+            }
+            if (fix) {
+              mbar_wait(aux, aux_phase, p.err, SITE_PRE_DEQ);
+              aux_phase ^= 1;
+              uint8_t* sp = smem + C::OFF_RING + slot * C::CHUNK;
+              for (int i = lane; i < (128 - valid) * 8; i += 32)
+                *reinterpret_cast<uint4*>(sp + (valid + (i >> 3)) * 128 + (i & 7) * 16) = make_uint4(0, 0, 0, 0);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&kv_full[slot]);
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (one thread)
+    if (lane == 0) {
+      constexpr uint32_t ID_QK = idesc_f16<true>(128, 128, false);
+      constexpr uint32_t ID_PV = idesc_f16<true>(128, 64, true);
+      // completions seen so far of s_free (one per QK after the first), p_full (one per PV)
+      // and o_free (one per finished pass)
+      uint32_t rc = 0, n_qk = 0, n_pv = 0, n_pass = 0;
+      int it_local = 0;
+      auto issue_qk = [&]() {
+        if (n_qk > 0) mbar_wait(s_free, (n_qk - 1) & 1, p.err, SITE_PRE_S_FREE);
+        for (int c = 0; c < C::NQC; ++c, ++rc) {
+          const int slot = rc % NSLOT;
+          mbar_wait(&kv_full[slot], (rc / NSLOT) & 1, p.err, SITE_PRE_KV_FULL);
+          tc_fence_after();
+          const uint32_t a = q_s + c * (C::M * 128), bsm = ring + slot * C::CHUNK;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_ss(tbase + C::TM_S, desc_kmajor_sw128(a + kk * 32), desc_kmajor_sw128(bsm + kk * 32), ID_QK,
+                      (c | kk) != 0);
+          tc_commit(&kv_empty[slot]);
+        }
+        tc_commit(s_full);
+        ++n_qk;
+      };
+      auto issue_pv = [&](bool first_of_pass) {
+        mbar_wait(p_full, n_pv & 1, p.err, SITE_PRE_P_FULL);
+        if (first_of_pass && n_pass > 0) mbar_wait(o_free, (n_pass - 1) & 1, p.err, SITE_PRE_O_DONE);
+        tc_fence_after();
+        for (int c = 0; c < C::NVC; ++c, ++rc) {
+          const int slot = rc % NSLOT;
+          mbar_wait(&kv_full[slot], (rc / NSLOT) & 1, p.err, SITE_PRE_KV_FULL);
+          tc_fence_after();
+          const uint32_t bsm = ring + slot * C::CHUNK;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            tc_mma_ts(tbase + C::TM_O + c * 64, tbase + C::TM_P + kk * 8, desc_mnmajor_sw128(bsm + kk * 2048, C::CHUNK),
+                      ID_PV, (!first_of_pass) || kk > 0);
+          tc_commit(&kv_empty[slot]);
+        }
+        tc_commit(o_done);
+        ++n_pv;
+        if (first_of_pass) ++n_pass;
+      };
+      for (int r = 0;; ++r, ++it_local) {
+        const int it = prefill_item_at(r);
+        if (it >= n_items) break;
+        const PrefillItemInfo f = prefill_item_info(p, it);
+        const int steps = C::NPASS * f.nt;
+        mbar_wait(q_full, it_local & 1, p.err, SITE_PRE_Q);
+        // S of step k+1 is computed while the softmax of step k runs; PV of step k follows
+        issue_qk();
+        if (steps == 1) tc_commit(q_empty);
+        for (int k = 0; k < steps; ++k) {
+          if (k + 1 < steps) {
+            issue_qk();
+            if (k + 1 == steps - 1) tc_commit(q_empty);
+          }
+          issue_pv(k % f.nt == 0);
+        }
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int row = threadIdx.x - 128;  // TMEM lane == tile row
+    const uint32_t lane_base = tbase + ((uint32_t)(32 * (warp - 4)) << 16);
+    const float scale_log2 = p.sm_scale * 1.4426950408889634f;
+    uint32_t gstep = 0;
+    for (int r = 0;; ++r) {
+      const int it = prefill_item_at(r);
+      if (it >= n_items) break;
+      const PrefillItemInfo f = prefill_item_info(p, it);
+      const int p_local = row / g, h_local = row % g;
+      const bool row_ok = (row < g * p.rows_per_tile) && (p_local < f.n_pos);
+      const int pos = f.pos0 + p_local;
+      const int khi = p.causal ? pos : f.kv_len - 1;
+      const int klo = p.window_left >= 0 ? pos - p.window_left : 0;
+      const int hq = f.kvh * g + h_local;
+      for (int pass = 0; pass < C::NPASS; ++pass) {
+        float m_used = -INFINITY, l = 0.f;
+        for (int jt = 0; jt < f.nt; ++jt, ++gstep) {
+          mbar_wait(s_full, gstep & 1, p.err, SITE_PRE_S_FULL);
+          __syncwarp();  // the tcgen05 loads below are warp-collective
+          tc_fence_after();
+          uint32_t sr[128];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + C::TM_S + 32 * c, sr + 32 * c);
+          tc_wait_ld();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free);
+          const int key0 = (f.jlo + jt) * 128;
+          float mx = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < 128; ++i) {
+            const int key = key0 + i;
+            const bool ok = key >= klo && key <= khi && key < f.kv_len;
+            const float x = ok ? __uint_as_float(sr[i]) * scale_log2 : -INFINITY;
+            sr[i] = __float_as_uint(x);
+            mx = fmaxf(mx, x);
+          }
+          const float m_new = fmaxf(m_used, mx);
+          bool resc = false;
+          float alpha = 1.f;
+          if (jt == 0) {
+            m_used = m_new;
+          } else if (m_new > m_used + 8.f) {  // lazy rescale: only when the max grows by > 2^8
+            alpha = fast_exp2(m_used - m_new);
+            m_used = m_new;
+            resc = true;
+          }
+          const float base = (m_used == -INFINITY) ? 0.f : m_used;
+          float sum = 0.f;
+          uint32_t pk[64];
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            const float p0 = fast_exp2(__uint_as_float(sr[2 * i]) - base);
+            const float p1 = fast_exp2(__uint_as_float(sr[2 * i + 1]) - base);
+            sum += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          if (gstep > 0) mbar_wait(o_done, (gstep - 1) & 1, p.err, SITE_PRE_O_DONE);
+          __syncwarp();
+          tc_fence_after();
+          // tcgen05.ld / st are warp-collective (.sync.aligned): the whole warp rescales when
+          // any of its rows needs it, the other rows with a factor of 1
+          if (__any_sync(0xffffffffu, resc)) {
+            const float a = resc ? alpha : 1.f;
+#pragma unroll 1
+            for (int c = 0; c < C::DVP / 32; ++c) {
+              uint32_t ov[32];
+              tmem_ld32(lane_base + C::TM_O + 32 * c, ov);
+              tc_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
+              tmem_st32(lane_base + C::TM_O + 32 * c, ov);
+            }
+          }
+          if (resc) l *= alpha;
+          l += sum;
+          tmem_st32(lane_base + C::TM_P, pk);
+          tmem_st32(lane_base + C::TM_P + 32, pk + 32);
+          tc_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(p_full);
+        }
+        // ---- epilogue of this pass: O / l -> bf16
+        mbar_wait(o_done, (gstep - 1) & 1, p.err, SITE_PRE_O_DONE);
+        __syncwarp();
+        tc_fence_after();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint16_t* orow = p.out + ((size_t)(f.q_row0 + p_local) * p.Hq + hq) * DVO + pass * C::DVP;
+#pragma unroll 1
+        for (int c = 0; c < C::DVP / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(lane_base + C::TM_O + 32 * c, ov);
+          tc_wait_ld();
+          uint32_t pkd[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pkd[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free);
+        if (pass == C::NPASS - 1 && row_ok && p.lse)
+          p.lse[(size_t)(f.q_row0 + p_local) * p.Hq + hq] =
+              l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tbase, 512);
+  }
+}
+
+}  // namespace pa

@@ -1,0 +1,55 @@
+"""Prefill parity: the tcgen05 path through the C ABI against the fp64 oracle (needs a GPU).
+
+Cases span several 128-row query tiles and 128-key KV tiles, ragged sequence ends,
+partial last pages, a cached prefix (bottom-right causal alignment), non-causal and
+windowed attention, group sizes 1..16 (row packing P x g), the three head-dim shapes.
+"""
+
+import pytest
+
+import paged_gqa_attention_hd512_gb300 as pa
+import synth
+from parity import check_full, ensure_built
+
+pytestmark = pytest.mark.gpu
+
+BF16 = synth.KV_BF16
+
+CASES = [
+    # (dqk, dvo, Hq, Hkv, page_size, kv_lens, qo_lens, causal, window)
+    (512, 512, 8, 2, 16, [130, 70], [130, 70], 1, -1),
+    (512, 512, 24, 4, 64, [300, 129, 1], [300, 129, 1], 1, -1),
+    (512, 512, 8, 8, 16, [257], [257], 1, -1),
+    (512, 512, 16, 1, 32, [200, 33], [200, 33], 1, -1),
+    (512, 512, 12, 4, 8, [150, 40], [150, 40], 1, -1),
+    (512, 512, 24, 4, 16, [300, 100], [50, 100], 1, -1),
+    (512, 512, 24, 4, 16, [200, 77], [200, 77], 0, -1),
+    (512, 512, 24, 4, 16, [400, 90], [400, 90], 1, 63),
+    (512, 256, 16, 2, 32, [200, 64], [200, 64], 1, -1),
+    (512, 256, 8, 1, 16, [333], [333], 1, -1),
+    (256, 256, 32, 16, 16, [190, 17], [190, 17], 1, -1),
+    (256, 256, 4, 2, 64, [129, 128], [129, 128], 1, 100),
+]
+
+
+def _id(c):
+    return (f"{c[0]}x{c[1]}-{c[2]}q{c[3]}kv-ps{c[4]}-kv{'_'.join(map(str, c[5]))}"
+            f"-qo{'_'.join(map(str, c[6]))}-c{c[7]}-w{c[8]}")
+
+
+@pytest.mark.parametrize("c", CASES, ids=[_id(c) for c in CASES])
+def test_prefill_parity(c):
+    dqk, dvo, hq, hkv, ps, kv, qo, causal, win = c
+    case = synth.make_case("prefill", batch=len(kv), Hq=hq, Hkv=hkv, d_qk=dqk, d_vo=dvo, page_size=ps,
+                           kv_lens=kv, qo_lens=qo, causal=causal, window_left=win, seed=500 + len(kv))
+    check_full(case, _id(c))
+    assert pa.paged_attn_last_variant() == f"prefill_{dqk}x{dvo}_bf16"
+
+
+def test_prefill_small_pages_are_refused():
+    ensure_built()
+    case = synth.make_case("prefill", batch=1, Hq=8, Hkv=1, d_qk=512, d_vo=512, page_size=4,
+                           kv_lens=[20], qo_lens=[20], seed=9).to("cuda")
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.run_case(case)
+    assert e.value.status == pa.PA_ERR_UNSUPPORTED
