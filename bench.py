@@ -386,6 +386,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
     ap.add_argument("--workload", default=MAIN, help="decode workload of the main line")
+    ap.add_argument("--prefill-only", action="store_true", help="time only the prefill workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -413,6 +414,11 @@ def main():
         barrier()
     torch.cuda.set_device(local)
     pk = peaks()
+    if args.prefill_only:
+        res = bench_prefill(PREFILL, max(3, min(50, args.steps // 40)), args.warmup, local, pk)
+        if rank == 0:
+            print(json.dumps({"prefill": res}), flush=True)
+        return 0
     main_res = bench_decode(args.workload, args.steps, args.warmup, barrier, local, pk,
                             with_e2e=not args.no_e2e, with_cpu=(rank == 0 and not args.no_cpu))
     ms = main_res["ms_per_step"]

@@ -385,6 +385,7 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   size_t off = kFixedBytes;
   const size_t o_hdr = off; off = align_up(off + 64, 256);
   const size_t o_items = off; off = align_up(off + (size_t)max_items * sizeof(PrefillItem), 256);
+  const size_t o_toff = off; off = align_up(off + (size_t)(batch + 1) * sizeof(int), 256);
   char* ws = static_cast<char*>(workspace(off, &st));
   if (!ws) return st;
 
@@ -422,6 +423,7 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   p.err = reinterpret_cast<int*>(ws + kErrOffset);
   p.hdr = reinterpret_cast<int*>(ws + o_hdr);
   p.items = reinterpret_cast<PrefillItem*>(ws + o_items);
+  p.tile_off = reinterpret_cast<int*>(ws + o_toff);
   p.batch = batch;
   p.total_q = total_q;
   p.Hq = num_qo_heads;

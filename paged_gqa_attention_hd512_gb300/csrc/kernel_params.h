@@ -75,6 +75,7 @@ struct PrefillParams {
   int* err;
   int* hdr;  // [0] number of items
   PrefillItem* items;
+  int* tile_off;  // [batch + 1] first tile of each sequence
   int batch, total_q, Hq, Hkv, group, page_size, window_left, causal, num_pages;
   int rows_per_tile;  // query positions per 128-row tile (128 / group)
   int max_items;

@@ -12,7 +12,7 @@
 //              ([128 keys][64 head-dim] bf16, 128B-swizzled) into a ring of 16 KB slots;
 //              zeroes V rows past the end of the sequence before releasing them
 //   warp 1     MMA issuer (one thread): S = Q K^T into TMEM (M 128, N 128, K 16 steps),
-//              O += P V with P read from TMEM (M 128, N 64 per V chunk)
+//              O += P V with P read from TMEM (M 128, N 128 per pair of V chunks)
 //   warps 4-7  softmax + epilogue: thread r owns row r (TMEM lane r): masks, online
 //              softmax in base 2 with lazy rescaling, writes P (bf16) into TMEM, and at the
 //              end normalises O and stores bf16 rows and lse
@@ -47,6 +47,9 @@ struct PrefillCfg {
   static constexpr int ALLOC = BYTES + 1024;
   static constexpr uint32_t TM_S = 0, TM_P = 128, TM_O = 256;
   static_assert(NSLOT >= 3, "KV ring too shallow");
+  // PV pairs adjacent V chunks into one N=128 MMA: every step consumes an even number of
+  // chunks (NQC + NVC), so with an even ring the pair never wraps
+  static_assert(NSLOT % 2 == 0 && NQC % 2 == 0 && NVC % 2 == 0, "V chunk pairs must sit in adjacent slots");
 };
 
 // ----------------------------------------------------------------------------- plan
@@ -64,57 +67,111 @@ __device__ __forceinline__ int prefill_tile_cost(const PrefillParams& p, int kv_
 }
 
 #ifdef PA_PREFILL_PLAN
+// Per-sequence tile offsets (exclusive scan over ceil(qo_len / P)), then a cost histogram
+// and a scatter over all tiles in parallel.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p) {
   __shared__ int hist[kPlanBuckets];
-  __shared__ int s_total;
+  __shared__ int s_red[32];
+  __shared__ int s_carry;
   const int tid = threadIdx.x;
   for (int i = tid; i < kPlanBuckets; i += blockDim.x) hist[i] = 0;
-  if (tid == 0) s_total = 0;
+  if (tid == 0) s_carry = 0;
   __syncthreads();
   const int P = p.rows_per_tile, ps = p.page_size;
-  // histogram of tile costs
-  for (int b = tid; b < p.batch; b += blockDim.x) {
-    const int qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
-    const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
-    const int kv_len = np > 0 ? (np - 1) * ps + p.kv_last_page_len[b] : 0;
-    int cnt = 0;
-    for (int q0 = 0; q0 < qo_len; q0 += P) {
-      const int c = min(kPlanBuckets - 1, prefill_tile_cost(p, kv_len, qo_len, q0));
-      atomicAdd(&hist[c], 1);
-      ++cnt;
+  int* off = p.tile_off;  // [batch + 1]
+  for (int base = 0; base < p.batch; base += blockDim.x) {
+    const int b = base + tid;
+    const int n = b < p.batch ? (p.qo_indptr[b + 1] - p.qo_indptr[b] + P - 1) / P : 0;
+    int v = n;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, v, o);
+      if ((tid & 31) >= o) v += t;
     }
-    atomicAdd(&s_total, cnt);
-  }
-  __syncthreads();
-  // exclusive prefix in descending cost order (bucket kPlanBuckets-1 first), serial: small
-  if (tid == 0) {
-    int run = 0;
-    for (int c = kPlanBuckets - 1; c >= 0; --c) {
-      const int n = hist[c];
-      hist[c] = run;
-      run += n;
-    }
-  }
-  __syncthreads();
-  for (int b = tid; b < p.batch; b += blockDim.x) {
-    const int qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
-    const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
-    const int kv_len = np > 0 ? (np - 1) * ps + p.kv_last_page_len[b] : 0;
-    for (int q0 = 0; q0 < qo_len; q0 += P) {
-      const int cost = prefill_tile_cost(p, kv_len, qo_len, q0);
-      const int slot = atomicAdd(&hist[min(kPlanBuckets - 1, cost)], 1);
-      for (int k = 0; k < p.Hkv; ++k) {
-        if (slot * p.Hkv + k >= p.max_items) break;  // cannot happen within the host bound
-        PrefillItem it;
-        it.b = b;
-        it.q_begin = q0;
-        it.kvh = k;
-        it.cost = cost;
-        p.items[slot * p.Hkv + k] = it;
+    if ((tid & 31) == 31) s_red[tid >> 5] = v;
+    __syncthreads();
+    if (tid < 32) {
+      int w = (tid < (int)(blockDim.x >> 5)) ? s_red[tid] : 0;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, w, o);
+        if (tid >= o) w += t;
       }
+      s_red[tid] = w;
+    }
+    __syncthreads();
+    const int excl = s_carry + v - n + ((tid >> 5) > 0 ? s_red[(tid >> 5) - 1] : 0);
+    if (b < p.batch) off[b] = excl;
+    __syncthreads();
+    if (tid == blockDim.x - 1) s_carry = excl + n;
+    __syncthreads();
+  }
+  const int n_tiles = s_carry;
+  if (tid == 0) off[p.batch] = n_tiles;
+  __syncthreads();
+  auto tile_of = [&](int t, int& b, int& q0, int& cost) {
+    int lo = 0, hi = p.batch - 1;  // last b with off[b] <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (off[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    b = lo;
+    q0 = (t - off[b]) * P;
+    const int qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
+    const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
+    const int kv_len = np > 0 ? (np - 1) * ps + p.kv_last_page_len[b] : 0;
+    cost = prefill_tile_cost(p, kv_len, qo_len, q0);
+  };
+  for (int t = tid; t < n_tiles; t += blockDim.x) {
+    int b, q0, cost;
+    tile_of(t, b, q0, cost);
+    atomicAdd(&hist[min(kPlanBuckets - 1, cost)], 1);
+  }
+  __syncthreads();
+  // exclusive prefix in descending cost order: bucket c starts after all buckets > c
+  {
+    constexpr int PER = kPlanBuckets / 1024;
+    int loc[PER], sum = 0;
+    for (int i = 0; i < PER; ++i) {  // thread tid owns buckets kPlanBuckets-1-(tid*PER+i)
+      loc[i] = hist[kPlanBuckets - 1 - (tid * PER + i)];
+      sum += loc[i];
+    }
+    int v = sum;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, v, o);
+      if ((tid & 31) >= o) v += t;
+    }
+    if ((tid & 31) == 31) s_red[tid >> 5] = v;
+    __syncthreads();
+    if (tid < 32) {
+      int w = s_red[tid];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, w, o);
+        if (tid >= o) w += t;
+      }
+      s_red[tid] = w;
+    }
+    __syncthreads();
+    int run = v - sum + ((tid >> 5) > 0 ? s_red[(tid >> 5) - 1] : 0);
+    for (int i = 0; i < PER; ++i) {
+      hist[kPlanBuckets - 1 - (tid * PER + i)] = run;
+      run += loc[i];
     }
   }
-  if (tid == 0) p.hdr[0] = min(s_total * p.Hkv, p.max_items);
+  __syncthreads();
+  for (int t = tid; t < n_tiles; t += blockDim.x) {
+    int b, q0, cost;
+    tile_of(t, b, q0, cost);
+    const int slot = atomicAdd(&hist[min(kPlanBuckets - 1, cost)], 1);
+    for (int k = 0; k < p.Hkv; ++k) {
+      if (slot * p.Hkv + k >= p.max_items) break;  // cannot happen within the host bound
+      PrefillItem it;
+      it.b = b;
+      it.q_begin = q0;
+      it.kvh = k;
+      it.cost = cost;
+      p.items[slot * p.Hkv + k] = it;
+    }
+  }
+  if (tid == 0) p.hdr[0] = min(n_tiles * p.Hkv, p.max_items);
 }
 #endif  // PA_PREFILL_PLAN
 
@@ -208,6 +265,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     uint32_t rc = 0, aux_phase = 0;
     int it_local = 0;
+    const uint64_t pol_kv = l2_policy_evict_last(), pol_q = l2_policy_evict_first();
     for (int r = 0;; ++r, ++it_local) {
       const int it = prefill_item_at(r);
       if (it >= n_items) break;
@@ -216,12 +274,22 @@ __global__ void __launch_bounds__(256, 1)
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQC * 128 * g * p.rows_per_tile));
         for (int c = 0; c < C::NQC; ++c)
-          tma_load_3d(q_s + c * (C::M * 128), &tm_q, c * 128, f.kvh * g, f.q_row0, q_full);
+          tma_load_3d_hint(q_s + c * (C::M * 128), &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
       }
       const int steps = C::NPASS * f.nt;
       const int page_tok_cap = f.np * ps;
+      // page ids of a step's KV tile, one per lane (lane < pieces); loaded a few steps
+      // ahead so the producer never waits on them
+      auto step_pages = [&](int st) -> int {
+        if (st < 0 || st >= steps) return 0;
+        const int key0 = (f.jlo + st % f.nt) * 128;
+        const int pieces = max(0, min(128, page_tok_cap - key0)) / ps;
+        return (lane < pieces) ? __ldg(p.kv_indices + f.ip0 + key0 / ps + lane) : 0;
+      };
+      int pg_v = 0, pg_k = step_pages(0), pg_f = step_pages(1);
       // chunks in the MMA thread's order: K of step 0, then (K of step k+1, V of step k)
       for (int k = -1; k < steps; ++k) {
+        const int pg_next = step_pages(k + 3);
         for (int part = 0; part < 2; ++part) {
           const bool is_k = (part == 0);
           const int st = is_k ? k + 1 : k;
@@ -231,7 +299,7 @@ __global__ void __launch_bounds__(256, 1)
           const int valid = max(0, min(128, f.kv_len - key0));
           const int load_rows = max(0, min(128, page_tok_cap - key0));
           const int pieces = load_rows / ps;
-          const int my_page = (lane < pieces) ? p.kv_indices[f.ip0 + key0 / ps + lane] : 0;
+          const int my_page = is_k ? pg_k : pg_v;
           const int nch = is_k ? C::NQC : C::NVC;
           for (int c = 0; c < nch; ++c, ++rc) {
             const int slot = rc % NSLOT;
@@ -245,7 +313,7 @@ __global__ void __launch_bounds__(256, 1)
             for (int pc = 0; pc < pieces; ++pc) {
               const int page = __shfl_sync(0xffffffffu, my_page, pc);
               if (lane == 0)
-                tma_load_3d(dst + pc * ps * 128, is_k ? &tm_k : &tm_v, col, f.kvh * ps, page, bar);
+                tma_load_3d_hint(dst + pc * ps * 128, is_k ? &tm_k : &tm_v, col, f.kvh * ps, page, bar, pol_kv);
             }
             if (fix) {
               mbar_wait(aux, aux_phase, p.err, SITE_PRE_DEQ);
@@ -259,13 +327,16 @@ __global__ void __launch_bounds__(256, 1)
             }
           }
         }
+        pg_v = pg_k;
+        pg_k = pg_f;
+        pg_f = pg_next;
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (one thread)
     if (lane == 0) {
       constexpr uint32_t ID_QK = idesc_f16<true>(128, 128, false);
-      constexpr uint32_t ID_PV = idesc_f16<true>(128, 64, true);
+      constexpr uint32_t ID_PV = idesc_f16<true>(128, 128, true);
       // completions seen so far of s_free (one per QK after the first), p_full (one per PV)
       // and o_free (one per finished pass)
       uint32_t rc = 0, n_qk = 0, n_pv = 0, n_pass = 0;
@@ -290,9 +361,12 @@ __global__ void __launch_bounds__(256, 1)
         mbar_wait(p_full, n_pv & 1, p.err, SITE_PRE_P_FULL);
         if (first_of_pass && n_pass > 0) mbar_wait(o_free, (n_pass - 1) & 1, p.err, SITE_PRE_O_DONE);
         tc_fence_after();
-        for (int c = 0; c < C::NVC; ++c, ++rc) {
+        // one N=128 MMA per 16 keys covers two adjacent V chunks (128 output columns); a
+        // TMEM-sourced MMA costs about the same time at N=64 as at N=128
+        for (int c = 0; c < C::NVC; c += 2, rc += 2) {
           const int slot = rc % NSLOT;
           mbar_wait(&kv_full[slot], (rc / NSLOT) & 1, p.err, SITE_PRE_KV_FULL);
+          mbar_wait(&kv_full[slot + 1], ((rc + 1) / NSLOT) & 1, p.err, SITE_PRE_KV_FULL);
           tc_fence_after();
           const uint32_t bsm = ring + slot * C::CHUNK;
 #pragma unroll
@@ -300,6 +374,7 @@ __global__ void __launch_bounds__(256, 1)
             tc_mma_ts(tbase + C::TM_O + c * 64, tbase + C::TM_P + kk * 8, desc_mnmajor_sw128(bsm + kk * 2048, C::CHUNK),
                       ID_PV, (!first_of_pass) || kk > 0);
           tc_commit(&kv_empty[slot]);
+          tc_commit(&kv_empty[slot + 1]);
         }
         tc_commit(o_done);
         ++n_pv;
@@ -426,7 +501,8 @@ __global__ void __launch_bounds__(256, 1)
           if (row_ok) {
             uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]);
+            for (int i = 0; i < 4; ++i)
+              st_global_stream_v4(dst + i, make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]));
           }
         }
         tc_fence_before();
