@@ -427,16 +427,20 @@ __global__ void __launch_bounds__(256, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(s_free);
+          // visible keys of this row as tile-local indices [lo, hi]: the mask is a select on
+          // two compares (short-circuit forms compiled to per-element branches), and the
+          // max / sum run as four independent chains
           const int key0 = (f.jlo + jt) * 128;
-          float mx = -INFINITY;
+          const int lo = klo - key0, hi = min(khi, f.kv_len - 1) - key0;
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
           for (int i = 0; i < 128; ++i) {
-            const int key = key0 + i;
-            const bool ok = key >= klo && key <= khi && key < f.kv_len;
+            const bool ok = (i >= lo) & (i <= hi);
             const float x = ok ? __uint_as_float(sr[i]) * scale_log2 : -INFINITY;
             sr[i] = __float_as_uint(x);
-            mx = fmaxf(mx, x);
+            mx4[i & 3] = fmaxf(mx4[i & 3], x);
           }
+          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
           const float m_new = fmaxf(m_used, mx);
           bool resc = false;
           float alpha = 1.f;
@@ -448,15 +452,16 @@ __global__ void __launch_bounds__(256, 1)
             resc = true;
           }
           const float base = (m_used == -INFINITY) ? 0.f : m_used;
-          float sum = 0.f;
+          float sum4[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t pk[64];
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
             const float p0 = fast_exp2(__uint_as_float(sr[2 * i]) - base);
             const float p1 = fast_exp2(__uint_as_float(sr[2 * i + 1]) - base);
-            sum += p0 + p1;
+            sum4[i & 3] += p0 + p1;
             pk[i] = pack_bf16x2(p0, p1);
           }
+          const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
           if (gstep > 0) mbar_wait(o_done, (gstep - 1) & 1, p.err, SITE_PRE_O_DONE);
           __syncwarp();
           tc_fence_after();

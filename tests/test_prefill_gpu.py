@@ -29,6 +29,9 @@ CASES = [
     (512, 256, 8, 1, 16, [333], [333], 1, -1),
     (256, 256, 32, 16, 16, [190, 17], [190, 17], 1, -1),
     (256, 256, 4, 2, 64, [129, 128], [129, 128], 1, 100),
+    (512, 512, 8, 2, 8, [600, 300], [600, 300], 1, -1),
+    (512, 256, 16, 2, 64, [700], [700], 1, 200),
+    (512, 512, 24, 4, 32, [900, 513], [400, 513], 1, -1),
 ]
 
 
