@@ -372,7 +372,6 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   if (batch == 0 || total_q == 0) return PA_OK;
   // K/V tiles are 128B-swizzled TMA boxes of page_size rows: they need whole 8-row atoms
   if (page_size < 8) return PA_ERR_UNSUPPORTED;
-  if (kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
   const int group = num_qo_heads / num_kv_heads;
   const int rows_per_tile = 128 / group;
   int smem_optin = 0;

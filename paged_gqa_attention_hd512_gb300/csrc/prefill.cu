@@ -5,30 +5,37 @@
 
 namespace pa {
 
-template <int DQK, int DVO>
+template <int KVT, int DQK, int DVO>
 static cudaError_t run_prefill(const PrefillLaunch& L) {
   using C = PrefillCfg<DQK, DVO>;
-  auto kern = prefill_kernel<DQK, DVO>;
+  auto kern = prefill_kernel<KVT, DQK, DVO>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC);
   if (e != cudaSuccess) return e;
   kern<<<L.grid, 256, C::ALLOC, L.stream>>>(L.tq, L.tk, L.tv, L.p);
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill(int kvt, int dqk, int dvo, const PrefillLaunch& L, const char** variant) {
-  if (kvt != KV_BF16) return cudaErrorInvalidValue;
+template <int KVT>
+static cudaError_t dispatch_prefill(int dqk, int dvo, const PrefillLaunch& L, const char** variant) {
   if (dqk == 512 && dvo == 512) {
     *variant = "prefill_512x512";
-    return run_prefill<512, 512>(L);
+    return run_prefill<KVT, 512, 512>(L);
   }
   if (dqk == 512 && dvo == 256) {
     *variant = "prefill_512x256";
-    return run_prefill<512, 256>(L);
+    return run_prefill<KVT, 512, 256>(L);
   }
   if (dqk == 256 && dvo == 256) {
     *variant = "prefill_256x256";
-    return run_prefill<256, 256>(L);
+    return run_prefill<KVT, 256, 256>(L);
   }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_prefill(int kvt, int dqk, int dvo, const PrefillLaunch& L, const char** variant) {
+  if (kvt == KV_BF16) return dispatch_prefill<KV_BF16>(dqk, dvo, L, variant);
+  if (kvt == KV_FP8) return dispatch_prefill<KV_FP8>(dqk, dvo, L, variant);
+  if (kvt == KV_NVFP4) return dispatch_prefill<KV_NVFP4>(dqk, dvo, L, variant);
   return cudaErrorInvalidValue;
 }
 

@@ -209,7 +209,7 @@ __device__ __forceinline__ int prefill_item_at(int r) {
   return r * (int)gridDim.x + off;
 }
 
-template <int DQK, int DVO>
+template <int KVT, int DQK, int DVO>
 __global__ void __launch_bounds__(256, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(256, 1)
     mbar_init(o_free, 4);
     mbar_init(aux, 1);
     for (int s = 0; s < NSLOT; ++s) {
-      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_full[s], KVT == KV_BF16 ? 1 : 2);  // quantised KV: both dequant warps arrive
       mbar_init(&kv_empty[s], 1);
     }
     fence_mbar_init();
@@ -256,7 +256,7 @@ __global__ void __launch_bounds__(256, 1)
   const int n_items = min(p.hdr[0], p.max_items);
   const int ps = p.page_size, g = p.group;
 
-  if (warp == 0) {
+  if (warp == 0 && KVT == KV_BF16) {
     // ------------------------------------------------------------ producer (whole warp)
     if (lane == 0) {
       tma_prefetch_desc(&tm_q);
@@ -332,6 +332,142 @@ __global__ void __launch_bounds__(256, 1)
         pg_f = pg_next;
       }
     }
+  } else if (warp == 0) {
+    // ------------------------------------------------------------ Q producer (quantised KV)
+    const uint64_t pol_q = l2_policy_evict_first();
+    if (lane == 0) tma_prefetch_desc(&tm_q);
+    for (int r = 0, it_local = 0;; ++r, ++it_local) {
+      const int it = prefill_item_at(r);
+      if (it >= n_items) break;
+      const PrefillItemInfo f = prefill_item_info(p, it);
+      mbar_wait(q_empty, (it_local & 1) ^ 1, p.err, SITE_PRE_Q);
+      if (lane == 0) {
+        mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQC * 128 * g * p.rows_per_tile));
+        for (int c = 0; c < C::NQC; ++c)
+          tma_load_3d_hint(q_s + c * (C::M * 128), &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
+      }
+    }
+  } else if (warp == 2 || warp == 3) {
+    if constexpr (KVT != KV_BF16) {
+      // ---------------------------------------------------------- dequantising KV producer
+      // Same slot order as the TMA producer.  Thread t (0..63) fills rows t and t + 64 of
+      // each [128 keys][64 dims] slot: FP8 / FP4 bytes (and NVFP4 block scales) are read
+      // with 16-byte loads, converted exactly to bf16 in registers (e4m3 and e2m1 x e4m3
+      // are exact in f16 and in bf16; the per-tensor / global scales are applied to the
+      // scores and the output instead) and written in the 128B-swizzled layout.  Loads of
+      // slot i are issued before slot i-1 is converted, to hide their latency.
+      constexpr int RAW16 = KVT == KV_FP8 ? 4 : 2;  // 16-byte loads per 64-element row slice
+      const int t = threadIdx.x - 64;
+      const size_t rows_per_block = (size_t)p.Hkv * ps;
+      const size_t page_bytes = rows_per_block * (DQK + DVO) * (KVT == KV_FP8 ? 2 : 1) / 2;
+      const size_t sf_page = rows_per_block * (DQK + DVO) / 16;
+      uint32_t rc = 0;
+      // the slot whose loads are in flight
+      bool pend = false;
+      uint32_t pend_rc = 0;
+      bool pend_ok[2] = {false, false};
+      uint4 pend_raw[2][RAW16];
+      uint32_t pend_sf[2] = {0u, 0u};
+      auto finish = [&]() {
+        if (!pend) return;
+        const int slot = pend_rc % NSLOT;
+        mbar_wait(&kv_empty[slot], ((pend_rc / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
+        uint8_t* sp = smem + C::OFF_RING + slot * C::CHUNK;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int row = t + 64 * h;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {  // 16-byte output chunk j = elements 8j .. 8j+7
+            uint4 o = make_uint4(0, 0, 0, 0);
+            if (pend_ok[h]) {
+              uint32_t w[4];
+              if constexpr (KVT == KV_FP8) {
+                const uint4 a = pend_raw[h][j >> 1];
+                const uint32_t w0 = (j & 1) ? a.z : a.x, w1 = (j & 1) ? a.w : a.y;
+                w[0] = f16x2_to_bf16x2(e4m3x2_to_f16x2(w0 & 0xFFFFu));
+                w[1] = f16x2_to_bf16x2(e4m3x2_to_f16x2(w0 >> 16));
+                w[2] = f16x2_to_bf16x2(e4m3x2_to_f16x2(w1 & 0xFFFFu));
+                w[3] = f16x2_to_bf16x2(e4m3x2_to_f16x2(w1 >> 16));
+              } else {
+                const uint4 a = pend_raw[h][j >> 2];
+                const uint32_t word = (j & 3) == 0 ? a.x : (j & 3) == 1 ? a.y : (j & 3) == 2 ? a.z : a.w;
+                const uint32_t sfb = (pend_sf[h] >> (8 * (j >> 1))) & 0xFFu;
+                const uint32_t sf2 = e4m3x2_to_f16x2(sfb | (sfb << 8));
+                uint32_t f[4];
+                e2m1x8_to_f16x2x4(word, f);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) w[q] = f16x2_to_bf16x2(hmul2_u32(f[q], sf2));
+              }
+              o = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+            *reinterpret_cast<uint4*>(sp + row * 128 + ((j ^ (row & 7)) << 4)) = o;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&kv_full[slot]);
+        pend = false;
+      };
+      for (int r = 0;; ++r) {
+        const int it = prefill_item_at(r);
+        if (it >= n_items) break;
+        const PrefillItemInfo f = prefill_item_info(p, it);
+        const int steps = C::NPASS * f.nt;
+        for (int k = -1; k < steps; ++k) {
+          for (int part = 0; part < 2; ++part) {
+            const bool is_k = (part == 0);
+            const int st = is_k ? k + 1 : k;
+            if (st < 0 || st >= steps) continue;
+            const int pass = st / f.nt, jt = st % f.nt;
+            const int key0 = (f.jlo + jt) * 128;
+            int page[2], pslot[2];
+            bool ok[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int key = key0 + t + 64 * h;
+              ok[h] = key < f.kv_len;
+              page[h] = ok[h] ? __ldg(p.kv_indices + f.ip0 + key / ps) : 0;
+              pslot[h] = key % ps;
+            }
+            const int dim = is_k ? DQK : DVO;
+            const int nch = is_k ? C::NQC : C::NVC;
+            for (int c = 0; c < nch; ++c, ++rc) {
+              const int d0 = is_k ? c * 64 : pass * C::DVP + c * 64;
+              uint4 raw[2][RAW16];
+              uint32_t sfw[2] = {0u, 0u};
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const size_t elem = ((size_t)(f.kvh * ps + pslot[h])) * dim + d0;
+                if (ok[h]) {
+                  const size_t blk = is_k ? 0 : rows_per_block * DQK;
+                  const uint8_t* src = p.kv_cache + (size_t)page[h] * page_bytes +
+                                       (KVT == KV_FP8 ? blk + elem : (blk + elem) / 2);
+#pragma unroll
+                  for (int q = 0; q < RAW16; ++q) raw[h][q] = __ldg(reinterpret_cast<const uint4*>(src) + q);
+                  if constexpr (KVT == KV_NVFP4)
+                    sfw[h] = __ldg(reinterpret_cast<const uint32_t*>(p.sf + (size_t)page[h] * sf_page +
+                                                                     (blk + elem) / 16));
+                } else {
+#pragma unroll
+                  for (int q = 0; q < RAW16; ++q) raw[h][q] = make_uint4(0, 0, 0, 0);
+                }
+              }
+              finish();
+              pend = true;
+              pend_rc = rc;
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                pend_ok[h] = ok[h];
+                pend_sf[h] = sfw[h];
+#pragma unroll
+                for (int q = 0; q < RAW16; ++q) pend_raw[h][q] = raw[h][q];
+              }
+            }
+          }
+        }
+      }
+      finish();
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (one thread)
     if (lane == 0) {
@@ -402,7 +538,9 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ softmax + epilogue
     const int row = threadIdx.x - 128;  // TMEM lane == tile row
     const uint32_t lane_base = tbase + ((uint32_t)(32 * (warp - 4)) << 16);
-    const float scale_log2 = p.sm_scale * 1.4426950408889634f;
+    // FP8 per-tensor / NVFP4 global K scale folds into the scores, the V scale into the output
+    const float scale_log2 = p.sm_scale * 1.4426950408889634f * (KVT == KV_BF16 ? 1.f : __ldg(p.k_scale));
+    const float v_scale = KVT == KV_BF16 ? 1.f : __ldg(p.v_scale);
     uint32_t gstep = 0;
     for (int r = 0;; ++r) {
       const int it = prefill_item_at(r);
@@ -492,7 +630,7 @@ __global__ void __launch_bounds__(256, 1)
         mbar_wait(o_done, (gstep - 1) & 1, p.err, SITE_PRE_O_DONE);
         __syncwarp();
         tc_fence_after();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const float inv = l > 0.f ? v_scale / l : 0.f;
         uint16_t* orow = p.out + ((size_t)(f.q_row0 + p_local) * p.Hq + hq) * DVO + pass * C::DVP;
 #pragma unroll 1
         for (int c = 0; c < C::DVP / 32; ++c) {

@@ -59,6 +59,12 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
       : "memory");
 }
 
+// f16x2 -> bf16x2 through f32 (exact for values representable in both)
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  return pack_bf16x2(f.x, f.y);
+}
+
 // L2 cache policies (createpolicy): keep K/V resident, stream Q through.
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t pol;

@@ -92,8 +92,9 @@ def _prefill_rows(c):
     return rows
 
 
-def test_fullsize_causal_prefill():
-    c = synth.workload("causal_prefill_bf16", device="cuda")
-    check_sampled(c, [0, 3], _prefill_rows(c))
+@pytest.mark.parametrize("name,seqs", [("causal_prefill_bf16", [0, 3]), ("nvfp4_asym_prefill", [0, 7])])
+def test_fullsize_prefill(name, seqs):
+    c = synth.workload(name, device="cuda")
+    check_sampled(c, seqs, _prefill_rows(c))
     del c
     torch.cuda.empty_cache()

@@ -49,10 +49,35 @@ def test_prefill_parity(c):
     assert pa.paged_attn_last_variant() == f"prefill_{dqk}x{dvo}_bf16"
 
 
-def test_prefill_small_pages_are_refused():
+def test_prefill_small_pages_are_refused():  # noqa: D103
     ensure_built()
     case = synth.make_case("prefill", batch=1, Hq=8, Hkv=1, d_qk=512, d_vo=512, page_size=4,
                            kv_lens=[20], qo_lens=[20], seed=9).to("cuda")
     with pytest.raises(pa.PagedAttnError) as e:
         pa.run_case(case)
     assert e.value.status == pa.PA_ERR_UNSUPPORTED
+
+
+QCASES = [
+    # (dtype, dqk, dvo, Hq, Hkv, page_size, kv_lens, qo_lens, causal, window)
+    (synth.KV_FP8, 512, 512, 24, 4, 16, [300, 129], [300, 129], 1, -1),
+    (synth.KV_FP8, 512, 256, 8, 1, 64, [200], [150], 1, -1),
+    (synth.KV_FP8, 256, 256, 6, 3, 16, [100, 31], [100, 31], 1, -1),
+    (synth.KV_NVFP4, 512, 256, 16, 2, 32, [300, 100], [300, 100], 1, -1),
+    (synth.KV_NVFP4, 512, 512, 8, 2, 16, [260, 64], [260, 64], 1, 40),
+    (synth.KV_NVFP4, 256, 256, 12, 4, 8, [150, 33], [150, 33], 0, -1),
+]
+
+
+def _qid(c):
+    return {synth.KV_FP8: "fp8", synth.KV_NVFP4: "nvfp4"}[c[0]] + "-" + _id(c[1:])
+
+
+@pytest.mark.parametrize("c", QCASES, ids=[_qid(c) for c in QCASES])
+def test_prefill_parity_quantised(c):
+    dt, dqk, dvo, hq, hkv, ps, kv, qo, causal, win = c
+    case = synth.make_case("prefill", batch=len(kv), Hq=hq, Hkv=hkv, d_qk=dqk, d_vo=dvo, page_size=ps,
+                           kv_lens=kv, qo_lens=qo, kv_dtype=dt, causal=causal, window_left=win, seed=600 + len(kv))
+    check_full(case, _qid(c))
+    names = {synth.KV_FP8: "fp8", synth.KV_NVFP4: "nvfp4"}
+    assert pa.paged_attn_last_variant() == f"prefill_{dqk}x{dvo}_{names[dt]}"
