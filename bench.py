@@ -19,6 +19,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import random
 import math
 import os
 import statistics
@@ -185,8 +186,14 @@ def time_region(fn, steps, warmup, barrier=None):
 
 
 def oracle_sample_rate(host_case, budget_s: float, kind: str):
-    """Time the fp64 oracle on a bounded sample of (sequence, kv head) units of the
-    workload; returns (rate in the metric's unit, seconds, description, threads)."""
+    """Time the fp64 oracle on a bounded sample of the workload and return (rate in the
+    metric's unit, seconds, description, threads).
+
+    Decode samples (sequence, kv head) units, all query heads of the group each; prefill
+    samples (query token, kv head) units, strided across every sequence so that short and
+    long causal rows are both represented.  The sample cycles through the units (repeating
+    them when the workload has fewer than the budget needs) and grows until it takes
+    roughly ``budget_s`` seconds."""
     import numpy as np
 
     import oracle
@@ -195,48 +202,48 @@ def oracle_sample_rate(host_case, budget_s: float, kind: str):
     c = host_case
     g = c.group
     qo = c.qo_indptr.tolist()
-    units = [(b, k) for b in range(c.batch) for k in range(c.Hkv)]
-    stride = max(1, len(units) // 64)
-    units = units[::stride]
+    if kind == "decode":
+        units = [(b, k, qo[b]) for b in range(c.batch) for k in range(c.Hkv) if qo[b + 1] > qo[b]]
+    else:
+        units = [(b, k, t) for b in range(c.batch) for t in range(qo[b], qo[b + 1]) for k in range(c.Hkv)]
+        units = units[::max(1, len(units) // 4096)]
+    # a fixed shuffle, so that any prefix of the sample spans the whole batch
+    random.Random(0).shuffle(units)
+
+    def work_of(sel):
+        if kind == "decode":
+            tok = 0
+            for b, _, _ in sel:
+                L = c.kv_lens[b]
+                tok += min(L, c.window_left + 1) if c.window_left >= 0 else L
+            return tok * (c.d_qk + c.d_vo) * _beta_x2(c.kv_dtype) // 2 + len(sel) * g * (2 * c.d_qk + 2 * c.d_vo + 4)
+        pairs = 0
+        for b, _, t in sel:
+            L, Q = c.kv_lens[b], c.qo_lens[b]
+            pos = L - Q + (t - qo[b])
+            lo = max(0, pos - c.window_left) if c.window_left >= 0 else 0
+            pairs += max(0, (pos if c.causal else L - 1) - lo + 1)
+        return pairs * g * (2 * c.d_qk + 2 * c.d_vo)
 
     def run(n):
-        sel = units[:n]
-        tok, head = [], []
-        for b, k in sel:
-            for t in range(qo[b], qo[b + 1]):
-                for h in range(k * g, (k + 1) * g):
-                    tok.append(t)
-                    head.append(h)
+        sel = [units[i % len(units)] for i in range(n)]
+        tok = np.repeat(np.array([t for _, _, t in sel], dtype=np.int64), g)
+        head = np.concatenate([np.arange(k * g, (k + 1) * g) for _, k, _ in sel])
         t0 = time.perf_counter()
-        oracle.rows(c, np.array(tok), np.array(head), threads=threads)
+        oracle.rows(c, tok, head, threads=threads)
         return time.perf_counter() - t0, sel
 
-    n = min(len(units), threads)
+    n = threads
     dt, sel = run(n)
-    while dt < budget_s * 0.4 and n < len(units):
-        n = min(len(units), max(n + 1, int(n * budget_s * 0.8 / max(dt, 1e-3))))
+    while dt < budget_s * 0.5:
+        n = max(n + 1, int(n * min(64.0, budget_s * 0.8 / max(dt, 1e-3))))
         dt, sel = run(n)
-    seqs = sorted({b for b, _ in sel})
-    if kind == "decode":
-        tok = 0
-        for b, _ in sel:
-            L = c.kv_lens[b]
-            tok += min(L, c.window_left + 1) if c.window_left >= 0 else L
-        work = tok * (c.d_qk + c.d_vo) * _beta_x2(c.kv_dtype) // 2 + len(sel) * g * (2 * c.d_qk + 2 * c.d_vo + 4)
-        rate = work / dt / 1e9
-    else:
-        sub = synth.Case(**{f: getattr(c, f) for f in c.__dataclass_fields__})
-        pairs = 0
-        for b, _ in sel:
-            L, Q = c.kv_lens[b], c.qo_lens[b]
-            for i in range(Q):
-                pos = L - Q + i
-                lo = max(0, pos - c.window_left) if c.window_left >= 0 else 0
-                pairs += max(0, (pos if c.causal else L - 1) - lo + 1)
-        work = pairs * g * (2 * c.d_qk + 2 * c.d_vo)
-        rate = work / dt / 1e12
-        del sub
-    desc = f"{len(sel)} (sequence, kv head) units of {len(seqs)} sequences, all {g} query heads each"
+    rate = work_of(sel) / dt / (1e9 if kind == "decode" else 1e12)
+    distinct = len({u for u in sel})
+    seqs = len({b for b, _, _ in sel})
+    what = "(sequence, kv head)" if kind == "decode" else "(query token, kv head)"
+    desc = (f"{len(sel)} {what} units ({distinct} distinct, from {seqs} sequences), all {g} query heads each, "
+            f"{dt:.1f} s of oracle time")
     return rate, dt, desc, threads
 
 
