@@ -394,6 +394,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
     ap.add_argument("--workload", default=MAIN, help="decode workload of the main line")
     ap.add_argument("--prefill-only", action="store_true", help="time only the prefill workload (profiling)")
+    ap.add_argument("--prefill-workload", default=PREFILL, help="prefill workload of --prefill-only")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -422,7 +423,7 @@ def main():
     torch.cuda.set_device(local)
     pk = peaks()
     if args.prefill_only:
-        res = bench_prefill(PREFILL, max(3, min(50, args.steps // 40)), args.warmup, local, pk)
+        res = bench_prefill(args.prefill_workload, max(3, min(50, args.steps // 40)), args.warmup, local, pk)
         if rank == 0:
             print(json.dumps({"prefill": res}), flush=True)
         return 0

@@ -161,17 +161,18 @@ int device_sms(int* smem_optin) {
   return sms;
 }
 
-// K, V (and NVFP4 scale) maps over the cache; box_rows rows per box.
+// K, V (and NVFP4 scale) maps over the cache; boxes of box_rows rows of box_inner bytes
+// (the scale boxes hold whole scale rows).
 bool make_kv_maps(CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tsfk, CUtensorMap* tsfv, const void* kv_cache,
                   const uint8_t* sf, int num_pages, int Hkv, int dqk, int dvo, int ps, int kvt, int box_rows,
-                  bool swz) {
+                  bool swz, uint32_t box_inner = 128) {
   const int x2 = x2_of(kvt);
   const uint64_t k_row = (uint64_t)dqk * x2 / 2, v_row = (uint64_t)dvo * x2 / 2;
   const uint64_t rows = (uint64_t)Hkv * ps;
   const uint64_t page_bytes = rows * (k_row + v_row);
   const uint8_t* base = static_cast<const uint8_t*>(kv_cache);
-  if (!make_map(tk, base, k_row, rows, num_pages, page_bytes, 128, box_rows, swz)) return false;
-  if (!make_map(tv, base + rows * k_row, v_row, rows, num_pages, page_bytes, 128, box_rows, swz)) return false;
+  if (!make_map(tk, base, k_row, rows, num_pages, page_bytes, box_inner, box_rows, swz)) return false;
+  if (!make_map(tv, base + rows * k_row, v_row, rows, num_pages, page_bytes, box_inner, box_rows, swz)) return false;
   if (kvt == KV_NVFP4) {
     const uint64_t sk = dqk / 16, sv = dvo / 16, sf_page = rows * (sk + sv);
     if (!make_map(tsfk, sf, sk, rows, num_pages, sf_page, (uint32_t)sk, box_rows, false)) return false;
@@ -390,9 +391,13 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
 
   PrefillLaunch L;
   std::memset(&L, 0, sizeof L);
-  CUtensorMap dummy_sf[2];
-  if (!make_kv_maps(&L.tk, &L.tv, &dummy_sf[0], &dummy_sf[1], kv_cache, nullptr, num_pages, num_kv_heads,
-                    head_dim_qk, head_dim_vo, page_size, kv_dtype, page_size, true))
+  // bf16 K/V: 128B-swizzled boxes of [page_size][64 elements], read by the MMAs as they land.
+  // FP8 / NVFP4: unswizzled boxes of the packed bytes of 64 elements per key (64 / 32 B) and
+  // whole block-scale rows, staged for the converter warps.
+  const bool quant = kv_dtype != PA_KV_BF16;
+  if (!make_kv_maps(&L.tk, &L.tv, &L.tsfk, &L.tsfv, kv_cache, kv_scales ? kv_scales->sf : nullptr, num_pages,
+                    num_kv_heads, head_dim_qk, head_dim_vo, page_size, kv_dtype, page_size, !quant,
+                    quant ? (kv_dtype == KV_FP8 ? 64u : 32u) : 128u))
     return PA_ERR_CUDA;
   // Q as [total_q][Hq][d_qk] bf16 bytes: boxes of [rows_per_tile][group][128 B]
   {

@@ -60,9 +60,9 @@ __device__ __forceinline__ uint64_t globaltimer() {
 }
 // Wait for the phase with the given parity to complete; give up after ~2 s.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int site) {
-  const uint32_t addr = smem_u32(bar);
-  if (mbar_try_wait(addr, parity)) return true;
+// The spinning part stays out of line: inlined into a tcgen05.mma issue loop it cost that
+// loop about half of its MMA rate (measured on sm_103a), even when never taken.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t addr, uint32_t parity, int* err, int site) {
   // once any wait of this launch (or an earlier one) has given up, do not wait again
   if (err && *reinterpret_cast<volatile int*>(err) != 0) return false;
   const uint64_t t0 = globaltimer();
@@ -74,6 +74,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* e
     }
   }
   return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int site) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try_wait(addr, parity)) return true;
+  return mbar_wait_slow(addr, parity, err, site);
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

@@ -19,6 +19,8 @@ enum {
   SITE_PRE_P_FULL = 206,
   SITE_PRE_O_DONE = 207,
   SITE_PRE_DEQ = 208,
+  SITE_PRE_STG = 209,
+  SITE_PRE_SF = 210,
 };
 
 // Decode work list entry: one page-aligned chunk of one sequence.

@@ -7,11 +7,11 @@ namespace pa {
 
 template <int KVT, int DQK, int DVO>
 static cudaError_t run_prefill(const PrefillLaunch& L) {
-  using C = PrefillCfg<DQK, DVO>;
+  using C = PrefillCfg<DQK, DVO, KVT>;
   auto kern = prefill_kernel<KVT, DQK, DVO>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC);
   if (e != cudaSuccess) return e;
-  kern<<<L.grid, 256, C::ALLOC, L.stream>>>(L.tq, L.tk, L.tv, L.p);
+  kern<<<L.grid, C::THREADS, C::ALLOC, L.stream>>>(L.tq, L.tk, L.tv, L.tsfk, L.tsfv, L.p);
   return cudaGetLastError();
 }
 
@@ -44,11 +44,17 @@ cudaError_t launch_prefill_plan(const PrefillParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <int KVT>
+static int smem_bytes(int dqk, int dvo) {
+  if (dqk == 512 && dvo == 512) return PrefillCfg<512, 512, KVT>::ALLOC;
+  if (dqk == 512 && dvo == 256) return PrefillCfg<512, 256, KVT>::ALLOC;
+  return PrefillCfg<256, 256, KVT>::ALLOC;
+}
+
 int prefill_smem_bytes(int kvt, int dqk, int dvo) {
-  (void)kvt;
-  if (dqk == 512 && dvo == 512) return PrefillCfg<512, 512>::ALLOC;
-  if (dqk == 512 && dvo == 256) return PrefillCfg<512, 256>::ALLOC;
-  return PrefillCfg<256, 256>::ALLOC;
+  if (kvt == KV_FP8) return smem_bytes<KV_FP8>(dqk, dvo);
+  if (kvt == KV_NVFP4) return smem_bytes<KV_NVFP4>(dqk, dvo);
+  return smem_bytes<KV_BF16>(dqk, dvo);
 }
 
 }  // namespace pa

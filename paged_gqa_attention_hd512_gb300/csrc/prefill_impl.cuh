@@ -8,17 +8,23 @@
 // One CTA per SM (persistent).  A work item is 128 query rows = P positions x g heads of
 // one kv head (P = 128 / g), so every K/V tile loaded into shared memory serves all g
 // query heads that read it.  Warp roles:
-//   warp 0     producer: TMA loads of the Q tile (once per item) and of K/V chunks
-//              ([128 keys][64 head-dim] bf16, 128B-swizzled) into a ring of 16 KB slots;
-//              zeroes V rows past the end of the sequence before releasing them
-//   warp 1     MMA issuer (one thread): S = Q K^T into TMEM (M 128, N 128, K 16 steps),
-//              O += P V with P read from TMEM (M 128, N 128 per pair of V chunks)
-//   warps 4-7  softmax + epilogue: thread r owns row r (TMEM lane r): masks, online
-//              softmax in base 2 with lazy rescaling, writes P (bf16) into TMEM, and at the
-//              end normalises O and stores bf16 rows and lse
-// TMEM (512 columns): S [0, 128), P [128, 192), O [256, 512).  A 128 x 512 fp32 O tile
-// would fill all of TMEM, so head_dim_vo 512 is computed in two passes of 256 columns over
-// the same KV range (S is recomputed; the softmax statistics of both passes are identical).
+//   warp 0      producer: TMA loads of the Q tile (once per item) and, for bf16 KV, of K/V
+//               chunks ([128 keys][64 head-dim], 128B-swizzled) into a ring of 16 KB slots
+//               (V rows past the end of the sequence are zeroed before release); for FP8 /
+//               NVFP4 KV, of the packed chunks and block scales into staging rings
+//   warp 1      MMA issuer (the warp polls, lane 0 issues): S = Q K^T into TMEM (M 128,
+//               N 128, K 16 steps), O += P V with P read from TMEM (M 128, N 128 per pair
+//               of V chunks)
+//   warps 4-7   softmax + epilogue: thread r owns row r (TMEM lane r): masks, online
+//               softmax in base 2 with lazy rescaling, writes P into TMEM, and at the end
+//               normalises O and stores bf16 rows and lse
+//   warps 8-11  (FP8 / NVFP4 KV only) converters: staged chunks -> the MMA ring
+// TMEM (512 columns): two S buffers [0, 128) and [128, 256), used by alternate KV steps,
+// each holding its step's P once the softmax has read S, and O [256, 512).  With two S
+// buffers the QK of the next step runs while the softmax works on this one.  A 128 x 512
+// fp32 O tile would fill all of TMEM, so head_dim_vo 512 is computed in two passes of 256
+// columns over the same KV range (S is recomputed; the softmax statistics of both passes
+// are identical).
 #pragma once
 
 #include "common.cuh"
@@ -26,7 +32,7 @@
 
 namespace pa {
 
-template <int DQK, int DVO>
+template <int DQK, int DVO, int KVT>
 struct PrefillCfg {
   static constexpr int M = 128;                 // query rows per tile
   static constexpr int N = 128;                 // keys per KV tile
@@ -37,16 +43,40 @@ struct PrefillCfg {
   static constexpr int NVC = DVP / 64;          // V chunks per pass
   static constexpr int Q_BYTES = NQC * M * 128;
   static constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
+  static constexpr bool QUANT = KVT != KV_BF16;
+  // quantised KV adds a warpgroup of converters (warps 8-11, one key row per thread)
+  static constexpr int THREADS = QUANT ? 384 : 256;
+  // Quantised KV: warp 0 streams the packed bytes of each chunk ([128 keys][CW bytes]) and,
+  // for NVFP4, the block scales of each K or V tile ([128 keys][D / 16 bytes]) into staging
+  // rings with TMA; the converters turn them into the bf16 / f16 ring the MMAs read.  The
+  // staging rings hide the L2 latency, so the converted ring only covers the conversion.
+  static constexpr int CW = KVT == KV_FP8 ? 64 : (KVT == KV_NVFP4 ? 32 : 0);  // packed bytes per key and chunk
+  static constexpr int STG_BYTES = N * CW;
+  static constexpr int SFW_K = DQK / 16, SFW_V = DVO / 16;                  // scale bytes per key
+  static constexpr int SF_BYTES = KVT == KV_NVFP4 ? N * SFW_K : 0;
+  static constexpr int NSF = KVT == KV_NVFP4 ? 2 : 0;
   static constexpr int NSLOT_RAW = (SMEM_BUDGET - Q_BYTES) / CHUNK;
-  static constexpr int NSLOT = NSLOT_RAW > 8 ? 8 : NSLOT_RAW;
+  static constexpr int NSLOT = QUANT ? 4 : (NSLOT_RAW > 8 ? 8 : NSLOT_RAW);
+  static constexpr int NSTG_RAW = QUANT ? (SMEM_BUDGET - Q_BYTES - NSLOT * CHUNK - NSF * SF_BYTES) / (STG_BYTES + 8) : 0;
+  static constexpr int NSTG = NSTG_RAW > 8 ? 8 : NSTG_RAW;
   static constexpr int OFF_RING = Q_BYTES;
-  static constexpr int OFF_BAR = Q_BYTES + NSLOT * CHUNK;
-  // barriers: q_full, q_empty, s_full, s_free, p_full, o_done, o_free, aux, kv_full[], kv_empty[]
-  static constexpr int NBAR = 8 + 2 * NSLOT;
+  static constexpr int OFF_STG = Q_BYTES + NSLOT * CHUNK;
+  static constexpr int OFF_SF = OFF_STG + NSTG * STG_BYTES;
+  static constexpr int OFF_DESC = OFF_SF + NSF * SF_BYTES;  // int2 per staging slot: valid keys, flags
+  static constexpr int OFF_BAR = OFF_DESC + NSTG * 8;
+  // barriers: q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_free, aux, kv_full[],
+  // kv_empty[], stg_full[], stg_empty[], sf_full[], sf_empty[].  Every waiter of a barrier
+  // is at most one phase behind or ahead of it (a parity wait cannot tell more apart):
+  // hence one s_full / p_full / pv_done per S buffer.
+  static constexpr int NBAR = 10 + 2 * NSLOT + 2 * NSTG + 2 * NSF;
   static constexpr int BYTES = OFF_BAR + NBAR * 8 + 16;
   static constexpr int ALLOC = BYTES + 1024;
-  static constexpr uint32_t TM_S = 0, TM_P = 128, TM_O = 256;
+  // TMEM columns: two S buffers of 128 keys (step j uses buffer j & 1; its P, 128 keys of
+  // bf16 / f16, is written over the first 64 columns of the same buffer), O from 256
+  static constexpr uint32_t TM_S = 0, TM_O = 256;
   static_assert(NSLOT >= 3, "KV ring too shallow");
+  static_assert(!QUANT || NSTG >= 3, "staging ring too shallow");
+  static_assert(ALLOC <= 232448, "shared memory");
   // PV pairs adjacent V chunks into one N=128 MMA: every step consumes an even number of
   // chunks (NQC + NVC), so with an even ring the pair never wraps
   static_assert(NSLOT % 2 == 0 && NQC % 2 == 0 && NVC % 2 == 0, "V chunk pairs must sit in adjacent slots");
@@ -210,10 +240,11 @@ __device__ __forceinline__ int prefill_item_at(int r) {
 }
 
 template <int KVT, int DQK, int DVO>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const PrefillParams p) {
-  using C = PrefillCfg<DQK, DVO>;
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sfk,
+                   const __grid_constant__ CUtensorMap tm_sfv, const PrefillParams p) {
+  using C = PrefillCfg<DQK, DVO, KVT>;
   constexpr int NSLOT = C::NSLOT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -222,29 +253,42 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* s_full = bars + 2;
-  uint64_t* s_free = bars + 3;
-  uint64_t* p_full = bars + 4;
-  uint64_t* o_done = bars + 5;
-  uint64_t* o_free = bars + 6;
-  uint64_t* aux = bars + 7;
-  uint64_t* kv_full = bars + 8;
-  uint64_t* kv_empty = bars + 8 + NSLOT;
+  uint64_t* s_full = bars + 2;  // [2]: S of step j complete in buffer j & 1
+  uint64_t* p_full = bars + 4;  // [2]: P of step j written over buffer j & 1
+  uint64_t* pv_done = bars + 6;  // [2]: PV of step j (which reads buffer j & 1) complete
+  uint64_t* o_free = bars + 8;
+  uint64_t* aux = bars + 9;
+  uint64_t* kv_full = bars + 10;
+  uint64_t* kv_empty = bars + 10 + NSLOT;
+  uint64_t* stg_full = bars + 10 + 2 * NSLOT;
+  uint64_t* stg_empty = stg_full + C::NSTG;
+  uint64_t* sf_full = stg_empty + C::NSTG;
+  uint64_t* sf_empty = sf_full + C::NSF;
+  int2* stg_desc = reinterpret_cast<int2*>(smem + C::OFF_DESC);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(s_free, 4);
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
+      mbar_init(&p_full[b], 4);
+      mbar_init(&pv_done[b], 1);
+    }
     mbar_init(o_free, 4);
     mbar_init(aux, 1);
     for (int s = 0; s < NSLOT; ++s) {
-      mbar_init(&kv_full[s], KVT == KV_BF16 ? 1 : 2);  // quantised KV: both dequant warps arrive
+      mbar_init(&kv_full[s], KVT == KV_BF16 ? 1 : 4);  // quantised KV: the four converter warps arrive
       mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < C::NSTG; ++s) {
+      mbar_init(&stg_full[s], 1);
+      mbar_init(&stg_empty[s], 4);
+    }
+    for (int s = 0; s < C::NSF; ++s) {
+      mbar_init(&sf_full[s], 1);
+      mbar_init(&sf_empty[s], 4);
     }
     fence_mbar_init();
   }
@@ -286,20 +330,20 @@ __global__ void __launch_bounds__(256, 1)
         const int pieces = max(0, min(128, page_tok_cap - key0)) / ps;
         return (lane < pieces) ? __ldg(p.kv_indices + f.ip0 + key0 / ps + lane) : 0;
       };
-      int pg_v = 0, pg_k = step_pages(0), pg_f = step_pages(1);
-      // chunks in the MMA thread's order: K of step 0, then (K of step k+1, V of step k)
-      for (int k = -1; k < steps; ++k) {
-        const int pg_next = step_pages(k + 3);
-        for (int part = 0; part < 2; ++part) {
-          const bool is_k = (part == 0);
-          const int st = is_k ? k + 1 : k;
-          if (st < 0 || st >= steps) continue;
+      int pg_a = step_pages(0), pg_b = step_pages(1);
+      // chunks in the MMA thread's order: steps in pairs, K of both, then V of both
+      for (int k = 0; k < steps; k += 2) {
+        const int pg_c = step_pages(k + 2), pg_d = step_pages(k + 3);
+        for (int part = 0; part < 4; ++part) {
+          const bool is_k = part < 2;
+          const int st = k + (part & 1);
+          if (st >= steps) continue;
           const int pass = st / f.nt, jt = st % f.nt;
           const int key0 = (f.jlo + jt) * 128;
           const int valid = max(0, min(128, f.kv_len - key0));
           const int load_rows = max(0, min(128, page_tok_cap - key0));
           const int pieces = load_rows / ps;
-          const int my_page = is_k ? pg_k : pg_v;
+          const int my_page = (part & 1) ? pg_b : pg_a;
           const int nch = is_k ? C::NQC : C::NVC;
           for (int c = 0; c < nch; ++c, ++rc) {
             const int slot = rc % NSLOT;
@@ -327,192 +371,247 @@ __global__ void __launch_bounds__(256, 1)
             }
           }
         }
-        pg_v = pg_k;
-        pg_k = pg_f;
-        pg_f = pg_next;
+        pg_a = pg_c;
+        pg_b = pg_d;
       }
     }
   } else if (warp == 0) {
-    // ------------------------------------------------------------ Q producer (quantised KV)
-    const uint64_t pol_q = l2_policy_evict_first();
-    if (lane == 0) tma_prefetch_desc(&tm_q);
-    for (int r = 0, it_local = 0;; ++r, ++it_local) {
-      const int it = prefill_item_at(r);
-      if (it >= n_items) break;
-      const PrefillItemInfo f = prefill_item_info(p, it);
-      mbar_wait(q_empty, (it_local & 1) ^ 1, p.err, SITE_PRE_Q);
+    // ------------------------------------------------ producer for quantised KV (whole warp)
+    // Q tiles as in the bf16 producer; K / V as packed bytes into the staging ring, one
+    // chunk per slot with a descriptor (valid keys, flags) the converters read after the
+    // slot fills; NVFP4 block scales of each K or V tile into the scale ring.
+    if constexpr (C::QUANT) {
+      constexpr int FL_V = 1, FL_FIRST = 2, FL_LAST = 4, FL_END = 8;
       if (lane == 0) {
-        mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQC * 128 * g * p.rows_per_tile));
-        for (int c = 0; c < C::NQC; ++c)
-          tma_load_3d_hint(q_s + c * (C::M * 128), &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
-      }
-    }
-  } else if (warp == 2 || warp == 3) {
-    if constexpr (KVT != KV_BF16) {
-      // ---------------------------------------------------------- dequantising KV producer
-      // Same slot order as the TMA producer.  Thread t (0..63) fills rows t and t + 64 of
-      // each [128 keys][64 dims] slot: FP8 / FP4 bytes (and NVFP4 block scales) are read
-      // with 16-byte loads, converted exactly to bf16 in registers (e4m3 and e2m1 x e4m3
-      // are exact in f16 and in bf16; the per-tensor / global scales are applied to the
-      // scores and the output instead) and written in the 128B-swizzled layout.  Loads of
-      // slot i are issued before slot i-1 is converted, to hide their latency.
-      constexpr int RAW16 = KVT == KV_FP8 ? 4 : 2;  // 16-byte loads per 64-element row slice
-      const int t = threadIdx.x - 64;
-      const size_t rows_per_block = (size_t)p.Hkv * ps;
-      const size_t page_bytes = rows_per_block * (DQK + DVO) * (KVT == KV_FP8 ? 2 : 1) / 2;
-      const size_t sf_page = rows_per_block * (DQK + DVO) / 16;
-      uint32_t rc = 0;
-      // the slot whose loads are in flight
-      bool pend = false;
-      uint32_t pend_rc = 0;
-      bool pend_ok[2] = {false, false};
-      uint4 pend_raw[2][RAW16];
-      uint32_t pend_sf[2] = {0u, 0u};
-      auto finish = [&]() {
-        if (!pend) return;
-        const int slot = pend_rc % NSLOT;
-        mbar_wait(&kv_empty[slot], ((pend_rc / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
-        uint8_t* sp = smem + C::OFF_RING + slot * C::CHUNK;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int row = t + 64 * h;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {  // 16-byte output chunk j = elements 8j .. 8j+7
-            uint4 o = make_uint4(0, 0, 0, 0);
-            if (pend_ok[h]) {
-              uint32_t w[4];
-              if constexpr (KVT == KV_FP8) {
-                const uint4 a = pend_raw[h][j >> 1];
-                const uint32_t w0 = (j & 1) ? a.z : a.x, w1 = (j & 1) ? a.w : a.y;
-                w[0] = f16x2_to_bf16x2(e4m3x2_to_f16x2(w0 & 0xFFFFu));
-                w[1] = f16x2_to_bf16x2(e4m3x2_to_f16x2(w0 >> 16));
-                w[2] = f16x2_to_bf16x2(e4m3x2_to_f16x2(w1 & 0xFFFFu));
-                w[3] = f16x2_to_bf16x2(e4m3x2_to_f16x2(w1 >> 16));
-              } else {
-                const uint4 a = pend_raw[h][j >> 2];
-                const uint32_t word = (j & 3) == 0 ? a.x : (j & 3) == 1 ? a.y : (j & 3) == 2 ? a.z : a.w;
-                const uint32_t sfb = (pend_sf[h] >> (8 * (j >> 1))) & 0xFFu;
-                const uint32_t sf2 = e4m3x2_to_f16x2(sfb | (sfb << 8));
-                uint32_t f[4];
-                e2m1x8_to_f16x2x4(word, f);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) w[q] = f16x2_to_bf16x2(hmul2_u32(f[q], sf2));
-              }
-              o = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-            *reinterpret_cast<uint4*>(sp + row * 128 + ((j ^ (row & 7)) << 4)) = o;
-          }
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+        if constexpr (KVT == KV_NVFP4) {
+          tma_prefetch_desc(&tm_sfk);
+          tma_prefetch_desc(&tm_sfv);
         }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&kv_full[slot]);
-        pend = false;
-      };
-      for (int r = 0;; ++r) {
+      }
+      const uint64_t pol_kv = l2_policy_evict_last(), pol_q = l2_policy_evict_first();
+      const uint32_t stg = q_s + C::OFF_STG, sfb = q_s + C::OFF_SF;
+      uint32_t n = 0, nsf = 0;
+      int it_local = 0;
+      for (int r = 0;; ++r, ++it_local) {
         const int it = prefill_item_at(r);
         if (it >= n_items) break;
         const PrefillItemInfo f = prefill_item_info(p, it);
+        mbar_wait(q_empty, (it_local & 1) ^ 1, p.err, SITE_PRE_Q);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQC * 128 * g * p.rows_per_tile));
+          for (int c = 0; c < C::NQC; ++c)
+            tma_load_3d_hint(q_s + c * (C::M * 128), &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
+        }
         const int steps = C::NPASS * f.nt;
-        for (int k = -1; k < steps; ++k) {
-          for (int part = 0; part < 2; ++part) {
-            const bool is_k = (part == 0);
-            const int st = is_k ? k + 1 : k;
-            if (st < 0 || st >= steps) continue;
+        const int page_tok_cap = f.np * ps;
+        auto step_pages = [&](int st) -> int {
+          if (st < 0 || st >= steps) return 0;
+          const int key0 = (f.jlo + st % f.nt) * 128;
+          const int pieces = max(0, min(128, page_tok_cap - key0)) / ps;
+          return (lane < pieces) ? __ldg(p.kv_indices + f.ip0 + key0 / ps + lane) : 0;
+        };
+        int pg_a = step_pages(0), pg_b = step_pages(1);
+        for (int k = 0; k < steps; k += 2) {
+          const int pg_c = step_pages(k + 2), pg_d = step_pages(k + 3);
+          for (int part = 0; part < 4; ++part) {
+            const bool is_k = part < 2;
+            const int st = k + (part & 1);
+            if (st >= steps) continue;
             const int pass = st / f.nt, jt = st % f.nt;
             const int key0 = (f.jlo + jt) * 128;
-            int page[2], pslot[2];
-            bool ok[2];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const int key = key0 + t + 64 * h;
-              ok[h] = key < f.kv_len;
-              page[h] = ok[h] ? __ldg(p.kv_indices + f.ip0 + key / ps) : 0;
-              pslot[h] = key % ps;
-            }
-            const int dim = is_k ? DQK : DVO;
-            const int nch = is_k ? C::NQC : C::NVC;
-            for (int c = 0; c < nch; ++c, ++rc) {
-              const int d0 = is_k ? c * 64 : pass * C::DVP + c * 64;
-              uint4 raw[2][RAW16];
-              uint32_t sfw[2] = {0u, 0u};
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                const size_t elem = ((size_t)(f.kvh * ps + pslot[h])) * dim + d0;
-                if (ok[h]) {
-                  const size_t blk = is_k ? 0 : rows_per_block * DQK;
-                  const uint8_t* src = p.kv_cache + (size_t)page[h] * page_bytes +
-                                       (KVT == KV_FP8 ? blk + elem : (blk + elem) / 2);
-#pragma unroll
-                  for (int q = 0; q < RAW16; ++q) raw[h][q] = __ldg(reinterpret_cast<const uint4*>(src) + q);
-                  if constexpr (KVT == KV_NVFP4)
-                    sfw[h] = __ldg(reinterpret_cast<const uint32_t*>(p.sf + (size_t)page[h] * sf_page +
-                                                                     (blk + elem) / 16));
-                } else {
-#pragma unroll
-                  for (int q = 0; q < RAW16; ++q) raw[h][q] = make_uint4(0, 0, 0, 0);
-                }
+            const int valid = max(0, min(128, f.kv_len - key0));
+            const int pieces = max(0, min(128, page_tok_cap - key0)) / ps;
+            const int my_page = (part & 1) ? pg_b : pg_a;
+            if constexpr (KVT == KV_NVFP4) {
+              const int sw = is_k ? C::SFW_K : C::SFW_V;
+              const int si = nsf % C::NSF;
+              mbar_wait(&sf_empty[si], ((nsf / C::NSF) & 1) ^ 1, p.err, SITE_PRE_SF);
+              if (lane == 0) mbar_arrive_expect_tx(&sf_full[si], (uint32_t)(pieces * ps * sw));
+              for (int pc = 0; pc < pieces; ++pc) {
+                const int page = __shfl_sync(0xffffffffu, my_page, pc);
+                if (lane == 0)
+                  tma_load_3d_hint(sfb + si * C::SF_BYTES + pc * ps * sw, is_k ? &tm_sfk : &tm_sfv, 0, f.kvh * ps,
+                                   page, &sf_full[si], pol_kv);
               }
-              finish();
-              pend = true;
-              pend_rc = rc;
-#pragma unroll
-              for (int h = 0; h < 2; ++h) {
-                pend_ok[h] = ok[h];
-                pend_sf[h] = sfw[h];
-#pragma unroll
-                for (int q = 0; q < RAW16; ++q) pend_raw[h][q] = raw[h][q];
+              ++nsf;
+            }
+            const int nch = is_k ? C::NQC : C::NVC;
+            for (int c = 0; c < nch; ++c, ++n) {
+              const int stage = n % C::NSTG;
+              mbar_wait(&stg_empty[stage], ((n / C::NSTG) & 1) ^ 1, p.err, SITE_PRE_STG);
+              const int d0 = is_k ? c * 64 : pass * C::DVP + c * 64;  // first head-dim element
+              const int col = d0 * C::CW / 64;                        // its byte in the packed row
+              if (lane == 0) {
+                const int flags = (is_k ? 0 : FL_V) | (c == 0 ? FL_FIRST : 0) | (c == nch - 1 ? FL_LAST : 0) |
+                                  ((d0 / 16) << 8);
+                stg_desc[stage] = make_int2(valid, flags);
+                mbar_arrive_expect_tx(&stg_full[stage], (uint32_t)(pieces * ps * C::CW));
+              }
+              for (int pc = 0; pc < pieces; ++pc) {
+                const int page = __shfl_sync(0xffffffffu, my_page, pc);
+                if (lane == 0)
+                  tma_load_3d_hint(stg + stage * C::STG_BYTES + pc * ps * C::CW, is_k ? &tm_k : &tm_v, col,
+                                   f.kvh * ps, page, &stg_full[stage], pol_kv);
               }
             }
           }
+          pg_a = pg_c;
+          pg_b = pg_d;
         }
       }
-      finish();
+      // end marker
+      const int stage = n % C::NSTG;
+      mbar_wait(&stg_empty[stage], ((n / C::NSTG) & 1) ^ 1, p.err, SITE_PRE_STG);
+      if (lane == 0) {
+        stg_desc[stage] = make_int2(0, FL_END);
+        mbar_arrive(&stg_full[stage]);
+      }
+    }
+  } else if (warp >= 8) {
+    if constexpr (C::QUANT) {
+      // ---------------------------------------------------------- converters (warps 8-11)
+      // Thread t owns key t of each staged chunk: it converts the chunk's packed values
+      // exactly (e4m3 and e2m1 x e4m3 are exact in f16 and in bf16; the per-tensor / global
+      // scales are applied to the scores and the output instead) and writes them in the
+      // 128B-swizzled layout the MMAs read: K as bf16 (the type of q), V as f16 (P is written
+      // in f16 for these kernels, and e4m3 / e2m1 convert to f16 in one instruction).  Keys
+      // past the end of the sequence are written as 0, whatever the slot holds.
+      constexpr int FL_V = 1, FL_FIRST = 2, FL_LAST = 4, FL_END = 8;
+      constexpr int RAW16 = C::CW / 16;
+      const int t = threadIdx.x - 256;
+      const uint8_t* stg = smem + C::OFF_STG;
+      const uint8_t* sfb = smem + C::OFF_SF;
+      uint32_t nsf = 0;
+      for (uint32_t j = 0;; ++j) {
+        const int stage = j % C::NSTG;
+        mbar_wait(&stg_full[stage], (j / C::NSTG) & 1, p.err, SITE_PRE_STG);
+        const int2 d = stg_desc[stage];
+        if (d.y & FL_END) break;
+        const bool is_v = d.y & FL_V;
+        const int si = C::NSF > 0 ? nsf % (C::NSF > 0 ? C::NSF : 1) : 0;
+        if constexpr (KVT == KV_NVFP4)
+          if (d.y & FL_FIRST) mbar_wait(&sf_full[si], (nsf / C::NSF) & 1, p.err, SITE_PRE_SF);
+        const int slot = j % NSLOT;
+        mbar_wait(&kv_empty[slot], ((j / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
+        __syncwarp();
+        uint8_t* sp = smem + C::OFF_RING + slot * C::CHUNK;
+        const bool ok = t < d.x;
+        uint4 raw[RAW16];
+#pragma unroll
+        for (int q = 0; q < RAW16; ++q)
+          raw[q] = ok ? *reinterpret_cast<const uint4*>(stg + stage * C::STG_BYTES + t * C::CW + 16 * q)
+                      : make_uint4(0, 0, 0, 0);
+        uint32_t sfw = 0;
+        if constexpr (KVT == KV_NVFP4)
+          if (ok)
+            sfw = *reinterpret_cast<const uint32_t*>(sfb + si * C::SF_BYTES + t * (is_v ? C::SFW_V : C::SFW_K) +
+                                                     (d.y >> 8));
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {  // 16-byte output chunk jj = elements 8jj .. 8jj+7
+          uint32_t w[4];
+          if constexpr (KVT == KV_FP8) {
+            const uint4 a = raw[jj >> 1];
+            const uint32_t w0 = (jj & 1) ? a.z : a.x, w1 = (jj & 1) ? a.w : a.y;
+            w[0] = e4m3x2_to_f16x2(w0 & 0xFFFFu);
+            w[1] = e4m3x2_to_f16x2(w0 >> 16);
+            w[2] = e4m3x2_to_f16x2(w1 & 0xFFFFu);
+            w[3] = e4m3x2_to_f16x2(w1 >> 16);
+          } else {
+            const uint4 a = raw[jj >> 2];
+            const uint32_t word = (jj & 3) == 0 ? a.x : (jj & 3) == 1 ? a.y : (jj & 3) == 2 ? a.z : a.w;
+            const uint32_t sb = (sfw >> (8 * (jj >> 1))) & 0xFFu;
+            const uint32_t sf2 = e4m3x2_to_f16x2(sb | (sb << 8));
+            uint32_t f4[4];
+            e2m1x8_to_f16x2x4(word, f4);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) w[q] = hmul2_u32(f4[q], sf2);
+          }
+          if (!is_v) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) w[q] = f16x2_to_bf16x2(w[q]);
+          }
+          *reinterpret_cast<uint4*>(sp + t * 128 + ((jj ^ (t & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&kv_full[slot]);
+          mbar_arrive(&stg_empty[stage]);
+          if (KVT == KV_NVFP4 && (d.y & FL_LAST)) mbar_arrive(&sf_empty[si]);
+        }
+        if (KVT == KV_NVFP4 && (d.y & FL_LAST)) ++nsf;
+      }
+      (void)FL_FIRST;
     }
   } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (one thread)
-    if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    // The whole warp walks the schedule and polls the barriers; lane 0 issues every MMA and
+    // commit (a commit tracks the MMAs of the thread that issues it).  Polling from a
+    // single diverged lane cost the issue loop about half of its MMA rate (measured).
+    {
       constexpr uint32_t ID_QK = idesc_f16<true>(128, 128, false);
-      constexpr uint32_t ID_PV = idesc_f16<true>(128, 128, true);
-      // completions seen so far of s_free (one per QK after the first), p_full (one per PV)
-      // and o_free (one per finished pass)
+      // quantised KV: P and V in f16
+      constexpr uint32_t ID_PV = idesc_f16<!C::QUANT>(128, 128, true);
+      const bool leader = lane == 0;
+      // steps issued so far (QK into S buffer n_qk & 1; PV reads P of step n_pv from buffer
+      // n_pv & 1) and passes finished.  QK of step j + 2 reuses the buffer of step j, where
+      // PV of step j reads P: it waits for that PV to complete (an MMA that reads its A
+      // operand from TMEM is not ordered against a later MMA writing the same columns).
+      // Steps are issued in pairs, QK QK PV PV, so that another MMA group is always queued
+      // behind the PV being waited for and the pipe never drains.  One barrier per buffer:
+      // the next PV on a buffer follows the QK that waits on it, so a barrier is never two
+      // phases ahead of its waiter.
       uint32_t rc = 0, n_qk = 0, n_pv = 0, n_pass = 0;
       int it_local = 0;
       auto issue_qk = [&]() {
-        if (n_qk > 0) mbar_wait(s_free, (n_qk - 1) & 1, p.err, SITE_PRE_S_FREE);
+        const uint32_t s_col = C::TM_S + 128 * (n_qk & 1);
+        if (n_qk >= 2) mbar_wait(&pv_done[n_qk & 1], ((n_qk - 2) >> 1) & 1, p.err, SITE_PRE_O_DONE);
         for (int c = 0; c < C::NQC; ++c, ++rc) {
           const int slot = rc % NSLOT;
           mbar_wait(&kv_full[slot], (rc / NSLOT) & 1, p.err, SITE_PRE_KV_FULL);
+          __syncwarp();
           tc_fence_after();
-          const uint32_t a = q_s + c * (C::M * 128), bsm = ring + slot * C::CHUNK;
+          if (leader) {
+            const uint32_t a = q_s + c * (C::M * 128), bsm = ring + slot * C::CHUNK;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            tc_mma_ss(tbase + C::TM_S, desc_kmajor_sw128(a + kk * 32), desc_kmajor_sw128(bsm + kk * 32), ID_QK,
-                      (c | kk) != 0);
-          tc_commit(&kv_empty[slot]);
+            for (int kk = 0; kk < 4; ++kk)
+              tc_mma_ss(tbase + s_col, desc_kmajor_sw128(a + kk * 32), desc_kmajor_sw128(bsm + kk * 32), ID_QK,
+                        (c | kk) != 0);
+            tc_commit(&kv_empty[slot]);
+          }
+          __syncwarp();
         }
-        tc_commit(s_full);
+        if (leader) tc_commit(&s_full[n_qk & 1]);
+        __syncwarp();
         ++n_qk;
       };
       auto issue_pv = [&](bool first_of_pass) {
-        mbar_wait(p_full, n_pv & 1, p.err, SITE_PRE_P_FULL);
+        mbar_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1, p.err, SITE_PRE_P_FULL);
+        const uint32_t p_col = C::TM_S + 128 * (n_pv & 1);
         if (first_of_pass && n_pass > 0) mbar_wait(o_free, (n_pass - 1) & 1, p.err, SITE_PRE_O_DONE);
-        tc_fence_after();
-        // one N=128 MMA per 16 keys covers two adjacent V chunks (128 output columns); a
-        // TMEM-sourced MMA costs about the same time at N=64 as at N=128
+        // one N=128 MMA per 16 keys covers two adjacent V chunks (128 output columns)
         for (int c = 0; c < C::NVC; c += 2, rc += 2) {
           const int slot = rc % NSLOT;
           mbar_wait(&kv_full[slot], (rc / NSLOT) & 1, p.err, SITE_PRE_KV_FULL);
           mbar_wait(&kv_full[slot + 1], ((rc + 1) / NSLOT) & 1, p.err, SITE_PRE_KV_FULL);
+          __syncwarp();
           tc_fence_after();
-          const uint32_t bsm = ring + slot * C::CHUNK;
+          if (leader) {
+            const uint32_t bsm = ring + slot * C::CHUNK;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            tc_mma_ts(tbase + C::TM_O + c * 64, tbase + C::TM_P + kk * 8, desc_mnmajor_sw128(bsm + kk * 2048, C::CHUNK),
-                      ID_PV, (!first_of_pass) || kk > 0);
-          tc_commit(&kv_empty[slot]);
-          tc_commit(&kv_empty[slot + 1]);
+            for (int kk = 0; kk < 8; ++kk)
+              tc_mma_ts(tbase + C::TM_O + c * 64, tbase + p_col + kk * 8,
+                        desc_mnmajor_sw128(bsm + kk * 2048, C::CHUNK), ID_PV, (!first_of_pass) || kk > 0);
+            tc_commit(&kv_empty[slot]);
+            tc_commit(&kv_empty[slot + 1]);
+          }
+          __syncwarp();
         }
-        tc_commit(o_done);
+        if (leader) tc_commit(&pv_done[n_pv & 1]);
+        __syncwarp();
         ++n_pv;
         if (first_of_pass) ++n_pass;
       };
@@ -522,19 +621,22 @@ __global__ void __launch_bounds__(256, 1)
         const PrefillItemInfo f = prefill_item_info(p, it);
         const int steps = C::NPASS * f.nt;
         mbar_wait(q_full, it_local & 1, p.err, SITE_PRE_Q);
-        // S of step k+1 is computed while the softmax of step k runs; PV of step k follows
-        issue_qk();
-        if (steps == 1) tc_commit(q_empty);
-        for (int k = 0; k < steps; ++k) {
-          if (k + 1 < steps) {
-            issue_qk();
-            if (k + 1 == steps - 1) tc_commit(q_empty);
+        // the S of the second step of a pair is computed while the softmax of the first
+        // runs, and the PVs of the pair while the softmax of the second finishes
+        for (int k = 0; k < steps; k += 2) {
+          const bool two = k + 1 < steps;
+          issue_qk();
+          if (two) issue_qk();
+          if (k + (two ? 1 : 0) == steps - 1) {  // the item's last QK: Q may be replaced
+            if (leader) tc_commit(q_empty);
+            __syncwarp();
           }
           issue_pv(k % f.nt == 0);
+          if (two) issue_pv((k + 1) % f.nt == 0);
         }
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax + epilogue
     const int row = threadIdx.x - 128;  // TMEM lane == tile row
     const uint32_t lane_base = tbase + ((uint32_t)(32 * (warp - 4)) << 16);
@@ -555,16 +657,14 @@ __global__ void __launch_bounds__(256, 1)
       for (int pass = 0; pass < C::NPASS; ++pass) {
         float m_used = -INFINITY, l = 0.f;
         for (int jt = 0; jt < f.nt; ++jt, ++gstep) {
-          mbar_wait(s_full, gstep & 1, p.err, SITE_PRE_S_FULL);
+          const uint32_t s_col = C::TM_S + 128 * (gstep & 1);
+          mbar_wait(&s_full[gstep & 1], (gstep >> 1) & 1, p.err, SITE_PRE_S_FULL);
           __syncwarp();  // the tcgen05 loads below are warp-collective
           tc_fence_after();
           uint32_t sr[128];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + C::TM_S + 32 * c, sr + 32 * c);
+          for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + 32 * c, sr + 32 * c);
           tc_wait_ld();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(s_free);
           // visible keys of this row as tile-local indices [lo, hi]: the mask is a select on
           // two compares (short-circuit forms compiled to per-element branches), and the
           // max / sum run as four independent chains
@@ -597,15 +697,16 @@ __global__ void __launch_bounds__(256, 1)
             const float p0 = fast_exp2(__uint_as_float(sr[2 * i]) - base);
             const float p1 = fast_exp2(__uint_as_float(sr[2 * i + 1]) - base);
             sum4[i & 3] += p0 + p1;
-            pk[i] = pack_bf16x2(p0, p1);
+            pk[i] = C::QUANT ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
           const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-          if (gstep > 0) mbar_wait(o_done, (gstep - 1) & 1, p.err, SITE_PRE_O_DONE);
-          __syncwarp();
-          tc_fence_after();
           // tcgen05.ld / st are warp-collective (.sync.aligned): the whole warp rescales when
-          // any of its rows needs it, the other rows with a factor of 1
+          // any of its rows needs it, the other rows with a factor of 1, once the PV of the
+          // previous step has finished with O
           if (__any_sync(0xffffffffu, resc)) {
+            mbar_wait(&pv_done[(gstep - 1) & 1], ((gstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
+            __syncwarp();
+            tc_fence_after();
             const float a = resc ? alpha : 1.f;
 #pragma unroll 1
             for (int c = 0; c < C::DVP / 32; ++c) {
@@ -619,15 +720,15 @@ __global__ void __launch_bounds__(256, 1)
           }
           if (resc) l *= alpha;
           l += sum;
-          tmem_st32(lane_base + C::TM_P, pk);
-          tmem_st32(lane_base + C::TM_P + 32, pk + 32);
+          tmem_st32(lane_base + s_col, pk);
+          tmem_st32(lane_base + s_col + 32, pk + 32);
           tc_wait_st();
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(p_full);
+          if (lane == 0) mbar_arrive(&p_full[gstep & 1]);
         }
         // ---- epilogue of this pass: O / l -> bf16
-        mbar_wait(o_done, (gstep - 1) & 1, p.err, SITE_PRE_O_DONE);
+        mbar_wait(&pv_done[(gstep - 1) & 1], ((gstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
         __syncwarp();
         tc_fence_after();
         const float inv = l > 0.f ? v_scale / l : 0.f;
