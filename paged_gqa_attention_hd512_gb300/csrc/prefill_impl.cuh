@@ -36,27 +36,31 @@ template <int DQK, int DVO, int KVT>
 struct PrefillCfg {
   static constexpr int M = 128;                 // query rows per tile
   static constexpr int N = 128;                 // keys per KV tile
-  static constexpr int CHUNK = N * 128;         // bytes of one [128 keys][64 dims] bf16 chunk
-  static constexpr int NQC = DQK / 64;          // Q / K chunks (64 head-dim columns each)
+  static constexpr int HALF = N * 128;          // one [128 keys][64 dims] bf16 block (16 KB)
+  static constexpr int CHUNK = 2 * HALF;        // one ring slot: [128 keys][128 dims], two blocks
+  static constexpr int NQB = DQK / 64;          // Q blocks of 64 head-dim columns
+  static constexpr int NQC = DQK / 128;         // K chunks per step (8 QK MMAs each)
   static constexpr int DVP = DVO > 256 ? 256 : DVO;  // output columns per pass
   static constexpr int NPASS = DVO / DVP;
-  static constexpr int NVC = DVP / 64;          // V chunks per pass
-  static constexpr int Q_BYTES = NQC * M * 128;
+  static constexpr int NVC = DVP / 128;         // V chunks per pass (one N=128 PV group each)
+  static constexpr int Q_BYTES = NQB * HALF;
   static constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
   static constexpr bool QUANT = KVT != KV_BF16;
   // quantised KV adds a warpgroup of converters (warps 8-11, one key row per thread)
   static constexpr int THREADS = QUANT ? 384 : 256;
-  // Quantised KV: warp 0 streams the packed bytes of each chunk ([128 keys][CW bytes]) and,
-  // for NVFP4, the block scales of each K or V tile ([128 keys][D / 16 bytes]) into staging
-  // rings with TMA; the converters turn them into the bf16 / f16 ring the MMAs read.  The
-  // staging rings hide the L2 latency, so the converted ring only covers the conversion.
-  static constexpr int CW = KVT == KV_FP8 ? 64 : (KVT == KV_NVFP4 ? 32 : 0);  // packed bytes per key and chunk
+  // Quantised KV: warp 0 streams the packed bytes of each 64-dim half chunk ([128 keys][CW
+  // bytes]) and, for NVFP4, the block scales of each K or V tile ([128 keys][D / 16 bytes])
+  // into staging rings with TMA; the converters turn two staged halves into one slot of the
+  // bf16 / f16 ring the MMAs read.  The staging rings hide the L2 latency, so the converted
+  // ring only covers the conversion.
+  static constexpr int CW = KVT == KV_FP8 ? 64 : (KVT == KV_NVFP4 ? 32 : 0);  // packed bytes per key and half
   static constexpr int STG_BYTES = N * CW;
+  static constexpr int NQS = 2 * NQC, NVS = 2 * NVC;                         // staged halves per step
   static constexpr int SFW_K = DQK / 16, SFW_V = DVO / 16;                  // scale bytes per key
   static constexpr int SF_BYTES = KVT == KV_NVFP4 ? N * SFW_K : 0;
   static constexpr int NSF = KVT == KV_NVFP4 ? 2 : 0;
   static constexpr int NSLOT_RAW = (SMEM_BUDGET - Q_BYTES) / CHUNK;
-  static constexpr int NSLOT = QUANT ? 4 : (NSLOT_RAW > 8 ? 8 : NSLOT_RAW);
+  static constexpr int NSLOT = QUANT ? (DQK > 256 ? 2 : 3) : (NSLOT_RAW > 4 ? 4 : NSLOT_RAW);
   static constexpr int NSTG_RAW = QUANT ? (SMEM_BUDGET - Q_BYTES - NSLOT * CHUNK - NSF * SF_BYTES) / (STG_BYTES + 8) : 0;
   static constexpr int NSTG = NSTG_RAW > 8 ? 8 : NSTG_RAW;
   static constexpr int OFF_RING = Q_BYTES;
@@ -74,12 +78,15 @@ struct PrefillCfg {
   // TMEM columns: two S buffers of 128 keys (step j uses buffer j & 1; its P, 128 keys of
   // bf16 / f16, is written over the first 64 columns of the same buffer), O from 256
   static constexpr uint32_t TM_S = 0, TM_O = 256;
-  static_assert(NSLOT >= 3, "KV ring too shallow");
+  // Named (hardware) barriers between the gate warp and the MMA warp, 64 threads each:
+  // one per ring slot, per S buffer for P and for PV completion, Q tile, O free.
+  static constexpr int NB_SLOT = 1, NB_P = NB_SLOT + NSLOT, NB_PV = NB_P + 2, NB_Q = NB_PV + 2,
+                       NB_OFREE = NB_Q + 1;
+  static_assert(NSLOT >= 2, "KV ring too shallow");
   static_assert(!QUANT || NSTG >= 3, "staging ring too shallow");
   static_assert(ALLOC <= 232448, "shared memory");
-  // PV pairs adjacent V chunks into one N=128 MMA: every step consumes an even number of
-  // chunks (NQC + NVC), so with an even ring the pair never wraps
-  static_assert(NSLOT % 2 == 0 && NQC % 2 == 0 && NVC % 2 == 0, "V chunk pairs must sit in adjacent slots");
+  static_assert(NB_OFREE < 16, "named barriers");
+  static_assert(DVP % 128 == 0 && DQK % 128 == 0, "head dims");
 };
 
 // ----------------------------------------------------------------------------- plan
@@ -316,9 +323,9 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
       const PrefillItemInfo f = prefill_item_info(p, it);
       mbar_wait(q_empty, (it_local & 1) ^ 1, p.err, SITE_PRE_Q);
       if (lane == 0) {
-        mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQC * 128 * g * p.rows_per_tile));
-        for (int c = 0; c < C::NQC; ++c)
-          tma_load_3d_hint(q_s + c * (C::M * 128), &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
+        mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQB * 128 * g * p.rows_per_tile));
+        for (int c = 0; c < C::NQB; ++c)
+          tma_load_3d_hint(q_s + c * C::HALF, &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
       }
       const int steps = C::NPASS * f.nt;
       const int page_tok_cap = f.np * ps;
@@ -349,22 +356,29 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
             const int slot = rc % NSLOT;
             mbar_wait(&kv_empty[slot], ((rc / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
             const uint32_t dst = ring + slot * C::CHUNK;
-            const uint32_t bytes = (uint32_t)(pieces * ps * 128);
+            const uint32_t bytes = (uint32_t)(2 * pieces * ps * 128);
             const bool fix = !is_k && valid < 128;  // V rows past the sequence must be zeroed
             uint64_t* bar = fix ? aux : &kv_full[slot];
             if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-            const int col = is_k ? c * 128 : (pass * C::DVP + c * 64) * 2;
+            // the chunk's two 64-dim blocks: bytes of dims [128 c, 128 c + 128) of the row
+            const int col = is_k ? c * 256 : (pass * C::DVP + c * 128) * 2;
             for (int pc = 0; pc < pieces; ++pc) {
               const int page = __shfl_sync(0xffffffffu, my_page, pc);
               if (lane == 0)
-                tma_load_3d_hint(dst + pc * ps * 128, is_k ? &tm_k : &tm_v, col, f.kvh * ps, page, bar, pol_kv);
+                for (int h = 0; h < 2; ++h)
+                  tma_load_3d_hint(dst + h * C::HALF + pc * ps * 128, is_k ? &tm_k : &tm_v, col + h * 128, f.kvh * ps,
+                                   page, bar, pol_kv);
             }
             if (fix) {
               mbar_wait(aux, aux_phase, p.err, SITE_PRE_DEQ);
               aux_phase ^= 1;
               uint8_t* sp = smem + C::OFF_RING + slot * C::CHUNK;
-              for (int i = lane; i < (128 - valid) * 8; i += 32)
-                *reinterpret_cast<uint4*>(sp + (valid + (i >> 3)) * 128 + (i & 7) * 16) = make_uint4(0, 0, 0, 0);
+              const int nz = (128 - valid) * 8;  // 16-byte pieces per block
+              for (int i = lane; i < 2 * nz; i += 32) {
+                const int h = i >= nz, k = i - h * nz;
+                *reinterpret_cast<uint4*>(sp + h * C::HALF + (valid + (k >> 3)) * 128 + (k & 7) * 16) =
+                    make_uint4(0, 0, 0, 0);
+              }
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) mbar_arrive(&kv_full[slot]);
@@ -401,9 +415,9 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
         const PrefillItemInfo f = prefill_item_info(p, it);
         mbar_wait(q_empty, (it_local & 1) ^ 1, p.err, SITE_PRE_Q);
         if (lane == 0) {
-          mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQC * 128 * g * p.rows_per_tile));
-          for (int c = 0; c < C::NQC; ++c)
-            tma_load_3d_hint(q_s + c * (C::M * 128), &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
+          mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQB * 128 * g * p.rows_per_tile));
+          for (int c = 0; c < C::NQB; ++c)
+            tma_load_3d_hint(q_s + c * C::HALF, &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
         }
         const int steps = C::NPASS * f.nt;
         const int page_tok_cap = f.np * ps;
@@ -438,7 +452,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
               }
               ++nsf;
             }
-            const int nch = is_k ? C::NQC : C::NVC;
+            const int nch = is_k ? C::NQS : C::NVS;  // staged 64-dim halves
             for (int c = 0; c < nch; ++c, ++n) {
               const int stage = n % C::NSTG;
               mbar_wait(&stg_empty[stage], ((n / C::NSTG) & 1) ^ 1, p.err, SITE_PRE_STG);
@@ -473,7 +487,8 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
   } else if (warp >= 8) {
     if constexpr (C::QUANT) {
       // ---------------------------------------------------------- converters (warps 8-11)
-      // Thread t owns key t of each staged chunk: it converts the chunk's packed values
+      // Staged halves come in pairs, the two 64-dim blocks of one ring slot.  Thread t owns
+      // key t of each staged half: it converts the half's packed values
       // exactly (e4m3 and e2m1 x e4m3 are exact in f16 and in bf16; the per-tensor / global
       // scales are applied to the scores and the output instead) and writes them in the
       // 128B-swizzled layout the MMAs read: K as bf16 (the type of q), V as f16 (P is written
@@ -494,10 +509,11 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
         const int si = C::NSF > 0 ? nsf % (C::NSF > 0 ? C::NSF : 1) : 0;
         if constexpr (KVT == KV_NVFP4)
           if (d.y & FL_FIRST) mbar_wait(&sf_full[si], (nsf / C::NSF) & 1, p.err, SITE_PRE_SF);
-        const int slot = j % NSLOT;
-        mbar_wait(&kv_empty[slot], ((j / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
+        const uint32_t rj = j >> 1, half = j & 1;  // ring chunk and block
+        const int slot = rj % NSLOT;
+        if (half == 0) mbar_wait(&kv_empty[slot], ((rj / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
         __syncwarp();
-        uint8_t* sp = smem + C::OFF_RING + slot * C::CHUNK;
+        uint8_t* sp = smem + C::OFF_RING + slot * C::CHUNK + half * C::HALF;
         const bool ok = t < d.x;
         uint4 raw[RAW16];
 #pragma unroll
@@ -538,7 +554,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&kv_full[slot]);
+          if (half == 1) mbar_arrive(&kv_full[slot]);
           mbar_arrive(&stg_empty[stage]);
           if (KVT == KV_NVFP4 && (d.y & FL_LAST)) mbar_arrive(&sf_empty[si]);
         }
@@ -546,94 +562,97 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
       }
       (void)FL_FIRST;
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // The whole warp walks the schedule and polls the barriers; lane 0 issues every MMA and
-    // commit (a commit tracks the MMAs of the thread that issues it).  Polling from a
-    // single diverged lane cost the issue loop about half of its MMA rate (measured).
-    {
-      constexpr uint32_t ID_QK = idesc_f16<true>(128, 128, false);
-      // quantised KV: P and V in f16
-      constexpr uint32_t ID_PV = idesc_f16<!C::QUANT>(128, 128, true);
-      const bool leader = lane == 0;
-      // steps issued so far (QK into S buffer n_qk & 1; PV reads P of step n_pv from buffer
-      // n_pv & 1) and passes finished.  QK of step j + 2 reuses the buffer of step j, where
-      // PV of step j reads P: it waits for that PV to complete (an MMA that reads its A
-      // operand from TMEM is not ordered against a later MMA writing the same columns).
-      // Steps are issued in pairs, QK QK PV PV, so that another MMA group is always queued
-      // behind the PV being waited for and the pipe never drains.  One barrier per buffer:
-      // the next PV on a buffer follows the QK that waits on it, so a barrier is never two
-      // phases ahead of its waiter.
-      uint32_t rc = 0, n_qk = 0, n_pv = 0, n_pass = 0;
-      int it_local = 0;
-      auto issue_qk = [&]() {
-        const uint32_t s_col = C::TM_S + 128 * (n_qk & 1);
-        if (n_qk >= 2) mbar_wait(&pv_done[n_qk & 1], ((n_qk - 2) >> 1) & 1, p.err, SITE_PRE_O_DONE);
-        for (int c = 0; c < C::NQC; ++c, ++rc) {
-          const int slot = rc % NSLOT;
-          mbar_wait(&kv_full[slot], (rc / NSLOT) & 1, p.err, SITE_PRE_KV_FULL);
-          __syncwarp();
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------- MMA issuer (1) and gate (2)
+    // Both warps walk the same schedule.  The gate polls the mbarriers; the MMA warp waits
+    // on a named barrier the gate meets once its poll succeeded, and lane 0 issues the
+    // MMAs and commits (a commit tracks the MMAs of the thread that issues it).  A shared
+    // memory poll from the issuing warp stalls the tensor pipe for hundreds of cycles
+    // while it reads its operands from shared memory; a named barrier does not touch it.
+    // Both sides use bar.sync, so the gate never runs more than one barrier ahead.
+    const bool gate = warp == 2;
+    const bool leader = warp == 1 && lane == 0;
+    constexpr uint32_t ID_QK = idesc_f16<true>(128, 128, false);
+    // quantised KV: P and V in f16
+    constexpr uint32_t ID_PV = idesc_f16<!C::QUANT>(128, 128, true);
+    // one synchronisation point of the schedule: the gate waits for the phase, then both
+    // warps meet at named barrier `id`
+    auto point = [&](int id, uint64_t* bar, uint32_t parity, int site) {
+      if (gate) mbar_wait(bar, parity, p.err, site);
+      named_bar_sync(id, 64);
+    };
+    // steps issued so far (QK into S buffer n_qk & 1; PV reads P of step n_pv from buffer
+    // n_pv & 1) and passes finished.  QK of step j + 2 reuses the buffer of step j, where
+    // PV of step j reads P: it waits for that PV to complete (an MMA that reads its A
+    // operand from TMEM is not ordered against a later MMA writing the same columns).
+    // Steps are issued in pairs, QK QK PV PV, so that another MMA group is always queued
+    // behind the PV being waited for and the pipe never drains.  One mbarrier per buffer:
+    // the next PV on a buffer follows the QK that waits on it, so a barrier is never two
+    // phases ahead of its waiter.
+    uint32_t rc = 0, n_qk = 0, n_pv = 0, n_pass = 0;
+    int it_local = 0;
+    auto issue_qk = [&]() {
+      const uint32_t s_col = C::TM_S + 128 * (n_qk & 1);
+      if (n_qk >= 2) point(C::NB_PV + (n_qk & 1), &pv_done[n_qk & 1], ((n_qk - 2) >> 1) & 1, SITE_PRE_O_DONE);
+      for (int c = 0; c < C::NQC; ++c, ++rc) {
+        const int slot = rc % NSLOT;
+        point(C::NB_SLOT + slot, &kv_full[slot], (rc / NSLOT) & 1, SITE_PRE_KV_FULL);
+        if (warp == 1) {
           tc_fence_after();
           if (leader) {
-            const uint32_t a = q_s + c * (C::M * 128), bsm = ring + slot * C::CHUNK;
+            const uint32_t bsm = ring + slot * C::CHUNK;
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc_mma_ss(tbase + s_col, desc_kmajor_sw128(a + kk * 32), desc_kmajor_sw128(bsm + kk * 32), ID_QK,
-                        (c | kk) != 0);
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                tc_mma_ss(tbase + s_col, desc_kmajor_sw128(q_s + (2 * c + h) * C::HALF + kk * 32),
+                          desc_kmajor_sw128(bsm + h * C::HALF + kk * 32), ID_QK, (c | h | kk) != 0);
             tc_commit(&kv_empty[slot]);
           }
-          __syncwarp();
         }
-        if (leader) tc_commit(&s_full[n_qk & 1]);
-        __syncwarp();
-        ++n_qk;
-      };
-      auto issue_pv = [&](bool first_of_pass) {
-        mbar_wait(&p_full[n_pv & 1], (n_pv >> 1) & 1, p.err, SITE_PRE_P_FULL);
-        const uint32_t p_col = C::TM_S + 128 * (n_pv & 1);
-        if (first_of_pass && n_pass > 0) mbar_wait(o_free, (n_pass - 1) & 1, p.err, SITE_PRE_O_DONE);
-        // one N=128 MMA per 16 keys covers two adjacent V chunks (128 output columns)
-        for (int c = 0; c < C::NVC; c += 2, rc += 2) {
-          const int slot = rc % NSLOT;
-          mbar_wait(&kv_full[slot], (rc / NSLOT) & 1, p.err, SITE_PRE_KV_FULL);
-          mbar_wait(&kv_full[slot + 1], ((rc + 1) / NSLOT) & 1, p.err, SITE_PRE_KV_FULL);
-          __syncwarp();
+      }
+      if (leader) tc_commit(&s_full[n_qk & 1]);
+      ++n_qk;
+    };
+    auto issue_pv = [&](bool first_of_pass) {
+      point(C::NB_P + (n_pv & 1), &p_full[n_pv & 1], (n_pv >> 1) & 1, SITE_PRE_P_FULL);
+      const uint32_t p_col = C::TM_S + 128 * (n_pv & 1);
+      if (first_of_pass && n_pass > 0) point(C::NB_OFREE, o_free, (n_pass - 1) & 1, SITE_PRE_O_DONE);
+      // one N=128 MMA per 16 keys covers the chunk's 128 output columns
+      for (int c = 0; c < C::NVC; ++c, ++rc) {
+        const int slot = rc % NSLOT;
+        point(C::NB_SLOT + slot, &kv_full[slot], (rc / NSLOT) & 1, SITE_PRE_KV_FULL);
+        if (warp == 1) {
           tc_fence_after();
           if (leader) {
             const uint32_t bsm = ring + slot * C::CHUNK;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              tc_mma_ts(tbase + C::TM_O + c * 64, tbase + p_col + kk * 8,
-                        desc_mnmajor_sw128(bsm + kk * 2048, C::CHUNK), ID_PV, (!first_of_pass) || kk > 0);
+              tc_mma_ts(tbase + C::TM_O + c * 128, tbase + p_col + kk * 8, desc_mnmajor_sw128(bsm + kk * 2048, C::HALF),
+                        ID_PV, (!first_of_pass) || kk > 0);
             tc_commit(&kv_empty[slot]);
-            tc_commit(&kv_empty[slot + 1]);
           }
-          __syncwarp();
         }
-        if (leader) tc_commit(&pv_done[n_pv & 1]);
-        __syncwarp();
-        ++n_pv;
-        if (first_of_pass) ++n_pass;
-      };
-      for (int r = 0;; ++r, ++it_local) {
-        const int it = prefill_item_at(r);
-        if (it >= n_items) break;
-        const PrefillItemInfo f = prefill_item_info(p, it);
-        const int steps = C::NPASS * f.nt;
-        mbar_wait(q_full, it_local & 1, p.err, SITE_PRE_Q);
-        // the S of the second step of a pair is computed while the softmax of the first
-        // runs, and the PVs of the pair while the softmax of the second finishes
-        for (int k = 0; k < steps; k += 2) {
-          const bool two = k + 1 < steps;
-          issue_qk();
-          if (two) issue_qk();
-          if (k + (two ? 1 : 0) == steps - 1) {  // the item's last QK: Q may be replaced
-            if (leader) tc_commit(q_empty);
-            __syncwarp();
-          }
-          issue_pv(k % f.nt == 0);
-          if (two) issue_pv((k + 1) % f.nt == 0);
-        }
+      }
+      if (leader) tc_commit(&pv_done[n_pv & 1]);
+      ++n_pv;
+      if (first_of_pass) ++n_pass;
+    };
+    for (int r = 0;; ++r, ++it_local) {
+      const int it = prefill_item_at(r);
+      if (it >= n_items) break;
+      const PrefillItemInfo f = prefill_item_info(p, it);
+      const int steps = C::NPASS * f.nt;
+      point(C::NB_Q, q_full, it_local & 1, SITE_PRE_Q);
+      // the S of the second step of a pair is computed while the softmax of the first
+      // runs, and the PVs of the pair while the softmax of the second finishes
+      for (int k = 0; k < steps; k += 2) {
+        const bool two = k + 1 < steps;
+        issue_qk();
+        if (two) issue_qk();
+        if (leader && k + (two ? 1 : 0) == steps - 1) tc_commit(q_empty);  // the item's last QK
+        issue_pv(k % f.nt == 0);
+        if (two) issue_pv((k + 1) % f.nt == 0);
       }
     }
   } else if (warp >= 4 && warp < 8) {
