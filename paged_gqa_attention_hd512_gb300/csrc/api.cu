@@ -53,6 +53,7 @@ struct Workspace {
 Workspace g_ws[kMaxDevices];
 constexpr size_t kErrOffset = 0;      // int error word
 constexpr size_t kFixedBytes = 256;   // error word region
+constexpr int kReuseTiles = 64;       // prefill P reuse: items of up to 64 KV tiles (8192 keys)
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -386,6 +387,11 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   const size_t o_hdr = off; off = align_up(off + 64, 256);
   const size_t o_items = off; off = align_up(off + (size_t)max_items * sizeof(PrefillItem), 256);
   const size_t o_toff = off; off = align_up(off + (size_t)(batch + 1) * sizeof(int), 256);
+  // head_dim_vo 512: per-CTA P tiles of the first pass for items of up to kReuseTiles KV
+  // tiles (longer ones recompute S in the second pass)
+  const int reuse_tiles = head_dim_vo == 512 ? kReuseTiles : 0;
+  const size_t o_pscr = off; off = align_up(off + (size_t)sms * reuse_tiles * 32768, 256);
+  const size_t o_mscr = off; off = align_up(off + (size_t)sms * reuse_tiles * 128 * sizeof(float), 256);
   char* ws = static_cast<char*>(workspace(off, &st));
   if (!ws) return st;
 
@@ -428,6 +434,9 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   p.hdr = reinterpret_cast<int*>(ws + o_hdr);
   p.items = reinterpret_cast<PrefillItem*>(ws + o_items);
   p.tile_off = reinterpret_cast<int*>(ws + o_toff);
+  p.p_scratch = reinterpret_cast<uint8_t*>(ws + o_pscr);
+  p.m_scratch = reinterpret_cast<float*>(ws + o_mscr);
+  p.reuse_tiles = reuse_tiles;
   p.batch = batch;
   p.total_q = total_q;
   p.Hq = num_qo_heads;

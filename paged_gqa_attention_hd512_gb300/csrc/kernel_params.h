@@ -78,6 +78,13 @@ struct PrefillParams {
   int* hdr;  // [0] number of items
   PrefillItem* items;
   int* tile_off;  // [batch + 1] first tile of each sequence
+  // head_dim_vo 512: P tiles of the first pass ([128 rows][128 keys] bf16, in the MMA's
+  // shared-memory image) and the softmax base of each row, per CTA, so that the second
+  // pass reuses P instead of recomputing S; items with more than reuse_tiles KV tiles
+  // recompute.
+  uint8_t* p_scratch;   // [grid][reuse_tiles][32 KB]
+  float* m_scratch;     // [grid][reuse_tiles][128]
+  int reuse_tiles;
   int batch, total_q, Hq, Hkv, group, page_size, window_left, causal, num_pages;
   int rows_per_tile;  // query positions per 128-row tile (128 / group)
   int max_items;

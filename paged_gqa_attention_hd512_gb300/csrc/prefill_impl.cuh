@@ -68,11 +68,15 @@ struct PrefillCfg {
   static constexpr int OFF_SF = OFF_STG + NSTG * STG_BYTES;
   static constexpr int OFF_DESC = OFF_SF + NSF * SF_BYTES;  // int2 per staging slot: valid keys, flags
   static constexpr int OFF_BAR = OFF_DESC + NSTG * 8;
-  // barriers: q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_free, aux, kv_full[],
-  // kv_empty[], stg_full[], stg_empty[], sf_full[], sf_empty[].  Every waiter of a barrier
-  // is at most one phase behind or ahead of it (a parity wait cannot tell more apart):
-  // hence one s_full / p_full / pv_done per S buffer.
-  static constexpr int NBAR = 10 + 2 * NSLOT + 2 * NSTG + 2 * NSF;
+  // head_dim_vo 512 with P reuse: the second pass reads the first pass's P tiles into
+  // NPS slots of the Q region (Q is not needed by then)
+  static constexpr int NPS = NPASS == 2 ? Q_BYTES / CHUNK : 0;
+  // barriers: q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_free, aux, sfree[2],
+  // ps_done, kv_full[], kv_empty[], stg_full[], stg_empty[], sf_full[], sf_empty[],
+  // pslot_full[], pslot_empty[].  Every waiter of a barrier is at most one phase behind or
+  // ahead of it (a parity wait cannot tell more apart): hence one s_full / p_full /
+  // pv_done / sfree per S buffer.
+  static constexpr int NBAR = 13 + 2 * NSLOT + 2 * NSTG + 2 * NSF + 2 * NPS;
   static constexpr int BYTES = OFF_BAR + NBAR * 8 + 16;
   static constexpr int ALLOC = BYTES + 1024;
   // TMEM columns: two S buffers of 128 keys (step j uses buffer j & 1; its P, 128 keys of
@@ -80,12 +84,13 @@ struct PrefillCfg {
   static constexpr uint32_t TM_S = 0, TM_O = 256;
   // Named (hardware) barriers between the gate warp and the MMA warp, 64 threads each:
   // one per ring slot, per S buffer for P and for PV completion, Q tile, O free.
-  static constexpr int NB_SLOT = 1, NB_P = NB_SLOT + NSLOT, NB_PV = NB_P + 2, NB_Q = NB_PV + 2,
-                       NB_OFREE = NB_Q + 1;
+  static constexpr int NB_SLOT = 1, NB_P = NB_SLOT + NSLOT, NB_SFREE = NB_P + 2, NB_Q = NB_SFREE + 2,
+                       NB_OFREE = NB_Q + 1, NB_PSLOT = NB_OFREE + 1;
   static_assert(NSLOT >= 2, "KV ring too shallow");
   static_assert(!QUANT || NSTG >= 3, "staging ring too shallow");
   static_assert(ALLOC <= 232448, "shared memory");
-  static_assert(NB_OFREE < 16, "named barriers");
+  static_assert(NB_PSLOT + NPS <= 16, "named barriers");
+  static_assert(NPASS == 1 || NPS >= 2, "P slots");
   static_assert(DVP % 128 == 0 && DQK % 128 == 0, "head dims");
 };
 
@@ -265,12 +270,16 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
   uint64_t* pv_done = bars + 6;  // [2]: PV of step j (which reads buffer j & 1) complete
   uint64_t* o_free = bars + 8;
   uint64_t* aux = bars + 9;
-  uint64_t* kv_full = bars + 10;
-  uint64_t* kv_empty = bars + 10 + NSLOT;
-  uint64_t* stg_full = bars + 10 + 2 * NSLOT;
+  uint64_t* sfree = bars + 10;    // [2]: the PV that read P from S buffer b is complete
+  uint64_t* ps_done = bars + 12;  // the first pass's P tiles of an item are in global memory
+  uint64_t* kv_full = bars + 13;
+  uint64_t* kv_empty = bars + 13 + NSLOT;
+  uint64_t* stg_full = bars + 13 + 2 * NSLOT;
   uint64_t* stg_empty = stg_full + C::NSTG;
   uint64_t* sf_full = stg_empty + C::NSTG;
   uint64_t* sf_empty = sf_full + C::NSF;
+  uint64_t* pslot_full = sf_empty + C::NSF;
+  uint64_t* pslot_empty = pslot_full + C::NPS;
   int2* stg_desc = reinterpret_cast<int2*>(smem + C::OFF_DESC);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
 
@@ -282,6 +291,12 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
       mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], 4);
       mbar_init(&pv_done[b], 1);
+      mbar_init(&sfree[b], 1);
+    }
+    mbar_init(ps_done, 4);
+    for (int s = 0; s < C::NPS; ++s) {
+      mbar_init(&pslot_full[s], 1);
+      mbar_init(&pslot_empty[s], 1);
     }
     mbar_init(o_free, 4);
     mbar_init(aux, 1);
@@ -306,6 +321,9 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
   const uint32_t tbase = *tmem_slot;
   const int n_items = min(p.hdr[0], p.max_items);
   const int ps = p.page_size, g = p.group;
+  // head_dim_vo 512 (bf16 KV): the second pass reads P of the first from global scratch
+  // instead of recomputing S, for items whose KV range fits the scratch
+  auto item_reuse = [&](const PrefillItemInfo& f) { return C::NPASS == 2 && !C::QUANT && f.nt <= p.reuse_tiles; };
 
   if (warp == 0 && KVT == KV_BF16) {
     // ------------------------------------------------------------ producer (whole warp)
@@ -314,79 +332,101 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
     }
-    uint32_t rc = 0, aux_phase = 0;
-    int it_local = 0;
+    uint32_t rc = 0, aux_phase = 0, qe = 0, psd = 0, np = 0;
     const uint64_t pol_kv = l2_policy_evict_last(), pol_q = l2_policy_evict_first();
-    for (int r = 0;; ++r, ++it_local) {
+    for (int r = 0;; ++r) {
       const int it = prefill_item_at(r);
       if (it >= n_items) break;
       const PrefillItemInfo f = prefill_item_info(p, it);
-      mbar_wait(q_empty, (it_local & 1) ^ 1, p.err, SITE_PRE_Q);
+      const bool reuse = item_reuse(f);
+      mbar_wait(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQB * 128 * g * p.rows_per_tile));
         for (int c = 0; c < C::NQB; ++c)
           tma_load_3d_hint(q_s + c * C::HALF, &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
       }
-      const int steps = C::NPASS * f.nt;
+      // steps that compute S: both passes, or only the first when the second reuses P
+      const int steps = reuse ? f.nt : C::NPASS * f.nt;
       const int page_tok_cap = f.np * ps;
       // page ids of a step's KV tile, one per lane (lane < pieces); loaded a few steps
       // ahead so the producer never waits on them
       auto step_pages = [&](int st) -> int {
-        if (st < 0 || st >= steps) return 0;
+        if (st < 0 || st >= C::NPASS * f.nt) return 0;
         const int key0 = (f.jlo + st % f.nt) * 128;
         const int pieces = max(0, min(128, page_tok_cap - key0)) / ps;
         return (lane < pieces) ? __ldg(p.kv_indices + f.ip0 + key0 / ps + lane) : 0;
+      };
+      // the K or V chunks of step st into the ring
+      auto emit = [&](bool is_k, int st, int my_page) {
+        const int pass = st / f.nt, jt = st % f.nt;
+        const int key0 = (f.jlo + jt) * 128;
+        const int valid = max(0, min(128, f.kv_len - key0));
+        const int load_rows = max(0, min(128, page_tok_cap - key0));
+        const int pieces = load_rows / ps;
+        const int nch = is_k ? C::NQC : C::NVC;
+        for (int c = 0; c < nch; ++c, ++rc) {
+          const int slot = rc % NSLOT;
+          mbar_wait(&kv_empty[slot], ((rc / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
+          const uint32_t dst = ring + slot * C::CHUNK;
+          const uint32_t bytes = (uint32_t)(2 * pieces * ps * 128);
+          const bool fix = !is_k && valid < 128;  // V rows past the sequence must be zeroed
+          uint64_t* bar = fix ? aux : &kv_full[slot];
+          if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+          // the chunk's two 64-dim blocks: bytes of dims [128 c, 128 c + 128) of the row
+          const int col = is_k ? c * 256 : (pass * C::DVP + c * 128) * 2;
+          for (int pc = 0; pc < pieces; ++pc) {
+            const int page = __shfl_sync(0xffffffffu, my_page, pc);
+            if (lane == 0)
+              for (int h = 0; h < 2; ++h)
+                tma_load_3d_hint(dst + h * C::HALF + pc * ps * 128, is_k ? &tm_k : &tm_v, col + h * 128, f.kvh * ps,
+                                 page, bar, pol_kv);
+          }
+          if (fix) {
+            mbar_wait(aux, aux_phase, p.err, SITE_PRE_DEQ);
+            aux_phase ^= 1;
+            uint8_t* sp = smem + C::OFF_RING + slot * C::CHUNK;
+            const int nz = (128 - valid) * 8;  // 16-byte pieces per block
+            for (int i = lane; i < 2 * nz; i += 32) {
+              const int h = i >= nz, k = i - h * nz;
+              *reinterpret_cast<uint4*>(sp + h * C::HALF + (valid + (k >> 3)) * 128 + (k & 7) * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&kv_full[slot]);
+          }
+        }
       };
       int pg_a = step_pages(0), pg_b = step_pages(1);
       // chunks in the MMA thread's order: steps in pairs, K of both, then V of both
       for (int k = 0; k < steps; k += 2) {
         const int pg_c = step_pages(k + 2), pg_d = step_pages(k + 3);
         for (int part = 0; part < 4; ++part) {
-          const bool is_k = part < 2;
           const int st = k + (part & 1);
-          if (st >= steps) continue;
-          const int pass = st / f.nt, jt = st % f.nt;
-          const int key0 = (f.jlo + jt) * 128;
-          const int valid = max(0, min(128, f.kv_len - key0));
-          const int load_rows = max(0, min(128, page_tok_cap - key0));
-          const int pieces = load_rows / ps;
-          const int my_page = (part & 1) ? pg_b : pg_a;
-          const int nch = is_k ? C::NQC : C::NVC;
-          for (int c = 0; c < nch; ++c, ++rc) {
-            const int slot = rc % NSLOT;
-            mbar_wait(&kv_empty[slot], ((rc / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
-            const uint32_t dst = ring + slot * C::CHUNK;
-            const uint32_t bytes = (uint32_t)(2 * pieces * ps * 128);
-            const bool fix = !is_k && valid < 128;  // V rows past the sequence must be zeroed
-            uint64_t* bar = fix ? aux : &kv_full[slot];
-            if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
-            // the chunk's two 64-dim blocks: bytes of dims [128 c, 128 c + 128) of the row
-            const int col = is_k ? c * 256 : (pass * C::DVP + c * 128) * 2;
-            for (int pc = 0; pc < pieces; ++pc) {
-              const int page = __shfl_sync(0xffffffffu, my_page, pc);
-              if (lane == 0)
-                for (int h = 0; h < 2; ++h)
-                  tma_load_3d_hint(dst + h * C::HALF + pc * ps * 128, is_k ? &tm_k : &tm_v, col + h * 128, f.kvh * ps,
-                                   page, bar, pol_kv);
-            }
-            if (fix) {
-              mbar_wait(aux, aux_phase, p.err, SITE_PRE_DEQ);
-              aux_phase ^= 1;
-              uint8_t* sp = smem + C::OFF_RING + slot * C::CHUNK;
-              const int nz = (128 - valid) * 8;  // 16-byte pieces per block
-              for (int i = lane; i < 2 * nz; i += 32) {
-                const int h = i >= nz, k = i - h * nz;
-                *reinterpret_cast<uint4*>(sp + h * C::HALF + (valid + (k >> 3)) * 128 + (k & 7) * 16) =
-                    make_uint4(0, 0, 0, 0);
-              }
-              fence_proxy_async_smem();
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&kv_full[slot]);
-            }
-          }
+          if (st < steps) emit(part < 2, st, (part & 1) ? pg_b : pg_a);
         }
         pg_a = pg_c;
         pg_b = pg_d;
+      }
+      if (reuse) {
+        // second pass: P tile j of the first pass (into a P slot of the Q region, free once
+        // the last QK of the item is done) and V of the upper output half
+        mbar_wait(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
+        mbar_wait(ps_done, psd++ & 1, p.err, SITE_PRE_P_FULL);
+        const uint8_t* pscr = p.p_scratch + (size_t)blockIdx.x * p.reuse_tiles * C::CHUNK;
+        int pg = step_pages(f.nt);
+        for (int j = 0; j < f.nt; ++j, ++np) {
+          const int pg_n = step_pages(f.nt + j + 1);
+          constexpr int NPS = C::NPS > 0 ? C::NPS : 1;
+          const int s = np % NPS;
+          mbar_wait(&pslot_empty[s], ((np / NPS) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&pslot_full[s], (uint32_t)C::CHUNK);
+            bulk_load_g2s(q_s + s * C::CHUNK, pscr + (size_t)j * C::CHUNK, (uint32_t)C::CHUNK, &pslot_full[s]);
+          }
+          emit(false, f.nt + j, pg);
+          pg = pg_n;
+        }
       }
     }
   } else if (warp == 0) {
@@ -589,11 +629,14 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     // behind the PV being waited for and the pipe never drains.  One mbarrier per buffer:
     // the next PV on a buffer follows the QK that waits on it, so a barrier is never two
     // phases ahead of its waiter.
-    uint32_t rc = 0, n_qk = 0, n_pv = 0, n_pass = 0;
+    // n_spv counts the PVs that read P from an S buffer (their order is the QKs' order);
+    // n_pv counts all PVs, including those of a second pass that reads P from shared
+    // memory; np counts P slots.
+    uint32_t rc = 0, n_qk = 0, n_spv = 0, n_pv = 0, n_pass = 0, np = 0;
     int it_local = 0;
     auto issue_qk = [&]() {
       const uint32_t s_col = C::TM_S + 128 * (n_qk & 1);
-      if (n_qk >= 2) point(C::NB_PV + (n_qk & 1), &pv_done[n_qk & 1], ((n_qk - 2) >> 1) & 1, SITE_PRE_O_DONE);
+      if (n_qk >= 2) point(C::NB_SFREE + (n_qk & 1), &sfree[n_qk & 1], ((n_qk - 2) >> 1) & 1, SITE_PRE_O_DONE);
       for (int c = 0; c < C::NQC; ++c, ++rc) {
         const int slot = rc % NSLOT;
         point(C::NB_SLOT + slot, &kv_full[slot], (rc / NSLOT) & 1, SITE_PRE_KV_FULL);
@@ -616,7 +659,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     };
     auto issue_pv = [&](bool first_of_pass) {
       point(C::NB_P + (n_pv & 1), &p_full[n_pv & 1], (n_pv >> 1) & 1, SITE_PRE_P_FULL);
-      const uint32_t p_col = C::TM_S + 128 * (n_pv & 1);
+      const uint32_t p_col = C::TM_S + 128 * (n_spv & 1);
       if (first_of_pass && n_pass > 0) point(C::NB_OFREE, o_free, (n_pass - 1) & 1, SITE_PRE_O_DONE);
       // one N=128 MMA per 16 keys covers the chunk's 128 output columns
       for (int c = 0; c < C::NVC; ++c, ++rc) {
@@ -634,15 +677,50 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
           }
         }
       }
-      if (leader) tc_commit(&pv_done[n_pv & 1]);
+      if (leader) {
+        tc_commit(&sfree[n_spv & 1]);
+        tc_commit(&pv_done[n_pv & 1]);
+      }
+      ++n_spv;
       ++n_pv;
       if (first_of_pass) ++n_pass;
+    };
+    // second pass with P reuse: P tile j from a P slot (shared memory) times V
+    auto issue_pv_reuse = [&](int j) {
+      point(C::NB_P + (n_pv & 1), &p_full[n_pv & 1], (n_pv >> 1) & 1, SITE_PRE_P_FULL);
+      if (j == 0) point(C::NB_OFREE, o_free, (n_pass - 1) & 1, SITE_PRE_O_DONE);
+      constexpr int NPS = C::NPS > 0 ? C::NPS : 1;
+      const int s = np % NPS;
+      point(C::NB_PSLOT + s, &pslot_full[s], (np / NPS) & 1, SITE_PRE_KV_FULL);
+      for (int c = 0; c < C::NVC; ++c, ++rc) {
+        const int slot = rc % NSLOT;
+        point(C::NB_SLOT + slot, &kv_full[slot], (rc / NSLOT) & 1, SITE_PRE_KV_FULL);
+        if (warp == 1) {
+          tc_fence_after();
+          if (leader) {
+            const uint32_t bsm = ring + slot * C::CHUNK, psm = q_s + s * C::CHUNK;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              tc_mma_ss(tbase + C::TM_O + c * 128, desc_kmajor_sw128(psm + (kk >> 2) * C::HALF + (kk & 3) * 32),
+                        desc_mnmajor_sw128(bsm + kk * 2048, C::HALF), ID_PV, (j > 0) || kk > 0);
+            tc_commit(&kv_empty[slot]);
+          }
+        }
+      }
+      if (leader) {
+        tc_commit(&pslot_empty[s]);
+        tc_commit(&pv_done[n_pv & 1]);
+      }
+      ++n_pv;
+      ++np;
+      if (j == 0) ++n_pass;
     };
     for (int r = 0;; ++r, ++it_local) {
       const int it = prefill_item_at(r);
       if (it >= n_items) break;
       const PrefillItemInfo f = prefill_item_info(p, it);
-      const int steps = C::NPASS * f.nt;
+      const bool reuse = item_reuse(f);
+      const int steps = reuse ? f.nt : C::NPASS * f.nt;
       point(C::NB_Q, q_full, it_local & 1, SITE_PRE_Q);
       // the S of the second step of a pair is computed while the softmax of the first
       // runs, and the PVs of the pair while the softmax of the second finishes
@@ -654,6 +732,10 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
         issue_pv(k % f.nt == 0);
         if (two) issue_pv((k + 1) % f.nt == 0);
       }
+      if (reuse) {
+        for (int j = 0; j < f.nt; ++j) issue_pv_reuse(j);
+        if (leader) tc_commit(q_empty);  // the P slots (Q region) are free
+      }
     }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax + epilogue
@@ -662,22 +744,56 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     // FP8 per-tensor / NVFP4 global K scale folds into the scores, the V scale into the output
     const float scale_log2 = p.sm_scale * 1.4426950408889634f * (KVT == KV_BF16 ? 1.f : __ldg(p.k_scale));
     const float v_scale = KVT == KV_BF16 ? 1.f : __ldg(p.v_scale);
-    uint32_t gstep = 0;
+    // gstep counts PV steps (both passes), sstep the steps that read an S buffer
+    uint32_t gstep = 0, sstep = 0;
+    uint8_t* pscr = p.p_scratch + (size_t)blockIdx.x * p.reuse_tiles * C::CHUNK;
+    float* mscr = p.m_scratch + (size_t)blockIdx.x * p.reuse_tiles * 128;
     for (int r = 0;; ++r) {
       const int it = prefill_item_at(r);
       if (it >= n_items) break;
       const PrefillItemInfo f = prefill_item_info(p, it);
+      const bool reuse = item_reuse(f);
       const int p_local = row / g, h_local = row % g;
       const bool row_ok = (row < g * p.rows_per_tile) && (p_local < f.n_pos);
       const int pos = f.pos0 + p_local;
       const int khi = p.causal ? pos : f.kv_len - 1;
       const int klo = p.window_left >= 0 ? pos - p.window_left : 0;
       const int hq = f.kvh * g + h_local;
+      float m_used = -INFINITY, l = 0.f;
       for (int pass = 0; pass < C::NPASS; ++pass) {
-        float m_used = -INFINITY, l = 0.f;
-        for (int jt = 0; jt < f.nt; ++jt, ++gstep) {
-          const uint32_t s_col = C::TM_S + 128 * (gstep & 1);
-          mbar_wait(&s_full[gstep & 1], (gstep >> 1) & 1, p.err, SITE_PRE_S_FULL);
+        if (reuse && pass == 1) {
+          // second pass reusing P: replay the first pass's O rescales, in step with the
+          // PVs; no S.  Waiting for the PV two steps back keeps every pv_done barrier
+          // within one phase of this warp's waits.
+          for (int j = 0; j < f.nt; ++j, ++gstep) {
+            if (gstep >= 2) mbar_wait(&pv_done[gstep & 1], ((gstep - 2) >> 1) & 1, p.err, SITE_PRE_O_DONE);
+            const float a = *reinterpret_cast<volatile float*>(mscr + j * 128 + row);
+            const bool resc = a != 1.f;
+            if (__any_sync(0xffffffffu, resc)) {
+              mbar_wait(&pv_done[(gstep - 1) & 1], ((gstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
+              __syncwarp();
+              tc_fence_after();
+#pragma unroll 1
+              for (int c = 0; c < C::DVP / 32; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(lane_base + C::TM_O + 32 * c, ov);
+                tc_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
+                tmem_st32(lane_base + C::TM_O + 32 * c, ov);
+              }
+              tc_wait_st();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[gstep & 1]);
+          }
+        } else {
+        m_used = -INFINITY;
+        l = 0.f;
+        for (int jt = 0; jt < f.nt; ++jt, ++gstep, ++sstep) {
+          const uint32_t s_col = C::TM_S + 128 * (sstep & 1);
+          mbar_wait(&s_full[sstep & 1], (sstep >> 1) & 1, p.err, SITE_PRE_S_FULL);
           __syncwarp();  // the tcgen05 loads below are warp-collective
           tc_fence_after();
           uint32_t sr[128];
@@ -739,12 +855,28 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
           }
           if (resc) l *= alpha;
           l += sum;
+          if (reuse) {
+            // P tile jt in the shared-memory image the second pass's MMAs read (two
+            // 128B-swizzled blocks of 64 keys), and the rescale factor applied before it
+            uint8_t* prow = pscr + (size_t)jt * C::CHUNK + row * 128;
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              *reinterpret_cast<uint4*>(prow + (q >> 3) * C::HALF + (((q & 7) ^ (row & 7)) << 4)) =
+                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            mscr[jt * 128 + row] = resc ? alpha : 1.f;
+          }
           tmem_st32(lane_base + s_col, pk);
           tmem_st32(lane_base + s_col + 32, pk + 32);
           tc_wait_st();
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&p_full[gstep & 1]);
+        }
+        if (reuse) {  // the P tiles of this pass are in global memory for the producer
+          fence_proxy_async_global();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(ps_done);
+        }
         }
         // ---- epilogue of this pass: O / l -> bf16
         mbar_wait(&pv_done[(gstep - 1) & 1], ((gstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);

@@ -32,6 +32,9 @@ CASES = [
     (512, 512, 8, 2, 8, [600, 300], [600, 300], 1, -1),
     (512, 256, 16, 2, 64, [700], [700], 1, 200),
     (512, 512, 24, 4, 32, [900, 513], [400, 513], 1, -1),
+    # more than 64 KV tiles: the second pass recomputes S instead of reusing P
+    (512, 512, 8, 2, 64, [9000, 300], [40, 300], 1, -1),
+    (512, 512, 8, 1, 64, [8300], [20], 0, -1),
 ]
 
 
@@ -47,6 +50,17 @@ def test_prefill_parity(c):
                            kv_lens=kv, qo_lens=qo, causal=causal, window_left=win, seed=500 + len(kv))
     check_full(case, _id(c))
     assert pa.paged_attn_last_variant() == f"prefill_{dqk}x{dvo}_bf16"
+
+
+@pytest.mark.parametrize("q_gain", [8.0, 32.0])
+def test_prefill_rescale_replay(q_gain):
+    """Large scores make the running maximum jump by more than 2^8 between KV tiles, so the
+    first pass rescales O; with head_dim_vo 512 the second pass replays those rescales
+    while reusing P.  q is scaled by a power of two (exact in bf16)."""
+    case = synth.make_case("prefill", batch=2, Hq=8, Hkv=2, d_qk=512, d_vo=512, page_size=16,
+                           kv_lens=[700, 333], qo_lens=[260, 333], seed=77)
+    case.q = (case.q.float() * q_gain).to(case.q.dtype)
+    check_full(case, f"q x {q_gain}")
 
 
 def test_prefill_small_pages_are_refused():  # noqa: D103
