@@ -743,6 +743,10 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     const uint32_t lane_base = tbase + ((uint32_t)(32 * (warp - 4)) << 16);
     // FP8 per-tensor / NVFP4 global K scale folds into the scores, the V scale into the output
     const float scale_log2 = p.sm_scale * 1.4426950408889634f * (KVT == KV_BF16 ? 1.f : __ldg(p.k_scale));
+    // scores are scaled inside the exponent's FMA; a non-positive scale is applied up
+    // front instead (the maximum of the raw scores is only the scaled maximum for scale > 0)
+    const bool pos_scale = scale_log2 > 0.f;
+    const float eff_scale = pos_scale ? scale_log2 : 1.f;
     const float v_scale = KVT == KV_BF16 ? 1.f : __ldg(p.v_scale);
     // gstep counts PV steps (both passes), sstep the steps that read an S buffer
     uint32_t gstep = 0, sstep = 0;
@@ -800,20 +804,31 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + 32 * c, sr + 32 * c);
           tc_wait_ld();
-          // visible keys of this row as tile-local indices [lo, hi]: the mask is a select on
-          // two compares (short-circuit forms compiled to per-element branches), and the
-          // max / sum run as four independent chains
+          // visible keys of this row as tile-local indices [lo, hi].  Tiles every row of the
+          // warp sees in full skip the mask; otherwise it is a select on two compares
+          // (short-circuit forms compiled to per-element branches).  The maximum is taken
+          // over the raw scores (the scale is positive, or applied first when it is not) and
+          // the max / sum run as four independent chains.
           const int key0 = (f.jlo + jt) * 128;
           const int lo = klo - key0, hi = min(khi, f.kv_len - 1) - key0;
           float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          if (!pos_scale) {
 #pragma unroll
-          for (int i = 0; i < 128; ++i) {
-            const bool ok = (i >= lo) & (i <= hi);
-            const float x = ok ? __uint_as_float(sr[i]) * scale_log2 : -INFINITY;
-            sr[i] = __float_as_uint(x);
-            mx4[i & 3] = fmaxf(mx4[i & 3], x);
+            for (int i = 0; i < 128; ++i) sr[i] = __float_as_uint(__uint_as_float(sr[i]) * scale_log2);
           }
-          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+          if (__all_sync(0xffffffffu, (lo <= 0) & (hi >= 127))) {
+#pragma unroll
+            for (int i = 0; i < 128; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[i]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 128; ++i) {
+              const bool ok = (i >= lo) & (i <= hi);
+              const float x = ok ? __uint_as_float(sr[i]) : -INFINITY;
+              sr[i] = __float_as_uint(x);
+              mx4[i & 3] = fmaxf(mx4[i & 3], x);
+            }
+          }
+          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * eff_scale;
           const float m_new = fmaxf(m_used, mx);
           bool resc = false;
           float alpha = 1.f;
@@ -825,12 +840,13 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
             resc = true;
           }
           const float base = (m_used == -INFINITY) ? 0.f : m_used;
+          const float nbase = -base;
           float sum4[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t pk[64];
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
-            const float p0 = fast_exp2(__uint_as_float(sr[2 * i]) - base);
-            const float p1 = fast_exp2(__uint_as_float(sr[2 * i + 1]) - base);
+            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), eff_scale, nbase));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), eff_scale, nbase));
             sum4[i & 3] += p0 + p1;
             pk[i] = C::QUANT ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
           }
