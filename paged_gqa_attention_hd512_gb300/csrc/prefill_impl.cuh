@@ -46,8 +46,11 @@ struct PrefillCfg {
   static constexpr int Q_BYTES = NQB * HALF;
   static constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
   static constexpr bool QUANT = KVT != KV_BF16;
-  // quantised KV adds a warpgroup of converters (warps 8-11, one key row per thread)
-  static constexpr int THREADS = QUANT ? 384 : 256;
+  // warps 8-11: converters for quantised KV (one key row per thread); for bf16 KV a second
+  // softmax warpgroup, so each softmax thread handles half of its row's 128 keys
+  static constexpr int THREADS = 384;
+  static constexpr int SMW = QUANT ? 1 : 2;   // softmax warpgroups
+  static constexpr int NCOL = 128 / SMW;      // S columns per softmax thread
   // Quantised KV: warp 0 streams the packed bytes of each 64-dim half chunk ([128 keys][CW
   // bytes]) and, for NVFP4, the block scales of each K or V tile ([128 keys][D / 16 bytes])
   // into staging rings with TMA; the converters turn two staged halves into one slot of the
@@ -67,7 +70,8 @@ struct PrefillCfg {
   static constexpr int OFF_STG = Q_BYTES + NSLOT * CHUNK;
   static constexpr int OFF_SF = OFF_STG + NSTG * STG_BYTES;
   static constexpr int OFF_DESC = OFF_SF + NSF * SF_BYTES;  // int2 per staging slot: valid keys, flags
-  static constexpr int OFF_BAR = OFF_DESC + NSTG * 8;
+  static constexpr int OFF_XCH = OFF_DESC + NSTG * 8;  // [2][128] floats: partial row maxima / sums
+  static constexpr int OFF_BAR = OFF_XCH + (SMW == 2 ? 1024 : 0);
   // head_dim_vo 512 with P reuse: the second pass reads the first pass's P tiles into
   // NPS slots of the Q region (Q is not needed by then)
   static constexpr int NPS = NPASS == 2 ? Q_BYTES / CHUNK : 0;
@@ -89,7 +93,8 @@ struct PrefillCfg {
   static_assert(NSLOT >= 2, "KV ring too shallow");
   static_assert(!QUANT || NSTG >= 3, "staging ring too shallow");
   static_assert(ALLOC <= 232448, "shared memory");
-  static_assert(NB_PSLOT + NPS <= 16, "named barriers");
+  static constexpr int NB_SMX = 15;  // the two softmax warpgroups (256 threads)
+  static_assert(NB_PSLOT + NPS <= NB_SMX, "named barriers");
   static_assert(NPASS == 1 || NPS >= 2, "P slots");
   static_assert(DVP % 128 == 0 && DQK % 128 == 0, "head dims");
 };
@@ -289,16 +294,16 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     mbar_init(q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 4);
+      mbar_init(&p_full[b], 4 * C::SMW);
       mbar_init(&pv_done[b], 1);
       mbar_init(&sfree[b], 1);
     }
-    mbar_init(ps_done, 4);
+    mbar_init(ps_done, 4 * C::SMW);
     for (int s = 0; s < C::NPS; ++s) {
       mbar_init(&pslot_full[s], 1);
       mbar_init(&pslot_empty[s], 1);
     }
-    mbar_init(o_free, 4);
+    mbar_init(o_free, 4 * C::SMW);
     mbar_init(aux, 1);
     for (int s = 0; s < NSLOT; ++s) {
       mbar_init(&kv_full[s], KVT == KV_BF16 ? 1 : 4);  // quantised KV: the four converter warps arrive
@@ -524,7 +529,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
         mbar_arrive(&stg_full[stage]);
       }
     }
-  } else if (warp >= 8) {
+  } else if (C::QUANT && warp >= 8) {
     if constexpr (C::QUANT) {
       // ---------------------------------------------------------- converters (warps 8-11)
       // Staged halves come in pairs, the two 64-dim blocks of one ring slot.  Thread t owns
@@ -737,10 +742,34 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
         if (leader) tc_commit(q_empty);  // the P slots (Q region) are free
       }
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax + epilogue
-    const int row = threadIdx.x - 128;  // TMEM lane == tile row
-    const uint32_t lane_base = tbase + ((uint32_t)(32 * (warp - 4)) << 16);
+    // Thread r of a warpgroup owns row r (TMEM lane r); with two warpgroups (bf16 KV) the
+    // first handles keys [0, 64) of each tile and the upper output columns' half of the
+    // O rescales and of the epilogue is split the same way; the row maximum is combined
+    // through shared memory once per tile, the row sums at the end of a pass.
+    constexpr int NCOL = C::NCOL;
+    const int wg = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int row = 32 * quarter + lane;  // TMEM lane == tile row
+    const int col0 = wg * NCOL;           // first key of this thread's columns
+    const uint32_t lane_base = tbase + ((uint32_t)(32 * quarter) << 16);
+    float* xch = reinterpret_cast<float*>(smem + C::OFF_XCH);
+    // combine a per-row value with the other warpgroup's (max or sum)
+    auto combine = [&](float v, bool is_max) -> float {
+      if constexpr (C::SMW == 1) {
+        return v;
+      } else {
+        xch[wg * 128 + row] = v;
+        named_bar_sync(C::NB_SMX, 256);
+        const float o = xch[(wg ^ 1) * 128 + row];
+        named_bar_sync(C::NB_SMX, 256);
+        return is_max ? fmaxf(v, o) : v + o;
+      }
+    };
+    // O columns this thread rescales and writes out
+    constexpr int OCOL = C::DVP / C::SMW;
+    const int ocol0 = wg * OCOL;
     // FP8 per-tensor / NVFP4 global K scale folds into the scores, the V scale into the output
     const float scale_log2 = p.sm_scale * 1.4426950408889634f * (KVT == KV_BF16 ? 1.f : __ldg(p.k_scale));
     // scores are scaled inside the exponent's FMA; a non-positive scale is applied up
@@ -748,6 +777,18 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     const bool pos_scale = scale_log2 > 0.f;
     const float eff_scale = pos_scale ? scale_log2 : 1.f;
     const float v_scale = KVT == KV_BF16 ? 1.f : __ldg(p.v_scale);
+    auto rescale_o = [&](float a) {
+#pragma unroll 1
+      for (int c = 0; c < OCOL / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(lane_base + C::TM_O + ocol0 + 32 * c, ov);
+        tc_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
+        tmem_st32(lane_base + C::TM_O + ocol0 + 32 * c, ov);
+      }
+      tc_wait_st();
+    };
     // gstep counts PV steps (both passes), sstep the steps that read an S buffer
     uint32_t gstep = 0, sstep = 0;
     uint8_t* pscr = p.p_scratch + (size_t)blockIdx.x * p.reuse_tiles * C::CHUNK;
@@ -777,133 +818,118 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
               mbar_wait(&pv_done[(gstep - 1) & 1], ((gstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
               __syncwarp();
               tc_fence_after();
-#pragma unroll 1
-              for (int c = 0; c < C::DVP / 32; ++c) {
-                uint32_t ov[32];
-                tmem_ld32(lane_base + C::TM_O + 32 * c, ov);
-                tc_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
-                tmem_st32(lane_base + C::TM_O + 32 * c, ov);
-              }
-              tc_wait_st();
+              rescale_o(a);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[gstep & 1]);
           }
         } else {
-        m_used = -INFINITY;
-        l = 0.f;
-        for (int jt = 0; jt < f.nt; ++jt, ++gstep, ++sstep) {
-          const uint32_t s_col = C::TM_S + 128 * (sstep & 1);
-          mbar_wait(&s_full[sstep & 1], (sstep >> 1) & 1, p.err, SITE_PRE_S_FULL);
-          __syncwarp();  // the tcgen05 loads below are warp-collective
-          tc_fence_after();
-          uint32_t sr[128];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(lane_base + s_col + 32 * c, sr + 32 * c);
-          tc_wait_ld();
-          // visible keys of this row as tile-local indices [lo, hi].  Tiles every row of the
-          // warp sees in full skip the mask; otherwise it is a select on two compares
-          // (short-circuit forms compiled to per-element branches).  The maximum is taken
-          // over the raw scores (the scale is positive, or applied first when it is not) and
-          // the max / sum run as four independent chains.
-          const int key0 = (f.jlo + jt) * 128;
-          const int lo = klo - key0, hi = min(khi, f.kv_len - 1) - key0;
-          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-          if (!pos_scale) {
-#pragma unroll
-            for (int i = 0; i < 128; ++i) sr[i] = __float_as_uint(__uint_as_float(sr[i]) * scale_log2);
-          }
-          if (__all_sync(0xffffffffu, (lo <= 0) & (hi >= 127))) {
-#pragma unroll
-            for (int i = 0; i < 128; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[i]));
-          } else {
-#pragma unroll
-            for (int i = 0; i < 128; ++i) {
-              const bool ok = (i >= lo) & (i <= hi);
-              const float x = ok ? __uint_as_float(sr[i]) : -INFINITY;
-              sr[i] = __float_as_uint(x);
-              mx4[i & 3] = fmaxf(mx4[i & 3], x);
-            }
-          }
-          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * eff_scale;
-          const float m_new = fmaxf(m_used, mx);
-          bool resc = false;
-          float alpha = 1.f;
-          if (jt == 0) {
-            m_used = m_new;
-          } else if (m_new > m_used + 8.f) {  // lazy rescale: only when the max grows by > 2^8
-            alpha = fast_exp2(m_used - m_new);
-            m_used = m_new;
-            resc = true;
-          }
-          const float base = (m_used == -INFINITY) ? 0.f : m_used;
-          const float nbase = -base;
-          float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-          uint32_t pk[64];
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), eff_scale, nbase));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), eff_scale, nbase));
-            sum4[i & 3] += p0 + p1;
-            pk[i] = C::QUANT ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
-          }
-          const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-          // tcgen05.ld / st are warp-collective (.sync.aligned): the whole warp rescales when
-          // any of its rows needs it, the other rows with a factor of 1, once the PV of the
-          // previous step has finished with O
-          if (__any_sync(0xffffffffu, resc)) {
-            mbar_wait(&pv_done[(gstep - 1) & 1], ((gstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
-            __syncwarp();
+          m_used = -INFINITY;
+          l = 0.f;
+          for (int jt = 0; jt < f.nt; ++jt, ++gstep, ++sstep) {
+            const uint32_t s_col = C::TM_S + 128 * (sstep & 1);
+            mbar_wait(&s_full[sstep & 1], (sstep >> 1) & 1, p.err, SITE_PRE_S_FULL);
+            __syncwarp();  // the tcgen05 loads below are warp-collective
             tc_fence_after();
-            const float a = resc ? alpha : 1.f;
-#pragma unroll 1
-            for (int c = 0; c < C::DVP / 32; ++c) {
-              uint32_t ov[32];
-              tmem_ld32(lane_base + C::TM_O + 32 * c, ov);
-              tc_wait_ld();
+            uint32_t sr[NCOL];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
-              tmem_st32(lane_base + C::TM_O + 32 * c, ov);
+            for (int c = 0; c < NCOL / 32; ++c) tmem_ld32(lane_base + s_col + col0 + 32 * c, sr + 32 * c);
+            tc_wait_ld();
+            // visible keys of this row as indices [lo, hi] into this thread's columns.
+            // Tiles every row of the warp sees in full skip the mask; otherwise it is a
+            // select on two compares (short-circuit forms compiled to per-element
+            // branches).  The maximum is taken over the raw scores (the scale is positive,
+            // or applied first when it is not); max and sum run as four chains.
+            const int key0 = (f.jlo + jt) * 128 + col0;
+            const int lo = klo - key0, hi = min(khi, f.kv_len - 1) - key0;
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            if (!pos_scale) {
+#pragma unroll
+              for (int i = 0; i < NCOL; ++i) sr[i] = __float_as_uint(__uint_as_float(sr[i]) * scale_log2);
+            }
+            if (__all_sync(0xffffffffu, (lo <= 0) & (hi >= NCOL - 1))) {
+#pragma unroll
+              for (int i = 0; i < NCOL; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[i]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < NCOL; ++i) {
+                const bool ok = (i >= lo) & (i <= hi);
+                const float x = ok ? __uint_as_float(sr[i]) : -INFINITY;
+                sr[i] = __float_as_uint(x);
+                mx4[i & 3] = fmaxf(mx4[i & 3], x);
+              }
+            }
+            const float mx =
+                combine(fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])), true) * eff_scale;
+            const float m_new = fmaxf(m_used, mx);
+            bool resc = false;
+            float alpha = 1.f;
+            if (jt == 0) {
+              m_used = m_new;
+            } else if (m_new > m_used + 8.f) {  // lazy rescale: only when the max grows by > 2^8
+              alpha = fast_exp2(m_used - m_new);
+              m_used = m_new;
+              resc = true;
+            }
+            const float base = (m_used == -INFINITY) ? 0.f : m_used;
+            const float nbase = -base;
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pk[NCOL / 2];
+#pragma unroll
+            for (int i = 0; i < NCOL / 2; ++i) {
+              const float p0 = fast_exp2(fmaf(__uint_as_float(sr[2 * i]), eff_scale, nbase));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(sr[2 * i + 1]), eff_scale, nbase));
+              sum4[i & 3] += p0 + p1;
+              pk[i] = C::QUANT ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+            }
+            const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+            // tcgen05.ld / st are warp-collective (.sync.aligned): the whole warp rescales
+            // when any of its rows needs it, the other rows with a factor of 1, once the PV
+            // of the previous step has finished with O
+            if (__any_sync(0xffffffffu, resc)) {
+              mbar_wait(&pv_done[(gstep - 1) & 1], ((gstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
+              __syncwarp();
+              tc_fence_after();
+              rescale_o(resc ? alpha : 1.f);
+            }
+            if (resc) l *= alpha;
+            l += sum;
+#pragma unroll
+            for (int c = 0; c < NCOL / 64; ++c) tmem_st32(lane_base + s_col + col0 / 2 + 32 * c, pk + 32 * c);
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[gstep & 1]);
+            if (reuse) {
+              // after the PV may start: this thread's keys of P tile jt in the shared-memory
+              // image the second pass's MMAs read (128B-swizzled blocks of 64 keys), and the
+              // rescale factor applied before it
+              uint8_t* prow = pscr + (size_t)jt * C::CHUNK + (col0 / 64) * C::HALF + row * 128;
+#pragma unroll
+              for (int q = 0; q < NCOL / 8; ++q)
+                *reinterpret_cast<uint4*>(prow + (q >> 3) * C::HALF + (((q & 7) ^ (row & 7)) << 4)) =
+                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+              mscr[jt * 128 + row] = resc ? alpha : 1.f;
             }
           }
-          if (resc) l *= alpha;
-          l += sum;
-          if (reuse) {
-            // P tile jt in the shared-memory image the second pass's MMAs read (two
-            // 128B-swizzled blocks of 64 keys), and the rescale factor applied before it
-            uint8_t* prow = pscr + (size_t)jt * C::CHUNK + row * 128;
-#pragma unroll
-            for (int q = 0; q < 16; ++q)
-              *reinterpret_cast<uint4*>(prow + (q >> 3) * C::HALF + (((q & 7) ^ (row & 7)) << 4)) =
-                  make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            mscr[jt * 128 + row] = resc ? alpha : 1.f;
+          if (reuse) {  // the P tiles of this pass are in global memory for the producer
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(ps_done);
           }
-          tmem_st32(lane_base + s_col, pk);
-          tmem_st32(lane_base + s_col + 32, pk + 32);
-          tc_wait_st();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&p_full[gstep & 1]);
-        }
-        if (reuse) {  // the P tiles of this pass are in global memory for the producer
-          fence_proxy_async_global();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(ps_done);
-        }
         }
         // ---- epilogue of this pass: O / l -> bf16
+        const float lt = combine(l, false);
         mbar_wait(&pv_done[(gstep - 1) & 1], ((gstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
         __syncwarp();
         tc_fence_after();
-        const float inv = l > 0.f ? v_scale / l : 0.f;
-        uint16_t* orow = p.out + ((size_t)(f.q_row0 + p_local) * p.Hq + hq) * DVO + pass * C::DVP;
+        const float inv = lt > 0.f ? v_scale / lt : 0.f;
+        uint16_t* orow = p.out + ((size_t)(f.q_row0 + p_local) * p.Hq + hq) * DVO + pass * C::DVP + ocol0;
 #pragma unroll 1
-        for (int c = 0; c < C::DVP / 32; ++c) {
+        for (int c = 0; c < OCOL / 32; ++c) {
           uint32_t ov[32];
-          tmem_ld32(lane_base + C::TM_O + 32 * c, ov);
+          tmem_ld32(lane_base + C::TM_O + ocol0 + 32 * c, ov);
           tc_wait_ld();
           uint32_t pkd[16];
 #pragma unroll
@@ -919,9 +945,9 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(o_free);
-        if (pass == C::NPASS - 1 && row_ok && p.lse)
+        if (pass == C::NPASS - 1 && row_ok && p.lse && wg == 0)
           p.lse[(size_t)(f.q_row0 + p_local) * p.Hq + hq] =
-              l > 0.f ? (m_used + log2f(l)) * 0.69314718055994531f : -INFINITY;
+              lt > 0.f ? (m_used + log2f(lt)) * 0.69314718055994531f : -INFINITY;
       }
     }
   }
