@@ -905,11 +905,16 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
               // after the PV may start: this thread's keys of P tile jt in the shared-memory
               // image the second pass's MMAs read (128B-swizzled blocks of 64 keys), and the
               // rescale factor applied before it
+              // 32-byte stores: logical pieces 2k and 2k+1 of a row land in one aligned pair of
+              // physical 16-byte slots, swapped when the row's swizzle phase is odd
               uint8_t* prow = pscr + (size_t)jt * C::CHUNK + (col0 / 64) * C::HALF + row * 128;
+              const bool odd = row & 1;
 #pragma unroll
-              for (int q = 0; q < NCOL / 8; ++q)
-                *reinterpret_cast<uint4*>(prow + (q >> 3) * C::HALF + (((q & 7) ^ (row & 7)) << 4)) =
-                    make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+              for (int k = 0; k < NCOL / 16; ++k) {
+                const uint32_t* a = pk + 8 * k + (odd ? 4 : 0);
+                const uint32_t* b = pk + 8 * k + (odd ? 0 : 4);
+                st_global_v8(prow + (k >> 2) * C::HALF + (((k & 3) ^ ((row & 7) >> 1)) << 5), a, b);
+              }
               mscr[jt * 128 + row] = resc ? alpha : 1.f;
             }
           }
