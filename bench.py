@@ -285,7 +285,7 @@ def bench_decode(name, steps, warmup, barrier, gpu_index, pk, with_e2e=True, wit
         res["e2e"] = decode_e2e(c, kw, max(3, min(steps, 10)), nbytes)
     if with_cpu:
         host = c.to("cpu")
-        rate, dt, desc, threads = oracle_sample_rate(host, 12.0, "decode")
+        rate, dt, desc, threads = oracle_sample_rate(host, 20.0, "decode")
         res["cpu_baseline"] = {"value": rate, "unit": "GB/s", "cores": threads, "kind": "oracle",
                                "sample": desc, "seconds": dt}
     del c
@@ -373,7 +373,7 @@ def bench_prefill(name, steps, warmup, gpu_index, pk, with_cpu=False):
                         "kernel_ms": kern_ms, "launches_timed": n_k, "peak_source": f"{pk[1]} bf16_tflops (burst)",
                         "source_digest": digest}}
     if with_cpu:
-        rate, dt, desc, threads = oracle_sample_rate(c.to("cpu"), 12.0, "prefill")
+        rate, dt, desc, threads = oracle_sample_rate(c.to("cpu"), 20.0, "prefill")
         res["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                "sample": desc, "seconds": dt}
     del c, flush
