@@ -167,6 +167,23 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------- timing
+def max_over_ranks(x: float, device="cuda") -> float:
+    """The largest x over all ranks of the default process group (x itself when there is
+    no group): the step time every rank reports is the slowest rank's."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(units_per_rank: float, world: int, ms: float, scale: float = 1e9) -> float:
+    """Whole-job throughput: every rank processes the same workload (weak scaling), so the
+    job processes `world` times the units of one rank in the slowest rank's time."""
+    return units_per_rank * world / (ms * 1e-3) / scale
+
+
 def time_region(fn, steps, warmup, barrier=None):
     for _ in range(warmup):
         fn()
@@ -429,13 +446,8 @@ def main():
         return 0
     main_res = bench_decode(args.workload, args.steps, args.warmup, barrier, local, pk,
                             with_e2e=not args.no_e2e, with_cpu=(rank == 0 and not args.no_cpu))
-    ms = main_res["ms_per_step"]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = main_res["bytes_per_step"] * world / (ms * 1e-3) / 1e9
+    ms = max_over_ranks(main_res["ms_per_step"])
+    value = weak_scaling_value(main_res["bytes_per_step"], world, ms)
     line = {
         "metric": "decode KV GB/s and prefill TFLOPS at hd512, % of GB300 roofline",
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,

@@ -810,9 +810,13 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
           // second pass reusing P: replay the first pass's O rescales, in step with the
           // PVs; no S.  Waiting for the PV two steps back keeps every pv_done barrier
           // within one phase of this warp's waits.
+          // this thread wrote the factors itself in the first pass; each is loaded one tile
+          // ahead so its latency overlaps the previous tile
+          float a_next = mscr[row];
           for (int j = 0; j < f.nt; ++j, ++gstep) {
+            const float a = a_next;
+            if (j + 1 < f.nt) a_next = mscr[(j + 1) * 128 + row];
             if (gstep >= 2) mbar_wait(&pv_done[gstep & 1], ((gstep - 2) >> 1) & 1, p.err, SITE_PRE_O_DONE);
-            const float a = *reinterpret_cast<volatile float*>(mscr + j * 128 + row);
             const bool resc = a != 1.f;
             if (__any_sync(0xffffffffu, resc)) {
               mbar_wait(&pv_done[(gstep - 1) & 1], ((gstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
