@@ -130,8 +130,14 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
  *
  * q [total_q, num_qo_heads, head_dim_qk] bf16; out [total_q, num_qo_heads, head_dim_vo]
  * bf16; lse [total_q, num_qo_heads] fp32 or NULL.  QK^T and PV run as tcgen05 MMAs with
- * TMEM accumulators; for head_dim_vo = 512 the VO dimension is processed in two halves.
- * Supported shapes, page sizes and dtypes as for decode; group size up to 16.
+ * TMEM accumulators; for head_dim_vo = 512 the VO dimension is processed in two halves
+ * (the second reuses the first's softmax probabilities from a workspace scratch).
+ * Shapes and dtypes as for decode; group size up to 16; page_size >= 8 (smaller pages
+ * return PA_ERR_UNSUPPORTED).  FP8 / NVFP4 KV: the pages kv_indices references are first
+ * converted to a bf16 copy in the library workspace (num_pages * num_kv_heads *
+ * page_size * (head_dim_qk + head_dim_vo) * 2 bytes) when that fits the limit set by
+ * paged_attn_set_prefill_dequant_limit (default 4 GiB), else converted inside the
+ * kernel on every read; both give the same values (the conversions are exact).
  * Returns as paged_attn_decode.
  */
 int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q,
@@ -157,6 +163,11 @@ int paged_attn_check_device_error(int* code);
 /* Test hook for split-K: force every decode chunk to `pages` pages (0 = automatic).
  * The device still widens chunks when the workspace bound requires it.  Process-wide. */
 int paged_attn_set_decode_chunk_pages(int pages);
+
+/* Largest bf16 copy (bytes) of FP8 / NVFP4 pages that paged_attn_prefill may build in its
+ * workspace; 0 = always convert inside the prefill kernel, negative = the default (4 GiB).
+ * Process-wide.  Returns PA_OK. */
+int paged_attn_set_prefill_dequant_limit(long long bytes);
 
 /* Name of the kernel variant the last successful call on this host thread launched
  * (for tests that must know which path ran).  Returns PA_OK; the text is truncated to

@@ -30,7 +30,8 @@ PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 EXPORTED = ("paged_attn_decode", "paged_attn_prefill", "paged_attn_status_string",
             "paged_attn_release_workspace", "paged_attn_check_device_error",
             "paged_attn_set_decode_chunk_pages", "paged_attn_last_variant",
-            "paged_attn_profile_begin", "paged_attn_profile_end", "paged_attn_decode_noalloc")
+            "paged_attn_profile_begin", "paged_attn_profile_end", "paged_attn_decode_noalloc",
+            "paged_attn_set_prefill_dequant_limit")
 
 _lib = None
 
@@ -70,6 +71,8 @@ def load(path: Optional[str] = None):
     lib.paged_attn_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
     lib.paged_attn_set_decode_chunk_pages.restype = i32
     lib.paged_attn_set_decode_chunk_pages.argtypes = [i32]
+    lib.paged_attn_set_prefill_dequant_limit.restype = i32
+    lib.paged_attn_set_prefill_dequant_limit.argtypes = [ctypes.c_longlong]
     lib.paged_attn_last_variant.restype = i32
     lib.paged_attn_last_variant.argtypes = [ctypes.c_char_p, i32]
     lib.paged_attn_profile_begin.restype = i32
@@ -215,6 +218,14 @@ def paged_attn_set_decode_chunk_pages(pages: int) -> None:
     st = load().paged_attn_set_decode_chunk_pages(pages)
     if st != PA_OK:
         raise PagedAttnError(st, "paged_attn_set_decode_chunk_pages")
+
+
+def paged_attn_set_prefill_dequant_limit(nbytes: int) -> None:
+    """Largest bf16 copy of FP8 / NVFP4 pages the prefill may build (0: convert inside the
+    kernel; negative: the library default)."""
+    st = load().paged_attn_set_prefill_dequant_limit(nbytes)
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_set_prefill_dequant_limit")
 
 
 def paged_attn_last_variant() -> str:

@@ -12,6 +12,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <vector>
 
@@ -54,6 +55,8 @@ Workspace g_ws[kMaxDevices];
 constexpr size_t kErrOffset = 0;      // int error word
 constexpr size_t kFixedBytes = 256;   // error word region
 constexpr int kReuseTiles = 64;       // prefill P reuse: items of up to 64 KV tiles (8192 keys)
+constexpr uint64_t kDefaultDequantLimit = 4ull << 30;  // prefill: largest bf16 copy of FP8 / NVFP4 pages
+std::atomic<uint64_t> g_prefill_dequant_limit{kDefaultDequantLimit};
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -209,6 +212,11 @@ const char* paged_attn_status_string(int status) {
 int paged_attn_last_variant(char* buf, int len) {
   if (!buf || len <= 0) return PA_ERR_INVALID_ARG;
   std::snprintf(buf, (size_t)len, "%s", g_variant);
+  return PA_OK;
+}
+
+int paged_attn_set_prefill_dequant_limit(long long bytes) {
+  g_prefill_dequant_limit = bytes < 0 ? kDefaultDequantLimit : (uint64_t)bytes;
   return PA_OK;
 }
 
@@ -379,7 +387,13 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   int smem_optin = 0;
   const int sms = device_sms(&smem_optin);
   if (sms <= 0) return PA_ERR_CUDA;
-  if (prefill_smem_bytes(kv_dtype, head_dim_qk, head_dim_vo) > smem_optin) return PA_ERR_SMEM;
+  // FP8 / NVFP4: convert the referenced pages once into a bf16 copy and run the bf16
+  // kernel on it, when the copy fits the limit; else convert inside the kernel
+  const bool quant = kv_dtype != PA_KV_BF16;
+  const uint64_t bf16_page = (uint64_t)num_kv_heads * page_size * (head_dim_qk + head_dim_vo) * 2;
+  const bool dequant = quant && (uint64_t)num_pages * bf16_page <= g_prefill_dequant_limit.load();
+  const int run_kvt = dequant ? (int)PA_KV_BF16 : kv_dtype;
+  if (prefill_smem_bytes(run_kvt, head_dim_qk, head_dim_vo) > smem_optin) return PA_ERR_SMEM;
 
   const long max_items = ((long)total_q / rows_per_tile + batch) * num_kv_heads;
   if (max_items > (1l << 30)) return PA_ERR_INVALID_ARG;
@@ -392,18 +406,21 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   const int reuse_tiles = head_dim_vo == 512 ? kReuseTiles : 0;
   const size_t o_pscr = off; off = align_up(off + (size_t)sms * reuse_tiles * 32768, 256);
   const size_t o_mscr = off; off = align_up(off + (size_t)sms * reuse_tiles * 128 * sizeof(float), 256);
+  const size_t o_shadow = off; off = align_up(off + (dequant ? (size_t)num_pages * bf16_page : 0), 256);
   char* ws = static_cast<char*>(workspace(off, &st));
   if (!ws) return st;
 
   PrefillLaunch L;
   std::memset(&L, 0, sizeof L);
-  // bf16 K/V: 128B-swizzled boxes of [page_size][64 elements], read by the MMAs as they land.
-  // FP8 / NVFP4: unswizzled boxes of the packed bytes of 64 elements per key (64 / 32 B) and
-  // whole block-scale rows, staged for the converter warps.
-  const bool quant = kv_dtype != PA_KV_BF16;
-  if (!make_kv_maps(&L.tk, &L.tv, &L.tsfk, &L.tsfv, kv_cache, kv_scales ? kv_scales->sf : nullptr, num_pages,
-                    num_kv_heads, head_dim_qk, head_dim_vo, page_size, kv_dtype, page_size, !quant,
-                    quant ? (kv_dtype == KV_FP8 ? 64u : 32u) : 128u))
+  // bf16 K/V (or the bf16 copy): 128B-swizzled boxes of [page_size][64 elements], read by
+  // the MMAs as they land.  FP8 / NVFP4 converted in the kernel: unswizzled boxes of the
+  // packed bytes of 64 elements per key (64 / 32 B) and whole block-scale rows, staged for
+  // the converter warps.
+  const void* kv_read = dequant ? static_cast<const void*>(ws + o_shadow) : kv_cache;
+  const bool packed = run_kvt != PA_KV_BF16;
+  if (!make_kv_maps(&L.tk, &L.tv, &L.tsfk, &L.tsfv, kv_read, packed ? kv_scales->sf : nullptr, num_pages,
+                    num_kv_heads, head_dim_qk, head_dim_vo, page_size, run_kvt, page_size, !packed,
+                    packed ? (run_kvt == KV_FP8 ? 64u : 32u) : 128u))
     return PA_ERR_CUDA;
   // Q as [total_q][Hq][d_qk] bf16 bytes: boxes of [rows_per_tile][group][128 B]
   {
@@ -454,14 +471,27 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   L.grid = sms;
   L.stream = static_cast<cudaStream_t>(stream);
 
+  if (dequant) {
+    DequantParams d;
+    d.cache = static_cast<const uint8_t*>(kv_cache);
+    d.sf = kv_scales->sf;
+    d.kv_indptr = kv_indptr;
+    d.kv_indices = kv_indices;
+    d.shadow = reinterpret_cast<uint16_t*>(ws + o_shadow);
+    d.batch = batch;
+    d.Hkv = num_kv_heads;
+    d.page_size = page_size;
+    if (launch_prefill_dequant(kv_dtype, head_dim_qk, head_dim_vo, d, 4 * sms, L.stream) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
   if (launch_prefill_plan(p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
   const char* name = "?";
   prof_mark(L.stream, true);
-  cudaError_t e = launch_prefill(kv_dtype, head_dim_qk, head_dim_vo, L, &name);
+  cudaError_t e = launch_prefill(run_kvt, head_dim_qk, head_dim_vo, L, &name);
   prof_mark(L.stream, false);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};
-  std::snprintf(g_variant, sizeof g_variant, "%s_%s", name, kv_names[kv_dtype]);
+  std::snprintf(g_variant, sizeof g_variant, "%s_%s%s", name, kv_names[kv_dtype], dequant ? "_dequant" : "");
   return PA_OK;
 }
 

@@ -93,4 +93,14 @@ struct PrefillParams {
   float sm_scale;
 };
 
+// FP8 / NVFP4 pages -> bf16 copy for the prefill (see prefill_dequant.cu)
+struct DequantParams {
+  const uint8_t* cache;  // packed pages
+  const uint8_t* sf;     // NVFP4 block-scale pool (same page indexing)
+  const int32_t* kv_indptr;
+  const int32_t* kv_indices;
+  uint16_t* shadow;      // bf16 pages, same page index
+  int batch, Hkv, page_size;
+};
+
 }  // namespace pa

@@ -38,5 +38,7 @@ int decode_tile_tokens(int kvt, int dqk);
 cudaError_t launch_prefill(int kvt, int dqk, int dvo, const PrefillLaunch& L, const char** variant);
 cudaError_t launch_prefill_plan(const PrefillParams& p, cudaStream_t s);
 int prefill_smem_bytes(int kvt, int dqk, int dvo);
+// FP8 / NVFP4 pages referenced by kv_indices -> bf16 pages of the same index.
+cudaError_t launch_prefill_dequant(int kvt, int dqk, int dvo, const DequantParams& d, int grid, cudaStream_t s);
 
 }  // namespace pa

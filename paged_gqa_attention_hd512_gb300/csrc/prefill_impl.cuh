@@ -771,12 +771,13 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     constexpr int OCOL = C::DVP / C::SMW;
     const int ocol0 = wg * OCOL;
     // FP8 per-tensor / NVFP4 global K scale folds into the scores, the V scale into the output
-    const float scale_log2 = p.sm_scale * 1.4426950408889634f * (KVT == KV_BF16 ? 1.f : __ldg(p.k_scale));
+    // (also given for bf16 KV when it is the bf16 copy of FP8 / NVFP4 pages)
+    const float scale_log2 = p.sm_scale * 1.4426950408889634f * (p.k_scale ? __ldg(p.k_scale) : 1.f);
     // scores are scaled inside the exponent's FMA; a non-positive scale is applied up
     // front instead (the maximum of the raw scores is only the scaled maximum for scale > 0)
     const bool pos_scale = scale_log2 > 0.f;
     const float eff_scale = pos_scale ? scale_log2 : 1.f;
-    const float v_scale = KVT == KV_BF16 ? 1.f : __ldg(p.v_scale);
+    const float v_scale = p.v_scale ? __ldg(p.v_scale) : 1.f;
     auto rescale_o = [&](float a) {
 #pragma unroll 1
       for (int c = 0; c < OCOL / 32; ++c) {

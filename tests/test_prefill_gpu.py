@@ -87,11 +87,23 @@ def _qid(c):
     return {synth.KV_FP8: "fp8", synth.KV_NVFP4: "nvfp4"}[c[0]] + "-" + _id(c[1:])
 
 
+@pytest.fixture
+def _dequant_limit():
+    yield
+    pa.paged_attn_set_prefill_dequant_limit(-1)
+
+
+@pytest.mark.parametrize("mode", ["dequant", "in_kernel"])
 @pytest.mark.parametrize("c", QCASES, ids=[_qid(c) for c in QCASES])
-def test_prefill_parity_quantised(c):
+def test_prefill_parity_quantised(c, mode, _dequant_limit):
+    """FP8 / NVFP4 pages converted once into a bf16 copy (the default) and converted inside
+    the kernel on every read (the path for caches whose copy would exceed the limit)."""
+    ensure_built()
+    pa.paged_attn_set_prefill_dequant_limit(-1 if mode == "dequant" else 0)
     dt, dqk, dvo, hq, hkv, ps, kv, qo, causal, win = c
     case = synth.make_case("prefill", batch=len(kv), Hq=hq, Hkv=hkv, d_qk=dqk, d_vo=dvo, page_size=ps,
                            kv_lens=kv, qo_lens=qo, kv_dtype=dt, causal=causal, window_left=win, seed=600 + len(kv))
-    check_full(case, _qid(c))
+    check_full(case, _qid(c) + "-" + mode)
     names = {synth.KV_FP8: "fp8", synth.KV_NVFP4: "nvfp4"}
-    assert pa.paged_attn_last_variant() == f"prefill_{dqk}x{dvo}_{names[dt]}"
+    suffix = "_dequant" if mode == "dequant" else ""
+    assert pa.paged_attn_last_variant() == f"prefill_{dqk}x{dvo}_{names[dt]}{suffix}"
