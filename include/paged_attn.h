@@ -169,6 +169,14 @@ int paged_attn_set_decode_chunk_pages(int pages);
  * Process-wide.  Returns PA_OK. */
 int paged_attn_set_prefill_dequant_limit(long long bytes);
 
+/* Prefill with bf16 KV (or the bf16 copy of FP8 / NVFP4 pages) on CTA pairs: two CTAs of
+ * a cluster on neighbouring SMs compute two query tiles of the same KV head with shared
+ * MMAs (M = 256), each loading half of every K/V tile.  mode 1 uses pairs whenever
+ * two-CTA clusters fit on the device; 0 and -1 (the default) use one CTA per query tile,
+ * which was faster on every measured workload.  Both give the same results up to
+ * summation order.  Process-wide.  Returns PA_OK, or PA_ERR_INVALID_ARG for another mode. */
+int paged_attn_set_prefill_cta_pairs(int mode);
+
 /* Name of the kernel variant the last successful call on this host thread launched
  * (for tests that must know which path ran).  Returns PA_OK; the text is truncated to
  * len-1 characters. */

@@ -31,7 +31,7 @@ EXPORTED = ("paged_attn_decode", "paged_attn_prefill", "paged_attn_status_string
             "paged_attn_release_workspace", "paged_attn_check_device_error",
             "paged_attn_set_decode_chunk_pages", "paged_attn_last_variant",
             "paged_attn_profile_begin", "paged_attn_profile_end", "paged_attn_decode_noalloc",
-            "paged_attn_set_prefill_dequant_limit")
+            "paged_attn_set_prefill_dequant_limit", "paged_attn_set_prefill_cta_pairs")
 
 _lib = None
 
@@ -73,6 +73,8 @@ def load(path: Optional[str] = None):
     lib.paged_attn_set_decode_chunk_pages.argtypes = [i32]
     lib.paged_attn_set_prefill_dequant_limit.restype = i32
     lib.paged_attn_set_prefill_dequant_limit.argtypes = [ctypes.c_longlong]
+    lib.paged_attn_set_prefill_cta_pairs.restype = i32
+    lib.paged_attn_set_prefill_cta_pairs.argtypes = [i32]
     lib.paged_attn_last_variant.restype = i32
     lib.paged_attn_last_variant.argtypes = [ctypes.c_char_p, i32]
     lib.paged_attn_profile_begin.restype = i32
@@ -226,6 +228,14 @@ def paged_attn_set_prefill_dequant_limit(nbytes: int) -> None:
     st = load().paged_attn_set_prefill_dequant_limit(nbytes)
     if st != PA_OK:
         raise PagedAttnError(st, "paged_attn_set_prefill_dequant_limit")
+
+
+def paged_attn_set_prefill_cta_pairs(mode: int) -> None:
+    """1: bf16 prefill on CTA pairs whenever two-CTA clusters fit; 0 or -1 (default): one
+    CTA per query tile."""
+    st = load().paged_attn_set_prefill_cta_pairs(mode)
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_set_prefill_cta_pairs")
 
 
 def paged_attn_last_variant() -> str:

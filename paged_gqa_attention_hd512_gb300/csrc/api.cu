@@ -12,6 +12,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <vector>
@@ -57,6 +58,29 @@ constexpr size_t kFixedBytes = 256;   // error word region
 constexpr int kReuseTiles = 64;       // prefill P reuse: items of up to 64 KV tiles (8192 keys)
 constexpr uint64_t kDefaultDequantLimit = 4ull << 30;  // prefill: largest bf16 copy of FP8 / NVFP4 pages
 std::atomic<uint64_t> g_prefill_dequant_limit{kDefaultDequantLimit};
+// prefill with bf16 KV on CTA pairs: 1 = whenever two-CTA clusters fit, 0 = never (the
+// default: on the measured workloads one CTA per query tile is faster)
+std::atomic<int> g_prefill_pairs{0};
+// two-CTA clusters of the pair kernel per device and shape (512x512, 512x256, 256x256);
+// -1 = not asked yet
+std::atomic<int> g_pair_clusters[kMaxDevices][3];
+std::once_flag g_pair_clusters_init;
+
+int pair_clusters(int dqk, int dvo) {
+  std::call_once(g_pair_clusters_init, [] {
+    for (auto& d : g_pair_clusters)
+      for (auto& v : d) v = -1;
+  });
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  const int shape = dvo == 512 ? 0 : (dqk == 512 ? 1 : 2);
+  int n = g_pair_clusters[dev][shape].load();
+  if (n < 0) {
+    n = prefill_pair_clusters(dqk, dvo);
+    g_pair_clusters[dev][shape] = n;
+  }
+  return n;
+}
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -217,6 +241,12 @@ int paged_attn_last_variant(char* buf, int len) {
 
 int paged_attn_set_prefill_dequant_limit(long long bytes) {
   g_prefill_dequant_limit = bytes < 0 ? kDefaultDequantLimit : (uint64_t)bytes;
+  return PA_OK;
+}
+
+int paged_attn_set_prefill_cta_pairs(int mode) {
+  if (mode < -1 || mode > 1) return PA_ERR_INVALID_ARG;
+  g_prefill_pairs = mode < 0 ? 0 : mode;
   return PA_OK;
 }
 
@@ -394,6 +424,9 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   const bool dequant = quant && (uint64_t)num_pages * bf16_page <= g_prefill_dequant_limit.load();
   const int run_kvt = dequant ? (int)PA_KV_BF16 : kv_dtype;
   if (prefill_smem_bytes(run_kvt, head_dim_qk, head_dim_vo) > smem_optin) return PA_ERR_SMEM;
+  // bf16 kernel (or the bf16 copy): CTA pairs share each MMA and each K/V tile
+  int pair_grid = 0;
+  if (run_kvt == PA_KV_BF16 && g_prefill_pairs.load() == 1) pair_grid = 2 * std::min(sms / 2, pair_clusters(head_dim_qk, head_dim_vo));
 
   const long max_items = ((long)total_q / rows_per_tile + batch) * num_kv_heads;
   if (max_items > (1l << 30)) return PA_ERR_INVALID_ARG;
@@ -435,6 +468,20 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return PA_ERR_CUDA;
   }
+  // CTA pairs: the P scratch as rows of 128 bytes, one P tile (32 KB) per box
+  L.tp = L.tq;
+  if (pair_grid > 0 && reuse_tiles > 0) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return PA_ERR_CUDA;
+    cuuint64_t dims[2] = {128, (cuuint64_t)sms * reuse_tiles * 256};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, 256};
+    cuuint32_t estr[2] = {1, 1};
+    if (fn(&L.tp, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, ws + o_pscr, dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return PA_ERR_CUDA;
+  }
   PrefillParams& p = L.p;
   p.q = static_cast<const uint16_t*>(q);
   p.qo_indptr = qo_indptr;
@@ -464,11 +511,12 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   p.causal = causal ? 1 : 0;
   p.num_pages = num_pages;
   p.rows_per_tile = rows_per_tile;
+  p.pair = pair_grid > 0 ? 1 : 0;
   p.max_items = (int)max_items;
   p.box_rows = page_size;
   p.swz = 7;
   p.sm_scale = sm_scale;
-  L.grid = sms;
+  L.grid = pair_grid > 0 ? pair_grid : sms;
   L.stream = static_cast<cudaStream_t>(stream);
 
   if (dequant) {

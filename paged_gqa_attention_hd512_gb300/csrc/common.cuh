@@ -42,15 +42,27 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// kCluster: acquire at cluster scope, for phases completed by arrivals from the other CTA
+// of a pair
+template <bool kCluster = false>
 __device__ __forceinline__ uint32_t mbar_try_wait(uint32_t addr, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(addr), "r"(parity)
-      : "memory");
+  if constexpr (kCluster)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
   return ok;
 }
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -62,12 +74,13 @@ __device__ __forceinline__ uint64_t globaltimer() {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // The spinning part stays out of line: inlined into a tcgen05.mma issue loop it cost that
 // loop about half of its MMA rate (measured on sm_103a), even when never taken.
+template <bool kCluster>
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t addr, uint32_t parity, int* err, int site) {
   // once any wait of this launch (or an earlier one) has given up, do not wait again
   if (err && *reinterpret_cast<volatile int*>(err) != 0) return false;
   const uint64_t t0 = globaltimer();
   uint32_t spins = 0;
-  while (!mbar_try_wait(addr, parity)) {
+  while (!mbar_try_wait<kCluster>(addr, parity)) {
     if ((++spins & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) {
       record_error(err, site);
       return false;
@@ -75,10 +88,11 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t addr, uint32_t parit
   }
   return true;
 }
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int site) {
   const uint32_t addr = smem_u32(bar);
-  if (mbar_try_wait(addr, parity)) return true;
-  return mbar_wait_slow(addr, parity, err, site);
+  if (mbar_try_wait<kCluster>(addr, parity)) return true;
+  return mbar_wait_slow<kCluster>(addr, parity, err, site);
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {

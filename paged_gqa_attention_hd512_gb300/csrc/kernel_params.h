@@ -87,6 +87,7 @@ struct PrefillParams {
   int reuse_tiles;
   int batch, total_q, Hq, Hkv, group, page_size, window_left, causal, num_pages;
   int rows_per_tile;  // query positions per 128-row tile (128 / group)
+  int pair;           // 1: items span two tiles, computed by the two CTAs of a cluster
   int max_items;
   int box_rows;
   int swz;

@@ -18,6 +18,7 @@ struct DecodeLaunch {
 
 struct PrefillLaunch {
   CUtensorMap tq, tk, tv, tsfk, tsfv;
+  CUtensorMap tp;  // CTA pairs: the P scratch (rows of 128 bytes, boxes of one P tile)
   PrefillParams p;
   int grid;
   cudaStream_t stream;
@@ -38,6 +39,8 @@ int decode_tile_tokens(int kvt, int dqk);
 cudaError_t launch_prefill(int kvt, int dqk, int dvo, const PrefillLaunch& L, const char** variant);
 cudaError_t launch_prefill_plan(const PrefillParams& p, cudaStream_t s);
 int prefill_smem_bytes(int kvt, int dqk, int dvo);
+// Two-CTA clusters of the bf16 prefill kernel that fit on the device at once.
+int prefill_pair_clusters(int dqk, int dvo);
 // FP8 / NVFP4 pages referenced by kv_indices -> bf16 pages of the same index.
 cudaError_t launch_prefill_dequant(int kvt, int dqk, int dvo, const DequantParams& d, int grid, cudaStream_t s);
 

@@ -5,37 +5,89 @@
 
 namespace pa {
 
-template <int KVT, int DQK, int DVO>
+template <int KVT, int DQK, int DVO, bool PAIR>
 static cudaError_t run_prefill(const PrefillLaunch& L) {
-  using C = PrefillCfg<DQK, DVO, KVT>;
-  auto kern = prefill_kernel<KVT, DQK, DVO>;
+  using C = PrefillCfg<DQK, DVO, KVT, PAIR>;
+  auto kern = prefill_kernel<KVT, DQK, DVO, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC);
   if (e != cudaSuccess) return e;
-  kern<<<L.grid, C::THREADS, C::ALLOC, L.stream>>>(L.tq, L.tk, L.tv, L.tsfk, L.tsfv, L.p);
-  return cudaGetLastError();
+  if constexpr (PAIR) {
+    // clusters of two CTAs (one per SM of a pair)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.grid);
+    cfg.blockDim = dim3(C::THREADS);
+    cfg.dynamicSmemBytes = C::ALLOC;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, L.tq, L.tk, L.tv, L.tsfk, L.tsfv, L.tp, L.p);
+  } else {
+    kern<<<L.grid, C::THREADS, C::ALLOC, L.stream>>>(L.tq, L.tk, L.tv, L.tsfk, L.tsfv, L.tp, L.p);
+    return cudaGetLastError();
+  }
 }
 
-template <int KVT>
+template <int KVT, bool PAIR>
 static cudaError_t dispatch_prefill(int dqk, int dvo, const PrefillLaunch& L, const char** variant) {
   if (dqk == 512 && dvo == 512) {
-    *variant = "prefill_512x512";
-    return run_prefill<KVT, 512, 512>(L);
+    *variant = PAIR ? "prefill_512x512_pair" : "prefill_512x512";
+    return run_prefill<KVT, 512, 512, PAIR>(L);
   }
   if (dqk == 512 && dvo == 256) {
-    *variant = "prefill_512x256";
-    return run_prefill<KVT, 512, 256>(L);
+    *variant = PAIR ? "prefill_512x256_pair" : "prefill_512x256";
+    return run_prefill<KVT, 512, 256, PAIR>(L);
   }
   if (dqk == 256 && dvo == 256) {
-    *variant = "prefill_256x256";
-    return run_prefill<KVT, 256, 256>(L);
+    *variant = PAIR ? "prefill_256x256_pair" : "prefill_256x256";
+    return run_prefill<KVT, 256, 256, PAIR>(L);
   }
   return cudaErrorInvalidValue;
 }
 
+// Largest number of two-CTA clusters of the bf16 kernel that fit on the device at once
+// (0 when none can, or on error).
+int prefill_pair_clusters(int dqk, int dvo) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  auto query = [&](auto kern, int threads, int smem) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return;
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  };
+  if (dqk == 512 && dvo == 512) {
+    using C = PrefillCfg<512, 512, KV_BF16, true>;
+    query(prefill_kernel<KV_BF16, 512, 512, true>, C::THREADS, C::ALLOC);
+  } else if (dqk == 512 && dvo == 256) {
+    using C = PrefillCfg<512, 256, KV_BF16, true>;
+    query(prefill_kernel<KV_BF16, 512, 256, true>, C::THREADS, C::ALLOC);
+  } else if (dqk == 256 && dvo == 256) {
+    using C = PrefillCfg<256, 256, KV_BF16, true>;
+    query(prefill_kernel<KV_BF16, 256, 256, true>, C::THREADS, C::ALLOC);
+  }
+  cudaGetLastError();  // a failed query leaves no sticky error
+  return n;
+}
+
 cudaError_t launch_prefill(int kvt, int dqk, int dvo, const PrefillLaunch& L, const char** variant) {
-  if (kvt == KV_BF16) return dispatch_prefill<KV_BF16>(dqk, dvo, L, variant);
-  if (kvt == KV_FP8) return dispatch_prefill<KV_FP8>(dqk, dvo, L, variant);
-  if (kvt == KV_NVFP4) return dispatch_prefill<KV_NVFP4>(dqk, dvo, L, variant);
+  if (kvt == KV_BF16)
+    return L.p.pair ? dispatch_prefill<KV_BF16, true>(dqk, dvo, L, variant)
+                    : dispatch_prefill<KV_BF16, false>(dqk, dvo, L, variant);
+  if (kvt == KV_FP8) return dispatch_prefill<KV_FP8, false>(dqk, dvo, L, variant);
+  if (kvt == KV_NVFP4) return dispatch_prefill<KV_NVFP4, false>(dqk, dvo, L, variant);
   return cudaErrorInvalidValue;
 }
 

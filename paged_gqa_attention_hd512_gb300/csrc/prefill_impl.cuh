@@ -32,8 +32,13 @@
 
 namespace pa {
 
-template <int DQK, int DVO, int KVT>
+template <int DQK, int DVO, int KVT, bool PAIR_ = false>
 struct PrefillCfg {
+  // PAIR: two CTAs (a cluster) share every MMA (tcgen05 cta_group::2, M = 256): each holds
+  // its own 128 query rows and loads half of every K/V tile, so the pair reads each K/V
+  // byte once instead of twice and each SM takes in half the K/V bytes per MMA cycle
+  static constexpr bool PAIR = PAIR_;
+  static constexpr int CL = PAIR ? 2 : 1;       // CTAs per MMA
   static constexpr int M = 128;                 // query rows per tile
   static constexpr int N = 128;                 // keys per KV tile
   static constexpr int HALF = N * 128;          // one [128 keys][64 dims] bf16 block (16 KB)
@@ -43,6 +48,11 @@ struct PrefillCfg {
   static constexpr int DVP = DVO > 256 ? 256 : DVO;  // output columns per pass
   static constexpr int NPASS = DVO / DVP;
   static constexpr int NVC = DVP / 128;         // V chunks per pass (one N=128 PV group each)
+  // PAIR: a K chunk is this CTA's 64 keys x 256 dims (four [64 keys][64 dims] 128B-swizzled
+  // blocks of 8 KB), a V chunk this CTA's 128 of the pass's 256 output columns
+  static constexpr int KBLK = 64 * 128;
+  static constexpr int NKC = PAIR ? DQK / 256 : NQC;  // K chunks per step
+  static constexpr int NVS_P = PAIR ? 1 : NVC;         // V chunks per step
   static constexpr int Q_BYTES = NQB * HALF;
   static constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
   static constexpr bool QUANT = KVT != KV_BF16;
@@ -71,16 +81,21 @@ struct PrefillCfg {
   static constexpr int OFF_SF = OFF_STG + NSTG * STG_BYTES;
   static constexpr int OFF_DESC = OFF_SF + NSF * SF_BYTES;  // int2 per staging slot: valid keys, flags
   static constexpr int OFF_XCH = OFF_DESC + NSTG * 8;  // [2][128] floats: partial row maxima / sums
-  static constexpr int OFF_BAR = OFF_XCH + (SMW == 2 ? 1024 : 0);
+  // head_dim_vo 512 with P reuse: per KV tile of an item, the item's local index + 1 when
+  // the first pass rescaled O before that tile's PV (the second pass replays only those)
+  static constexpr int MAX_RT = 64;
+  static constexpr int OFF_RTAG = OFF_XCH + (SMW == 2 ? 1024 : 0);
+  static constexpr int OFF_BAR = OFF_RTAG + (NPASS == 2 ? MAX_RT * 4 : 0);
   // head_dim_vo 512 with P reuse: the second pass reads the first pass's P tiles into
   // NPS slots of the Q region (Q is not needed by then)
   static constexpr int NPS = NPASS == 2 ? Q_BYTES / CHUNK : 0;
   // barriers: q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_free, aux, sfree[2],
-  // ps_done, kv_full[], kv_empty[], stg_full[], stg_empty[], sf_full[], sf_empty[],
-  // pslot_full[], pslot_empty[].  Every waiter of a barrier is at most one phase behind or
-  // ahead of it (a parity wait cannot tell more apart): hence one s_full / p_full /
-  // pv_done / sfree per S buffer.
-  static constexpr int NBAR = 13 + 2 * NSLOT + 2 * NSTG + 2 * NSF + 2 * NPS;
+  // ps_done, o_done, o_ready, resc_done, tags_done, kv_full[], kv_empty[], stg_full[], stg_empty[],
+  // sf_full[], sf_empty[], pslot_full[], pslot_empty[].  Every waiter of a barrier is at
+  // most one phase behind or ahead of it (a parity wait cannot tell more apart): hence one
+  // s_full / p_full / pv_done / sfree per S buffer.
+  static constexpr int NB_FIXED = 17;
+  static constexpr int NBAR = NB_FIXED + 2 * NSLOT + 2 * NSTG + 2 * NSF + 2 * NPS;
   static constexpr int BYTES = OFF_BAR + NBAR * 8 + 16;
   static constexpr int ALLOC = BYTES + 1024;
   // TMEM columns: two S buffers of 128 keys (step j uses buffer j & 1; its P, 128 keys of
@@ -97,6 +112,7 @@ struct PrefillCfg {
   static_assert(NB_PSLOT + NPS <= NB_SMX, "named barriers");
   static_assert(NPASS == 1 || NPS >= 2, "P slots");
   static_assert(DVP % 128 == 0 && DQK % 128 == 0, "head dims");
+  static_assert(!PAIR || (KVT == KV_BF16 && DVP == 256 && DQK % 256 == 0), "CTA pairs: bf16 KV");
 };
 
 // ----------------------------------------------------------------------------- plan
@@ -104,8 +120,10 @@ struct PrefillCfg {
 // they visit, so that a static round-robin over persistent CTAs balances.
 constexpr int kPlanBuckets = 2048;
 
+// KV tiles visited by the item starting at new-token q_begin (one query tile, or the two
+// consecutive tiles of a CTA pair)
 __device__ __forceinline__ int prefill_tile_cost(const PrefillParams& p, int kv_len, int qo_len, int q_begin) {
-  const int n_pos = min(p.rows_per_tile, qo_len - q_begin);
+  const int n_pos = min(p.rows_per_tile * (p.pair ? 2 : 1), qo_len - q_begin);
   const int pos0 = kv_len - qo_len + q_begin;
   const int hi = p.causal ? min(kv_len - 1, pos0 + n_pos - 1) : kv_len - 1;
   const int lo = p.window_left >= 0 ? max(0, pos0 - p.window_left) : 0;
@@ -124,7 +142,7 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p) {
   for (int i = tid; i < kPlanBuckets; i += blockDim.x) hist[i] = 0;
   if (tid == 0) s_carry = 0;
   __syncthreads();
-  const int P = p.rows_per_tile, ps = p.page_size;
+  const int P = p.rows_per_tile * (p.pair ? 2 : 1), ps = p.page_size;  // positions per item
   int* off = p.tile_off;  // [batch + 1]
   for (int base = 0; base < p.batch; base += blockDim.x) {
     const int b = base + tid;
@@ -227,21 +245,25 @@ struct PrefillItemInfo {
   int b, kvh, q_begin, n_pos, qo_len, kv_len, q_row0, pos0, jlo, nt, ip0, np;
 };
 
-__device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams& p, int it) {
+// `rank`: which tile of a CTA pair's item this CTA computes (0 without pairs).  Both CTAs
+// of a pair walk the KV range of the whole item; the second tile may be empty (n_pos 0).
+__device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams& p, int it, int rank) {
   const PrefillItem item = p.items[it];
   PrefillItemInfo f;
   f.b = item.b;
   f.kvh = item.kvh;
-  f.q_begin = item.q_begin;
+  f.q_begin = item.q_begin + rank * p.rows_per_tile;
   f.qo_len = p.qo_indptr[f.b + 1] - p.qo_indptr[f.b];
   f.ip0 = p.kv_indptr[f.b];
   f.np = p.kv_indptr[f.b + 1] - f.ip0;
   f.kv_len = f.np > 0 ? (f.np - 1) * p.page_size + p.kv_last_page_len[f.b] : 0;
-  f.n_pos = min(p.rows_per_tile, f.qo_len - f.q_begin);
+  f.n_pos = max(0, min(p.rows_per_tile, f.qo_len - f.q_begin));
   f.q_row0 = p.qo_indptr[f.b] + f.q_begin;
   f.pos0 = f.kv_len - f.qo_len + f.q_begin;
-  int hi = p.causal ? min(f.kv_len - 1, f.pos0 + f.n_pos - 1) : f.kv_len - 1;
-  int lo = p.window_left >= 0 ? max(0, f.pos0 - p.window_left) : 0;
+  const int ipos0 = f.kv_len - f.qo_len + item.q_begin;
+  const int inpos = min(p.rows_per_tile * (p.pair ? 2 : 1), f.qo_len - item.q_begin);
+  int hi = p.causal ? min(f.kv_len - 1, ipos0 + inpos - 1) : f.kv_len - 1;
+  int lo = p.window_left >= 0 ? max(0, ipos0 - p.window_left) : 0;
   hi = max(hi, 0);  // at least one tile: rows without a visible key come out as 0 / -inf
   lo = min(lo, hi);
   f.jlo = lo / 128;
@@ -249,19 +271,24 @@ __device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams
   return f;
 }
 
-// r-th item of this CTA: rounds of gridDim.x items, alternating direction, over a list
-// sorted by descending cost.
+// r-th item of this CTA (or CTA pair): rounds of one item per CTA (pair), alternating
+// direction, over a list sorted by descending cost.
+template <bool PAIR>
 __device__ __forceinline__ int prefill_item_at(int r) {
-  const int off = (r & 1) ? (int)(gridDim.x - 1 - blockIdx.x) : (int)blockIdx.x;
-  return r * (int)gridDim.x + off;
+  const int n = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int u = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int off = (r & 1) ? n - 1 - u : u;
+  return r * n + off;
 }
 
-template <int KVT, int DQK, int DVO>
-__global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
+// tm_p (CTA pairs only): the P scratch as rows of 128 bytes, boxes of one 32 KB P tile
+template <int KVT, int DQK, int DVO, bool PAIR>
+__global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sfk,
-                   const __grid_constant__ CUtensorMap tm_sfv, const PrefillParams p) {
-  using C = PrefillCfg<DQK, DVO, KVT>;
+                   const __grid_constant__ CUtensorMap tm_sfv, const __grid_constant__ CUtensorMap tm_p,
+                   const PrefillParams p) {
+  using C = PrefillCfg<DQK, DVO, KVT, PAIR>;
   constexpr int NSLOT = C::NSLOT;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -277,9 +304,13 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
   uint64_t* aux = bars + 9;
   uint64_t* sfree = bars + 10;    // [2]: the PV that read P from S buffer b is complete
   uint64_t* ps_done = bars + 12;  // the first pass's P tiles of an item are in global memory
-  uint64_t* kv_full = bars + 13;
-  uint64_t* kv_empty = bars + 13 + NSLOT;
-  uint64_t* stg_full = bars + 13 + 2 * NSLOT;
+  uint64_t* o_done = bars + 13;   // the last PV of a pass is complete (once per pass)
+  uint64_t* o_ready = bars + 14;  // P reuse: the PVs before a replayed rescale are complete
+  uint64_t* resc_done = bars + 15;  // P reuse: the softmax warps rescaled O
+  uint64_t* tags_done = bars + 16;  // CTA pairs: both CTAs' rescale tags of an item are written
+  uint64_t* kv_full = bars + C::NB_FIXED;
+  uint64_t* kv_empty = kv_full + NSLOT;
+  uint64_t* stg_full = kv_full + 2 * NSLOT;
   uint64_t* stg_empty = stg_full + C::NSTG;
   uint64_t* sf_full = stg_empty + C::NSTG;
   uint64_t* sf_empty = sf_full + C::NSF;
@@ -289,24 +320,34 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA pairs: the barriers the MMA issuer waits on live in the pair's first CTA (rank 0)
+  // and count the arrivals of both CTAs; the barriers MMA completion signals exist in both
+  // CTAs (multicast commits).  `lead` gives a barrier's address in the first CTA.
+  const uint32_t rank = C::PAIR ? cluster_ctarank() : 0;
+  auto lead = [&](uint64_t* b) -> uint32_t { return C::PAIR ? mapa_shared(smem_u32(b), 0) : smem_u32(b); };
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(q_full, C::CL);
     mbar_init(q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
-      mbar_init(&p_full[b], 4 * C::SMW);
+      mbar_init(&p_full[b], 4 * C::SMW * C::CL);
       mbar_init(&pv_done[b], 1);
       mbar_init(&sfree[b], 1);
     }
     mbar_init(ps_done, 4 * C::SMW);
+    mbar_init(o_done, 1);
+    mbar_init(o_ready, 1);
+    mbar_init(resc_done, 4 * C::SMW * C::CL);
+    mbar_init(tags_done, 4 * C::SMW * C::CL);
     for (int s = 0; s < C::NPS; ++s) {
-      mbar_init(&pslot_full[s], 1);
+      mbar_init(&pslot_full[s], C::CL);
       mbar_init(&pslot_empty[s], 1);
     }
-    mbar_init(o_free, 4 * C::SMW);
+    mbar_init(o_free, 4 * C::SMW * C::CL);
     mbar_init(aux, 1);
     for (int s = 0; s < NSLOT; ++s) {
-      mbar_init(&kv_full[s], KVT == KV_BF16 ? 1 : 4);  // quantised KV: the four converter warps arrive
+      // quantised KV: the four converter warps arrive; pairs: both CTAs' producers
+      mbar_init(&kv_full[s], KVT == KV_BF16 ? C::CL : 4);
       mbar_init(&kv_empty[s], 1);
     }
     for (int s = 0; s < C::NSTG; ++s) {
@@ -319,16 +360,25 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     }
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(tmem_slot, 512);
+  if (warp == 1) {
+    if constexpr (C::PAIR) tmem_alloc_pair(tmem_slot, 512);
+    else tmem_alloc(tmem_slot, 512);
+  }
+  if (C::NPASS == 2)
+    for (int i = threadIdx.x; i < C::MAX_RT; i += C::THREADS) reinterpret_cast<int*>(smem + C::OFF_RTAG)[i] = 0;
   tc_fence_before();
-  __syncthreads();
+  if constexpr (C::PAIR) cluster_sync_all();  // the peer's barriers exist before any remote arrival
+  else __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   const int n_items = min(p.hdr[0], p.max_items);
   const int ps = p.page_size, g = p.group;
   // head_dim_vo 512 (bf16 KV): the second pass reads P of the first from global scratch
   // instead of recomputing S, for items whose KV range fits the scratch
-  auto item_reuse = [&](const PrefillItemInfo& f) { return C::NPASS == 2 && !C::QUANT && f.nt <= p.reuse_tiles; };
+  auto item_reuse = [&](const PrefillItemInfo& f) {
+    return C::NPASS == 2 && !C::QUANT && f.nt <= p.reuse_tiles && f.nt <= C::MAX_RT;
+  };
+  int* rtag = reinterpret_cast<int*>(smem + C::OFF_RTAG);
 
   if (warp == 0 && KVT == KV_BF16) {
     // ------------------------------------------------------------ producer (whole warp)
@@ -340,15 +390,22 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     uint32_t rc = 0, aux_phase = 0, qe = 0, psd = 0, np = 0;
     const uint64_t pol_kv = l2_policy_evict_last(), pol_q = l2_policy_evict_first();
     for (int r = 0;; ++r) {
-      const int it = prefill_item_at(r);
+      const int it = prefill_item_at<C::PAIR>(r);
       if (it >= n_items) break;
-      const PrefillItemInfo f = prefill_item_info(p, it);
+      const PrefillItemInfo f = prefill_item_info(p, it, rank);
       const bool reuse = item_reuse(f);
-      mbar_wait(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
+      mbar_wait<C::PAIR>(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
       if (lane == 0) {
-        mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQB * 128 * g * p.rows_per_tile));
-        for (int c = 0; c < C::NQB; ++c)
-          tma_load_3d_hint(q_s + c * C::HALF, &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
+        const uint32_t qbytes = (uint32_t)(C::NQB * 128 * g * p.rows_per_tile);
+        if constexpr (C::PAIR) {
+          mbar_arrive_expect_tx_cluster(lead(q_full), qbytes);
+          for (int c = 0; c < C::NQB; ++c)
+            tma_load_3d_pair(q_s + c * C::HALF, &tm_q, c * 128, f.kvh * g, f.q_row0, lead(q_full), pol_q);
+        } else {
+          mbar_arrive_expect_tx(q_full, qbytes);
+          for (int c = 0; c < C::NQB; ++c)
+            tma_load_3d_hint(q_s + c * C::HALF, &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
+        }
       }
       // steps that compute S: both passes, or only the first when the second reuses P
       const int steps = reuse ? f.nt : C::NPASS * f.nt;
@@ -366,25 +423,62 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
         const int pass = st / f.nt, jt = st % f.nt;
         const int key0 = (f.jlo + jt) * 128;
         const int valid = max(0, min(128, f.kv_len - key0));
+        if constexpr (C::PAIR) {
+          if (is_k) {
+            // this CTA's 64 keys of the tile (B rows of its half of N), in chunks of 256
+            // dims: four [64 keys][64 dims] blocks per page piece
+            const int h0 = key0 + 64 * (int)rank;
+            const int pieces = max(0, min(64, page_tok_cap - h0)) / ps;
+            const int pg0 = 64 * (int)rank / ps;
+            for (int c = 0; c < C::NKC; ++c, ++rc) {
+              const int slot = rc % NSLOT;
+              mbar_wait<C::PAIR>(&kv_empty[slot], ((rc / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
+              const uint32_t dst = ring + slot * C::CHUNK;
+              const uint32_t fb = lead(&kv_full[slot]);
+              if (lane == 0) mbar_arrive_expect_tx_cluster(fb, (uint32_t)(4 * pieces * ps * 128));
+              for (int pc = 0; pc < pieces; ++pc) {
+                const int page = __shfl_sync(0xffffffffu, my_page, pg0 + pc);
+                if (lane == 0)
+                  for (int blk = 0; blk < 4; ++blk)
+                    tma_load_3d_pair(dst + blk * C::KBLK + pc * ps * 128, &tm_k, c * 512 + blk * 128, f.kvh * ps,
+                                     page, fb, pol_kv);
+              }
+            }
+            return;
+          }
+        }
         const int load_rows = max(0, min(128, page_tok_cap - key0));
         const int pieces = load_rows / ps;
-        const int nch = is_k ? C::NQC : C::NVC;
+        const int nch = is_k ? C::NQC : C::NVS_P;
         for (int c = 0; c < nch; ++c, ++rc) {
           const int slot = rc % NSLOT;
-          mbar_wait(&kv_empty[slot], ((rc / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
+          mbar_wait<C::PAIR>(&kv_empty[slot], ((rc / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
           const uint32_t dst = ring + slot * C::CHUNK;
           const uint32_t bytes = (uint32_t)(2 * pieces * ps * 128);
           const bool fix = !is_k && valid < 128;  // V rows past the sequence must be zeroed
+          // pairs: the chunk completes on the first CTA's barrier (the zeroing path on this
+          // CTA's aux first)
+          const bool remote = C::PAIR && !fix;
           uint64_t* bar = fix ? aux : &kv_full[slot];
-          if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
+          const uint32_t fb = lead(&kv_full[slot]);
+          if (lane == 0) {
+            if (remote) mbar_arrive_expect_tx_cluster(fb, bytes);
+            else mbar_arrive_expect_tx(bar, bytes);
+          }
           // the chunk's two 64-dim blocks: bytes of dims [128 c, 128 c + 128) of the row
-          const int col = is_k ? c * 256 : (pass * C::DVP + c * 128) * 2;
+          // (pairs: of this CTA's 128 of the pass's output columns)
+          const int col = is_k ? c * 256 : (pass * C::DVP + (C::PAIR ? (int)rank : c) * 128) * 2;
           for (int pc = 0; pc < pieces; ++pc) {
             const int page = __shfl_sync(0xffffffffu, my_page, pc);
             if (lane == 0)
-              for (int h = 0; h < 2; ++h)
-                tma_load_3d_hint(dst + h * C::HALF + pc * ps * 128, is_k ? &tm_k : &tm_v, col + h * 128, f.kvh * ps,
-                                 page, bar, pol_kv);
+              for (int h = 0; h < 2; ++h) {
+                if (remote)
+                  tma_load_3d_pair(dst + h * C::HALF + pc * ps * 128, &tm_v, col + h * 128, f.kvh * ps, page, fb,
+                                   pol_kv);
+                else
+                  tma_load_3d_hint(dst + h * C::HALF + pc * ps * 128, is_k ? &tm_k : &tm_v, col + h * 128,
+                                   f.kvh * ps, page, bar, pol_kv);
+              }
           }
           if (fix) {
             mbar_wait(aux, aux_phase, p.err, SITE_PRE_DEQ);
@@ -398,7 +492,10 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
             }
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&kv_full[slot]);
+            if (lane == 0) {
+              if constexpr (C::PAIR) mbar_arrive_cluster(fb);
+              else mbar_arrive(&kv_full[slot]);
+            }
           }
         }
       };
@@ -416,7 +513,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
       if (reuse) {
         // second pass: P tile j of the first pass (into a P slot of the Q region, free once
         // the last QK of the item is done) and V of the upper output half
-        mbar_wait(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
+        mbar_wait<C::PAIR>(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
         mbar_wait(ps_done, psd++ & 1, p.err, SITE_PRE_P_FULL);
         const uint8_t* pscr = p.p_scratch + (size_t)blockIdx.x * p.reuse_tiles * C::CHUNK;
         int pg = step_pages(f.nt);
@@ -424,10 +521,16 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
           const int pg_n = step_pages(f.nt + j + 1);
           constexpr int NPS = C::NPS > 0 ? C::NPS : 1;
           const int s = np % NPS;
-          mbar_wait(&pslot_empty[s], ((np / NPS) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
+          mbar_wait<C::PAIR>(&pslot_empty[s], ((np / NPS) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
           if (lane == 0) {
-            mbar_arrive_expect_tx(&pslot_full[s], (uint32_t)C::CHUNK);
-            bulk_load_g2s(q_s + s * C::CHUNK, pscr + (size_t)j * C::CHUNK, (uint32_t)C::CHUNK, &pslot_full[s]);
+            if constexpr (C::PAIR) {
+              mbar_arrive_expect_tx_cluster(lead(&pslot_full[s]), (uint32_t)C::CHUNK);
+              tma_load_2d_pair(q_s + s * C::CHUNK, &tm_p, 0, ((int)blockIdx.x * p.reuse_tiles + j) * 256,
+                               lead(&pslot_full[s]), pol_q);
+            } else {
+              mbar_arrive_expect_tx(&pslot_full[s], (uint32_t)C::CHUNK);
+              bulk_load_g2s(q_s + s * C::CHUNK, pscr + (size_t)j * C::CHUNK, (uint32_t)C::CHUNK, &pslot_full[s]);
+            }
           }
           emit(false, f.nt + j, pg);
           pg = pg_n;
@@ -455,9 +558,9 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
       uint32_t n = 0, nsf = 0;
       int it_local = 0;
       for (int r = 0;; ++r, ++it_local) {
-        const int it = prefill_item_at(r);
+        const int it = prefill_item_at<C::PAIR>(r);
         if (it >= n_items) break;
-        const PrefillItemInfo f = prefill_item_info(p, it);
+        const PrefillItemInfo f = prefill_item_info(p, it, rank);
         mbar_wait(q_empty, (it_local & 1) ^ 1, p.err, SITE_PRE_Q);
         if (lane == 0) {
           mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQB * 128 * g * p.rows_per_tile));
@@ -607,7 +710,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
       }
       (void)FL_FIRST;
     }
-  } else if (warp == 1 || warp == 2) {
+  } else if ((warp == 1 || warp == 2) && rank == 0) {
     // ------------------------------------------------------- MMA issuer (1) and gate (2)
     // Both warps walk the same schedule.  The gate polls the mbarriers; the MMA warp waits
     // on a named barrier the gate meets once its poll succeeded, and lane 0 issues the
@@ -617,17 +720,36 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     // Both sides use bar.sync, so the gate never runs more than one barrier ahead.
     const bool gate = warp == 2;
     const bool leader = warp == 1 && lane == 0;
-    constexpr uint32_t ID_QK = idesc_f16<true>(128, 128, false);
-    // quantised KV: P and V in f16
-    constexpr uint32_t ID_PV = idesc_f16<!C::QUANT>(128, 128, true);
+    constexpr uint32_t ID_QK = idesc_f16<true>(128 * C::CL, 128, false);
+    // quantised KV: P and V in f16.  Pairs: one N = 256 MMA per 16 keys covers the pass's
+    // output columns (128 from each CTA's V chunk)
+    constexpr uint32_t ID_PV = idesc_f16<!C::QUANT>(128 * C::CL, 128 * C::CL, true);
+    // MMA issue and commits: the pair forms (cta_group::2) in a CTA pair.  commit_both
+    // signals the barrier in both CTAs, commit_here only in this (the first) CTA.
+    auto mma_ss = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+      if constexpr (C::PAIR) tc_mma_ss_pair(d, a, b, id, acc);
+      else tc_mma_ss(d, a, b, id, acc);
+    };
+    auto mma_ts = [&](uint32_t d, uint32_t a, uint64_t b, uint32_t id, uint32_t acc) {
+      if constexpr (C::PAIR) tc_mma_ts_pair(d, a, b, id, acc);
+      else tc_mma_ts(d, a, b, id, acc);
+    };
+    auto commit_both = [&](uint64_t* b) {
+      if constexpr (C::PAIR) tc_commit_pair_both(b);
+      else tc_commit(b);
+    };
+    auto commit_here = [&](uint64_t* b) {
+      if constexpr (C::PAIR) tc_commit_pair_local(b);
+      else tc_commit(b);
+    };
     // one synchronisation point of the schedule: the gate waits for the phase, then both
     // warps meet at named barrier `id`
     auto point = [&](int id, uint64_t* bar, uint32_t parity, int site) {
-      if (gate) mbar_wait(bar, parity, p.err, site);
+      if (gate) mbar_wait<C::PAIR>(bar, parity, p.err, site);
       named_bar_sync(id, 64);
     };
-    // steps issued so far (QK into S buffer n_qk & 1; PV reads P of step n_pv from buffer
-    // n_pv & 1) and passes finished.  QK of step j + 2 reuses the buffer of step j, where
+    // steps issued so far (QK into S buffer n_qk & 1; PV reads P of step n_spv from buffer
+    // n_spv & 1) and passes finished.  QK of step j + 2 reuses the buffer of step j, where
     // PV of step j reads P: it waits for that PV to complete (an MMA that reads its A
     // operand from TMEM is not ordered against a later MMA writing the same columns).
     // Steps are issued in pairs, QK QK PV PV, so that another MMA group is always queued
@@ -635,39 +757,50 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     // the next PV on a buffer follows the QK that waits on it, so a barrier is never two
     // phases ahead of its waiter.
     // n_spv counts the PVs that read P from an S buffer (their order is the QKs' order);
-    // n_pv counts all PVs, including those of a second pass that reads P from shared
-    // memory; np counts P slots.
-    uint32_t rc = 0, n_qk = 0, n_spv = 0, n_pv = 0, n_pass = 0, np = 0;
+    // np counts P slots, n_rs the rescales replayed in second passes that reuse P.  The
+    // last PV of every pass commits o_done, which the epilogue waits for.
+    uint32_t rc = 0, n_qk = 0, n_spv = 0, n_pass = 0, np = 0, n_rs = 0;
     int it_local = 0;
     auto issue_qk = [&]() {
       const uint32_t s_col = C::TM_S + 128 * (n_qk & 1);
       if (n_qk >= 2) point(C::NB_SFREE + (n_qk & 1), &sfree[n_qk & 1], ((n_qk - 2) >> 1) & 1, SITE_PRE_O_DONE);
-      for (int c = 0; c < C::NQC; ++c, ++rc) {
+      for (int c = 0; c < C::NKC; ++c, ++rc) {
         const int slot = rc % NSLOT;
         point(C::NB_SLOT + slot, &kv_full[slot], (rc / NSLOT) & 1, SITE_PRE_KV_FULL);
         if (warp == 1) {
           tc_fence_after();
           if (leader) {
             const uint32_t bsm = ring + slot * C::CHUNK;
+            if constexpr (C::PAIR) {
+              // dims [256 c, 256 c + 256): Q blocks 4c..4c+3, this CTA's 64 keys in 8 KB blocks
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+              for (int h = 0; h < 4; ++h)
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                tc_mma_ss(tbase + s_col, desc_kmajor_sw128(q_s + (2 * c + h) * C::HALF + kk * 32),
-                          desc_kmajor_sw128(bsm + h * C::HALF + kk * 32), ID_QK, (c | h | kk) != 0);
-            tc_commit(&kv_empty[slot]);
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_ss(tbase + s_col, desc_kmajor_sw128(q_s + (4 * c + h) * C::HALF + kk * 32),
+                         desc_kmajor_sw128(bsm + h * C::KBLK + kk * 32), ID_QK, (c | h | kk) != 0);
+            } else {
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                  mma_ss(tbase + s_col, desc_kmajor_sw128(q_s + (2 * c + h) * C::HALF + kk * 32),
+                         desc_kmajor_sw128(bsm + h * C::HALF + kk * 32), ID_QK, (c | h | kk) != 0);
+            }
+            commit_both(&kv_empty[slot]);
           }
         }
       }
-      if (leader) tc_commit(&s_full[n_qk & 1]);
+      if (leader) commit_both(&s_full[n_qk & 1]);
       ++n_qk;
     };
-    auto issue_pv = [&](bool first_of_pass) {
-      point(C::NB_P + (n_pv & 1), &p_full[n_pv & 1], (n_pv >> 1) & 1, SITE_PRE_P_FULL);
+    auto issue_pv = [&](bool first_of_pass, bool last_of_pass) {
+      point(C::NB_P + (n_spv & 1), &p_full[n_spv & 1], (n_spv >> 1) & 1, SITE_PRE_P_FULL);
       const uint32_t p_col = C::TM_S + 128 * (n_spv & 1);
       if (first_of_pass && n_pass > 0) point(C::NB_OFREE, o_free, (n_pass - 1) & 1, SITE_PRE_O_DONE);
-      // one N=128 MMA per 16 keys covers the chunk's 128 output columns
-      for (int c = 0; c < C::NVC; ++c, ++rc) {
+      // one N=128 MMA per 16 keys covers the chunk's 128 output columns (pairs: N=256
+      // over both CTAs' chunks)
+      for (int c = 0; c < C::NVS_P; ++c, ++rc) {
         const int slot = rc % NSLOT;
         point(C::NB_SLOT + slot, &kv_full[slot], (rc / NSLOT) & 1, SITE_PRE_KV_FULL);
         if (warp == 1) {
@@ -676,28 +809,35 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
             const uint32_t bsm = ring + slot * C::CHUNK;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              tc_mma_ts(tbase + C::TM_O + c * 128, tbase + p_col + kk * 8, desc_mnmajor_sw128(bsm + kk * 2048, C::HALF),
-                        ID_PV, (!first_of_pass) || kk > 0);
-            tc_commit(&kv_empty[slot]);
+              mma_ts(tbase + C::TM_O + c * 128, tbase + p_col + kk * 8, desc_mnmajor_sw128(bsm + kk * 2048, C::HALF),
+                     ID_PV, (!first_of_pass) || kk > 0);
+            commit_both(&kv_empty[slot]);
           }
         }
       }
       if (leader) {
-        tc_commit(&sfree[n_spv & 1]);
-        tc_commit(&pv_done[n_pv & 1]);
+        commit_here(&sfree[n_spv & 1]);
+        commit_both(&pv_done[n_spv & 1]);
+        if (last_of_pass) commit_both(o_done);
       }
       ++n_spv;
-      ++n_pv;
       if (first_of_pass) ++n_pass;
     };
-    // second pass with P reuse: P tile j from a P slot (shared memory) times V
-    auto issue_pv_reuse = [&](int j) {
-      point(C::NB_P + (n_pv & 1), &p_full[n_pv & 1], (n_pv >> 1) & 1, SITE_PRE_P_FULL);
+    // second pass with P reuse: P tile j from a P slot (shared memory) times V.  The PVs
+    // follow one another without the softmax, except where the first pass rescaled O
+    // before tile j: then the MMAs so far are committed to o_ready, and the PV waits until
+    // the softmax warps have applied the same factor (resc_done).
+    auto issue_pv_reuse = [&](int j, int last, int tag) {
       if (j == 0) point(C::NB_OFREE, o_free, (n_pass - 1) & 1, SITE_PRE_O_DONE);
+      if (rtag[j] == tag) {
+        if (leader) commit_both(o_ready);
+        point(C::NB_OFREE, resc_done, n_rs & 1, SITE_PRE_P_FULL);
+        ++n_rs;
+      }
       constexpr int NPS = C::NPS > 0 ? C::NPS : 1;
       const int s = np % NPS;
       point(C::NB_PSLOT + s, &pslot_full[s], (np / NPS) & 1, SITE_PRE_KV_FULL);
-      for (int c = 0; c < C::NVC; ++c, ++rc) {
+      for (int c = 0; c < C::NVS_P; ++c, ++rc) {
         const int slot = rc % NSLOT;
         point(C::NB_SLOT + slot, &kv_full[slot], (rc / NSLOT) & 1, SITE_PRE_KV_FULL);
         if (warp == 1) {
@@ -706,24 +846,23 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
             const uint32_t bsm = ring + slot * C::CHUNK, psm = q_s + s * C::CHUNK;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              tc_mma_ss(tbase + C::TM_O + c * 128, desc_kmajor_sw128(psm + (kk >> 2) * C::HALF + (kk & 3) * 32),
-                        desc_mnmajor_sw128(bsm + kk * 2048, C::HALF), ID_PV, (j > 0) || kk > 0);
-            tc_commit(&kv_empty[slot]);
+              mma_ss(tbase + C::TM_O + c * 128, desc_kmajor_sw128(psm + (kk >> 2) * C::HALF + (kk & 3) * 32),
+                     desc_mnmajor_sw128(bsm + kk * 2048, C::HALF), ID_PV, (j > 0) || kk > 0);
+            commit_both(&kv_empty[slot]);
           }
         }
       }
       if (leader) {
-        tc_commit(&pslot_empty[s]);
-        tc_commit(&pv_done[n_pv & 1]);
+        commit_both(&pslot_empty[s]);
+        if (j == last) commit_both(o_done);
       }
-      ++n_pv;
       ++np;
       if (j == 0) ++n_pass;
     };
     for (int r = 0;; ++r, ++it_local) {
-      const int it = prefill_item_at(r);
+      const int it = prefill_item_at<C::PAIR>(r);
       if (it >= n_items) break;
-      const PrefillItemInfo f = prefill_item_info(p, it);
+      const PrefillItemInfo f = prefill_item_info(p, it, rank);
       const bool reuse = item_reuse(f);
       const int steps = reuse ? f.nt : C::NPASS * f.nt;
       point(C::NB_Q, q_full, it_local & 1, SITE_PRE_Q);
@@ -733,13 +872,13 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
         const bool two = k + 1 < steps;
         issue_qk();
         if (two) issue_qk();
-        if (leader && k + (two ? 1 : 0) == steps - 1) tc_commit(q_empty);  // the item's last QK
-        issue_pv(k % f.nt == 0);
-        if (two) issue_pv((k + 1) % f.nt == 0);
+        if (leader && k + (two ? 1 : 0) == steps - 1) commit_both(q_empty);  // the item's last QK
+        issue_pv(k % f.nt == 0, (k + 1) % f.nt == 0);
+        if (two) issue_pv((k + 1) % f.nt == 0, (k + 2) % f.nt == 0);
       }
       if (reuse) {
-        for (int j = 0; j < f.nt; ++j) issue_pv_reuse(j);
-        if (leader) tc_commit(q_empty);  // the P slots (Q region) are free
+        for (int j = 0; j < f.nt; ++j) issue_pv_reuse(j, f.nt - 1, it_local + 1);
+        if (leader) commit_both(q_empty);  // the P slots (Q region) are free
       }
     }
   } else if (warp >= 4) {
@@ -790,15 +929,23 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
       }
       tc_wait_st();
     };
-    // gstep counts PV steps (both passes), sstep the steps that read an S buffer
-    uint32_t gstep = 0, sstep = 0;
+    // sstep counts the steps that read an S buffer, n_epi the epilogues (passes), n_rs the
+    // rescales replayed in second passes that reuse P
+    uint32_t sstep = 0, n_epi = 0, n_rs = 0, n_tags = 0;
+    // arrival on a barrier the MMA issuer waits for (pairs: the first CTA's)
+    auto arrive_lead = [&](uint64_t* b) {
+      if constexpr (C::PAIR) mbar_arrive_cluster(lead(b));
+      else mbar_arrive(b);
+    };
+    int it_local = 0;
     uint8_t* pscr = p.p_scratch + (size_t)blockIdx.x * p.reuse_tiles * C::CHUNK;
     float* mscr = p.m_scratch + (size_t)blockIdx.x * p.reuse_tiles * 128;
-    for (int r = 0;; ++r) {
-      const int it = prefill_item_at(r);
+    for (int r = 0;; ++r, ++it_local) {
+      const int it = prefill_item_at<C::PAIR>(r);
       if (it >= n_items) break;
-      const PrefillItemInfo f = prefill_item_info(p, it);
+      const PrefillItemInfo f = prefill_item_info(p, it, rank);
       const bool reuse = item_reuse(f);
+      const int tag = it_local + 1;
       const int p_local = row / g, h_local = row % g;
       const bool row_ok = (row < g * p.rows_per_tile) && (p_local < f.n_pos);
       const int pos = f.pos0 + p_local;
@@ -808,33 +955,29 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
       float m_used = -INFINITY, l = 0.f;
       for (int pass = 0; pass < C::NPASS; ++pass) {
         if (reuse && pass == 1) {
-          // second pass reusing P: replay the first pass's O rescales, in step with the
-          // PVs; no S.  Waiting for the PV two steps back keeps every pv_done barrier
-          // within one phase of this warp's waits.
-          // this thread wrote the factors itself in the first pass; each is loaded one tile
-          // ahead so its latency overlaps the previous tile
-          float a_next = mscr[row];
-          for (int j = 0; j < f.nt; ++j, ++gstep) {
-            const float a = a_next;
-            if (j + 1 < f.nt) a_next = mscr[(j + 1) * 128 + row];
-            if (gstep >= 2) mbar_wait(&pv_done[gstep & 1], ((gstep - 2) >> 1) & 1, p.err, SITE_PRE_O_DONE);
-            const bool resc = a != 1.f;
-            if (__any_sync(0xffffffffu, resc)) {
-              mbar_wait(&pv_done[(gstep - 1) & 1], ((gstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
-              __syncwarp();
-              tc_fence_after();
-              rescale_o(a);
-            }
+          // second pass reusing P: no S; replay the first pass's O rescales at the tiles
+          // tagged in the first pass (every softmax warp takes part in each, so that the
+          // barrier phases stay in step).  The tags of all warps are visible here: the
+          // first pass's epilogue met at the warpgroups' named barrier after them.  This
+          // thread wrote its factors itself.
+          for (int j = 0; j < f.nt; ++j) {
+            if (rtag[j] != tag) continue;
+            const float a = mscr[j * 128 + row];
+            mbar_wait<C::PAIR>(o_ready, n_rs & 1, p.err, SITE_PRE_O_DONE);
+            ++n_rs;
+            __syncwarp();
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, a != 1.f)) rescale_o(a);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[gstep & 1]);
+            if (lane == 0) arrive_lead(resc_done);
           }
         } else {
           m_used = -INFINITY;
           l = 0.f;
-          for (int jt = 0; jt < f.nt; ++jt, ++gstep, ++sstep) {
+          for (int jt = 0; jt < f.nt; ++jt, ++sstep) {
             const uint32_t s_col = C::TM_S + 128 * (sstep & 1);
-            mbar_wait(&s_full[sstep & 1], (sstep >> 1) & 1, p.err, SITE_PRE_S_FULL);
+            mbar_wait<C::PAIR>(&s_full[sstep & 1], (sstep >> 1) & 1, p.err, SITE_PRE_S_FULL);
             __syncwarp();  // the tcgen05 loads below are warp-collective
             tc_fence_after();
             uint32_t sr[NCOL];
@@ -893,10 +1036,14 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
             // when any of its rows needs it, the other rows with a factor of 1, once the PV
             // of the previous step has finished with O
             if (__any_sync(0xffffffffu, resc)) {
-              mbar_wait(&pv_done[(gstep - 1) & 1], ((gstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
+              mbar_wait<C::PAIR>(&pv_done[(sstep - 1) & 1], ((sstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
               __syncwarp();
               tc_fence_after();
               rescale_o(resc ? alpha : 1.f);
+              if (reuse && lane == 0) {  // the second pass replays this rescale (pairs: in both CTAs)
+                rtag[jt] = tag;
+                if constexpr (C::PAIR) st_shared_cluster_u32(mapa_shared(smem_u32(&rtag[jt]), rank ^ 1), (uint32_t)tag);
+              }
             }
             if (resc) l *= alpha;
             l += sum;
@@ -905,7 +1052,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
             tc_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[gstep & 1]);
+            if (lane == 0) arrive_lead(&p_full[sstep & 1]);
             if (reuse) {
               // after the PV may start: this thread's keys of P tile jt in the shared-memory
               // image the second pass's MMAs read (128B-swizzled blocks of 64 keys), and the
@@ -927,11 +1074,23 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
             fence_proxy_async_global();
             __syncwarp();
             if (lane == 0) mbar_arrive(ps_done);
+            if constexpr (C::PAIR) {
+              // both CTAs' rescale tags of the item are in both copies before either CTA's
+              // second pass reads them
+              if (lane == 0) {
+                mbar_arrive_cluster(mapa_shared(smem_u32(tags_done), 0));
+                mbar_arrive_cluster(mapa_shared(smem_u32(tags_done), 1));
+              }
+              mbar_wait<true>(tags_done, n_tags & 1, p.err, SITE_PRE_P_FULL);
+              ++n_tags;
+            }
           }
         }
         // ---- epilogue of this pass: O / l -> bf16
+        static_assert(C::NPASS == 1 || C::QUANT || C::SMW == 2, "P reuse orders the rescale tags through the warpgroups' barrier");
         const float lt = combine(l, false);
-        mbar_wait(&pv_done[(gstep - 1) & 1], ((gstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
+        mbar_wait<C::PAIR>(o_done, n_epi & 1, p.err, SITE_PRE_O_DONE);
+        ++n_epi;
         __syncwarp();
         tc_fence_after();
         const float inv = lt > 0.f ? v_scale / lt : 0.f;
@@ -954,7 +1113,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(o_free);
+        if (lane == 0) arrive_lead(o_free);
         if (pass == C::NPASS - 1 && row_ok && p.lse && wg == 0)
           p.lse[(size_t)(f.q_row0 + p_local) * p.Hq + hq] =
               lt > 0.f ? (m_used + log2f(lt)) * 0.69314718055994531f : -INFINITY;
@@ -962,12 +1121,17 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT>::THREADS, 1)
     }
   }
   tc_fence_before();
-  __syncthreads();
+  // pairs: neither CTA leaves (or frees TMEM) while the other may still reach its shared
+  // memory or barriers
+  if constexpr (C::PAIR) cluster_sync_all();
+  else __syncthreads();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tbase, 512);
+    if constexpr (C::PAIR) tmem_dealloc_pair(tbase, 512);
+    else tmem_dealloc(tbase, 512);
   }
+  if constexpr (C::PAIR) cluster_sync_all();
 }
 
 }  // namespace pa

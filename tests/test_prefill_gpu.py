@@ -43,24 +43,50 @@ def _id(c):
             f"-qo{'_'.join(map(str, c[6]))}-c{c[7]}-w{c[8]}")
 
 
+@pytest.fixture(params=["pairs", "single"])
+def cta_mode(request):
+    """bf16 prefill on one CTA per query tile (the default) and on CTA pairs."""
+    ensure_built()
+    pa.paged_attn_set_prefill_cta_pairs(1 if request.param == "pairs" else -1)
+    yield "_pair" if request.param == "pairs" else ""
+    pa.paged_attn_set_prefill_cta_pairs(-1)
+
+
 @pytest.mark.parametrize("c", CASES, ids=[_id(c) for c in CASES])
-def test_prefill_parity(c):
+def test_prefill_parity(c, cta_mode):
     dqk, dvo, hq, hkv, ps, kv, qo, causal, win = c
     case = synth.make_case("prefill", batch=len(kv), Hq=hq, Hkv=hkv, d_qk=dqk, d_vo=dvo, page_size=ps,
                            kv_lens=kv, qo_lens=qo, causal=causal, window_left=win, seed=500 + len(kv))
-    check_full(case, _id(c))
-    assert pa.paged_attn_last_variant() == f"prefill_{dqk}x{dvo}_bf16"
+    check_full(case, _id(c) + cta_mode)
+    assert pa.paged_attn_last_variant() == f"prefill_{dqk}x{dvo}{cta_mode}_bf16"
 
 
 @pytest.mark.parametrize("q_gain", [8.0, 32.0])
-def test_prefill_rescale_replay(q_gain):
+def test_prefill_rescale_replay(q_gain, cta_mode):
     """Large scores make the running maximum jump by more than 2^8 between KV tiles, so the
     first pass rescales O; with head_dim_vo 512 the second pass replays those rescales
     while reusing P.  q is scaled by a power of two (exact in bf16)."""
     case = synth.make_case("prefill", batch=2, Hq=8, Hkv=2, d_qk=512, d_vo=512, page_size=16,
                            kv_lens=[700, 333], qo_lens=[260, 333], seed=77)
     case.q = (case.q.float() * q_gain).to(case.q.dtype)
-    check_full(case, f"q x {q_gain}")
+    check_full(case, f"q x {q_gain}{cta_mode}")
+
+
+def test_prefill_cta_pairs_setter_rejects_other_modes():  # noqa: D103
+    ensure_built()
+    for bad in (2, -2):
+        with pytest.raises(pa.PagedAttnError) as e:
+            pa.paged_attn_set_prefill_cta_pairs(bad)
+        assert e.value.status == pa.PA_ERR_INVALID_ARG
+
+
+def test_prefill_pairs_on_the_dequantised_copy(cta_mode, _dequant_limit):
+    """NVFP4 pages through the bf16 copy, on CTA pairs and on single CTAs."""
+    pa.paged_attn_set_prefill_dequant_limit(-1)
+    case = synth.make_case("prefill", batch=2, Hq=16, Hkv=2, d_qk=512, d_vo=256, page_size=32,
+                           kv_lens=[300, 100], qo_lens=[300, 100], kv_dtype=synth.KV_NVFP4, seed=602)
+    check_full(case, "nvfp4 copy" + cta_mode)
+    assert pa.paged_attn_last_variant() == f"prefill_512x256{cta_mode}_nvfp4_dequant"
 
 
 def test_prefill_small_pages_are_refused():  # noqa: D103
