@@ -90,11 +90,11 @@ struct PrefillCfg {
   // NPS slots of the Q region (Q is not needed by then)
   static constexpr int NPS = NPASS == 2 ? Q_BYTES / CHUNK : 0;
   // barriers: q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_free, aux, sfree[2],
-  // ps_done, o_done, o_ready, resc_done, tags_done, kv_full[], kv_empty[], stg_full[], stg_empty[],
+  // ps_done, o_done, o_ready, resc_done, tags_done, qreg_free, kv_full[], kv_empty[], stg_full[], stg_empty[],
   // sf_full[], sf_empty[], pslot_full[], pslot_empty[].  Every waiter of a barrier is at
   // most one phase behind or ahead of it (a parity wait cannot tell more apart): hence one
   // s_full / p_full / pv_done / sfree per S buffer.
-  static constexpr int NB_FIXED = 17;
+  static constexpr int NB_FIXED = 18;
   static constexpr int NBAR = NB_FIXED + 2 * NSLOT + 2 * NSTG + 2 * NSF + 2 * NPS;
   static constexpr int BYTES = OFF_BAR + NBAR * 8 + 16;
   static constexpr int ALLOC = BYTES + 1024;
@@ -308,6 +308,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
   uint64_t* o_ready = bars + 14;  // P reuse: the PVs before a replayed rescale are complete
   uint64_t* resc_done = bars + 15;  // P reuse: the softmax warps rescaled O
   uint64_t* tags_done = bars + 16;  // CTA pairs: both CTAs' rescale tags of an item are written
+  uint64_t* qreg_free = bars + 17;  // P reuse: the item's last QK is done (P slots may fill)
   uint64_t* kv_full = bars + C::NB_FIXED;
   uint64_t* kv_empty = kv_full + NSLOT;
   uint64_t* stg_full = kv_full + 2 * NSLOT;
@@ -339,6 +340,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     mbar_init(o_ready, 1);
     mbar_init(resc_done, 4 * C::SMW * C::CL);
     mbar_init(tags_done, 4 * C::SMW * C::CL);
+    mbar_init(qreg_free, 1);
     for (int s = 0; s < C::NPS; ++s) {
       mbar_init(&pslot_full[s], C::CL);
       mbar_init(&pslot_empty[s], 1);
@@ -387,7 +389,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
     }
-    uint32_t rc = 0, aux_phase = 0, qe = 0, psd = 0, np = 0;
+    uint32_t rc = 0, aux_phase = 0, qe = 0;
     const uint64_t pol_kv = l2_policy_evict_last(), pol_q = l2_policy_evict_first();
     for (int r = 0;; ++r) {
       const int it = prefill_item_at<C::PAIR>(r);
@@ -511,30 +513,47 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
         pg_b = pg_d;
       }
       if (reuse) {
-        // second pass: P tile j of the first pass (into a P slot of the Q region, free once
-        // the last QK of the item is done) and V of the upper output half
+        // second pass: V of the upper output half (the P tiles come from warp 3)
         mbar_wait<C::PAIR>(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
-        mbar_wait(ps_done, psd++ & 1, p.err, SITE_PRE_P_FULL);
-        const uint8_t* pscr = p.p_scratch + (size_t)blockIdx.x * p.reuse_tiles * C::CHUNK;
         int pg = step_pages(f.nt);
-        for (int j = 0; j < f.nt; ++j, ++np) {
+        for (int j = 0; j < f.nt; ++j) {
           const int pg_n = step_pages(f.nt + j + 1);
-          constexpr int NPS = C::NPS > 0 ? C::NPS : 1;
-          const int s = np % NPS;
-          mbar_wait<C::PAIR>(&pslot_empty[s], ((np / NPS) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
-          if (lane == 0) {
-            if constexpr (C::PAIR) {
-              mbar_arrive_expect_tx_cluster(lead(&pslot_full[s]), (uint32_t)C::CHUNK);
-              tma_load_2d_pair(q_s + s * C::CHUNK, &tm_p, 0, ((int)blockIdx.x * p.reuse_tiles + j) * 256,
-                               lead(&pslot_full[s]), pol_q);
-            } else {
-              mbar_arrive_expect_tx(&pslot_full[s], (uint32_t)C::CHUNK);
-              bulk_load_g2s(q_s + s * C::CHUNK, pscr + (size_t)j * C::CHUNK, (uint32_t)C::CHUNK, &pslot_full[s]);
-            }
-          }
           emit(false, f.nt + j, pg);
           pg = pg_n;
         }
+      }
+    }
+  } else if (warp == 3 && C::NPASS == 2 && !C::QUANT) {
+    // ------------------------------------------- P tiles of second passes (lane 0 of warp 3)
+    // The first pass's P tiles of an item (usually back from HBM) go into the P slots of the
+    // Q region once the item's last QK is done and the softmax has written them; up to NPS
+    // tiles ahead of the PVs, independently of the V chunks in the ring.
+    constexpr int NPS = C::NPS > 0 ? C::NPS : 1;
+    const uint8_t* pscr = p.p_scratch + (size_t)blockIdx.x * p.reuse_tiles * C::CHUNK;
+    const uint64_t pol_p = l2_policy_evict_first();
+    uint32_t np = 0, n_reuse = 0;
+    for (int r = 0;; ++r) {
+      const int it = prefill_item_at<C::PAIR>(r);
+      if (it >= n_items) break;
+      const PrefillItemInfo f = prefill_item_info(p, it, rank);
+      if (!item_reuse(f)) continue;
+      mbar_wait<C::PAIR>(qreg_free, n_reuse & 1, p.err, SITE_PRE_Q);
+      mbar_wait(ps_done, n_reuse & 1, p.err, SITE_PRE_P_FULL);
+      ++n_reuse;
+      for (int j = 0; j < f.nt; ++j, ++np) {
+        const int s = np % NPS;
+        mbar_wait<C::PAIR>(&pslot_empty[s], ((np / NPS) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
+        if (lane == 0) {
+          if constexpr (C::PAIR) {
+            mbar_arrive_expect_tx_cluster(lead(&pslot_full[s]), (uint32_t)C::CHUNK);
+            tma_load_2d_pair(q_s + s * C::CHUNK, &tm_p, 0, ((int)blockIdx.x * p.reuse_tiles + j) * 256,
+                             lead(&pslot_full[s]), pol_p);
+          } else {
+            mbar_arrive_expect_tx(&pslot_full[s], (uint32_t)C::CHUNK);
+            bulk_load_g2s(q_s + s * C::CHUNK, pscr + (size_t)j * C::CHUNK, (uint32_t)C::CHUNK, &pslot_full[s]);
+          }
+        }
+        __syncwarp();
       }
     }
   } else if (warp == 0) {
@@ -872,7 +891,10 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
         const bool two = k + 1 < steps;
         issue_qk();
         if (two) issue_qk();
-        if (leader && k + (two ? 1 : 0) == steps - 1) commit_both(q_empty);  // the item's last QK
+        if (leader && k + (two ? 1 : 0) == steps - 1) {  // the item's last QK
+          commit_both(q_empty);
+          if (reuse) commit_both(qreg_free);
+        }
         issue_pv(k % f.nt == 0, (k + 1) % f.nt == 0);
         if (two) issue_pv((k + 1) % f.nt == 0, (k + 2) % f.nt == 0);
       }
