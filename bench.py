@@ -398,6 +398,71 @@ def bench_prefill(name, steps, warmup, gpu_index, pk, with_cpu=False):
     return res
 
 
+# ------------------------------------------------------------------------- append
+APPEND_WORKLOADS = {
+    # name: (kv dtype, sequences, new tokens each, kv heads, d_qk, d_vo, page_size)
+    "append_nvfp4_asym": (synth.KV_NVFP4, 64, 1024, 2, 512, 256, 32),
+    "append_fp8_gqa": (synth.KV_FP8, 128, 512, 4, 512, 512, 16),
+}
+
+
+def append_bytes(kv_dtype, total, hkv, dqk, dvo) -> int:
+    """bf16 rows read + converted rows (and NVFP4 block scales) written."""
+    elems = total * hkv * (dqk + dvo)
+    out = elems * _beta_x2(kv_dtype) // 2 + (elems // 16 if kv_dtype == synth.KV_NVFP4 else 0)
+    return elems * 2 + out
+
+
+def bench_append(name, steps, warmup, gpu_index, pk):
+    """paged_attn_append_kv writing whole sequences of new tokens into an empty cache."""
+    import numpy as np
+    import paged_gqa_attention_hd512_gb300 as pa
+
+    kvt, nseq, ntok, hkv, dqk, dvo, ps = APPEND_WORKLOADS[name]
+    total = nseq * ntok
+    pages_per = -(-ntok // ps)
+    num_pages = nseq * pages_per
+    dev = "cuda"
+    perm = torch.from_numpy(np.random.default_rng(4242).permutation(num_pages).astype(np.int32))
+    kv_indices = perm.to(dev)
+    kv_indptr = torch.arange(0, num_pages + 1, pages_per, dtype=torch.int32, device=dev)
+    last = torch.full((nseq,), (ntok - 1) % ps + 1, dtype=torch.int32, device=dev)
+    append_indptr = torch.arange(0, total + 1, ntok, dtype=torch.int32, device=dev)
+    k_new = synth.normal_bf16(4242, 1, 0, total * hkv * dqk, dev).view(total, hkv, dqk)
+    v_new = synth.normal_bf16(4242, 2, 0, total * hkv * dvo, dev).view(total, hkv, dvo)
+    page_bytes = hkv * ps * (dqk + dvo) * _beta_x2(kvt) // 2
+    cache = torch.zeros(num_pages * page_bytes, dtype=torch.uint8, device=dev)
+    sf = torch.zeros(num_pages * hkv * ps * (dqk + dvo) // 16, dtype=torch.uint8, device=dev) \
+        if kvt == synth.KV_NVFP4 else None
+    ks = torch.tensor([2.0 ** -8 if kvt == synth.KV_NVFP4 else 0.02], dtype=torch.float32, device=dev)
+    vs = ks.clone()
+
+    def step():
+        pa.paged_attn_append_kv(k_new, v_new, append_indptr, cache, kv_indptr, kv_indices, last, page_size=ps,
+                                kv_dtype=kvt, k_scale=ks, v_scale=vs, sf=sf, num_pages=num_pages)
+
+    step()
+    torch.cuda.synchronize()
+    if pa.paged_attn_check_device_error() != 0:
+        raise RuntimeError("device error word set after the first append call")
+    nbytes = append_bytes(kvt, total, hkv, dqk, dvo)
+    with ClockSampler(gpu_index) as clk:
+        pa.paged_attn_profile_begin(steps)
+        ms = time_region(step, steps, warmup)
+        n_k, k_ms = pa.paged_attn_profile_end()
+    kern_ms = k_ms / max(1, n_k)
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    res = {"workload": name, "ms_per_step": ms / steps, "value": nbytes / (ms / steps * 1e-3) / 1e9, "unit": "GB/s",
+           "bytes_per_step": nbytes, "variant": pa.paged_attn_last_variant(), "clocks": clk.summary(),
+           "l2": f"{nbytes / 1e6:.0f} MB per step, larger than L2", "gpu_launches": steps,
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk[0]["hbm_gbs"], "unit": "GB/s",
+                        "frac": achieved / pk[0]["hbm_gbs"], "traffic": None, "kernel": "append_kv_kernel",
+                        "kernel_ms": kern_ms, "launches_timed": n_k, "peak_source": f"{pk[1]} hbm_gbs"}}
+    del k_new, v_new, cache, sf
+    torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------------------------- main
 def main():
     ap = argparse.ArgumentParser()
@@ -469,6 +534,8 @@ def main():
             extra.append(bench_decode(name, max(3, args.steps // 10), args.warmup, barrier, local, pk,
                                       with_e2e=False, with_cpu=False))
         extra.append(bench_prefill("nvfp4_asym_prefill", max(3, min(50, args.steps // 40)), 3, local, pk))
+        for name in APPEND_WORKLOADS:
+            extra.append(bench_append(name, max(3, args.steps // 10), args.warmup, local, pk))
         line["secondary"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)

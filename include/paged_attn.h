@@ -148,6 +148,48 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q,
                        int causal, int kv_dtype, const pa_kv_scales* kv_scales, void* out,
                        float* lse, void* stream);
 
+/*
+ * paged_attn_append_kv -- write the K and V of new tokens (bf16) into the paged cache,
+ * converted to the cache's element type (quantise-on-write): the step that produces the
+ * FP8 / NVFP4 caches the attention calls read ("feat(attention): asymmetric VO-split NVFP4
+ * paged prefill (qk=512/vo=256) for Gemma-4 on SM120/121", validation on caches written by
+ * an in-tree NVFP4 KV quantisation kernel from bf16 sources).
+ *
+ * k_new [total_new, num_kv_heads, head_dim_qk] and v_new [total_new, num_kv_heads,
+ * head_dim_vo] bf16, rows append_indptr[b]..append_indptr[b+1] belonging to sequence b
+ * (append_indptr int32 [batch + 1], append_indptr[batch] = total_new).  The page table
+ * (kv_indptr, kv_indices, kv_last_page_len) describes each sequence after the append: its
+ * last n_b = append_indptr[b+1] - append_indptr[b] tokens are the new ones, so new row j
+ * of sequence b goes to position t = kv_len_b - n_b + j, page kv_indices[kv_indptr[b] +
+ * t / page_size], slot t % page_size, in the cache layout paged_attn_decode reads.
+ * Nothing else in the cache or the scale pool is written.
+ *
+ * Conversion of a bf16 value x (as fp32), with correctly rounded fp32 operations in
+ * this order; a code carries the sign of its operand, also when it rounds to zero:
+ *   PA_KV_BF16      x copied;
+ *   PA_KV_FP8_E4M3  e4m3 code of x / s, round to nearest even, saturating at +-448;
+ *                   s = *k_scale for K, *v_scale for V (per-tensor fp32, on the device);
+ *   PA_KV_NVFP4     per block of 16 consecutive head-dim elements of one token and head,
+ *                   with the global scale G = *k_scale or *v_scale: amax = max |x|,
+ *                   sf = e4m3 code of (amax / 6) / G (nearest even, saturating), d =
+ *                   value(sf) * G; codes = e2m1 of x / d (nearest even, saturating at +-6),
+ *                   or 0 when d = 0; sf goes to the block-scale pool `sf` (layout as in
+ *                   pa_kv_scales.sf), the codes two per byte, element 2i in the low nibble.
+ * k_scale / v_scale (device fp32 scalars) are required for FP8 and NVFP4 and ignored for
+ * bf16; sf is required for NVFP4 and ignored otherwise.  The caller owns every buffer.
+ * k_new, v_new and kv_cache must be 16-byte aligned.  A new row whose position falls
+ * outside its sequence (n_b > kv_len_b) or whose page id is outside [0, num_pages) is
+ * skipped and sets the device error word (paged_attn_check_device_error).
+ * Returns PA_OK, or PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED / PA_ERR_ALIGNMENT /
+ * PA_ERR_CUDA; nothing is launched on error.
+ */
+int paged_attn_append_kv(const void* k_new, const void* v_new, const int32_t* append_indptr,
+                         int total_new, void* kv_cache, const int32_t* kv_indptr,
+                         const int32_t* kv_indices, const int32_t* kv_last_page_len, int batch,
+                         int num_pages, int num_kv_heads, int head_dim_qk, int head_dim_vo,
+                         int page_size, int kv_dtype, const float* k_scale,
+                         const float* v_scale, uint8_t* sf, void* stream);
+
 /* Human-readable text of a pa_status value (static storage, never NULL). */
 const char* paged_attn_status_string(int status);
 

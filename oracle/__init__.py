@@ -73,6 +73,14 @@ def _bind(lib):
         _u8p, _i32p, _i32p, _i32p, _u8p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_int,
         ctypes.c_int, ctypes.c_int, _f64p]
+    lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+    lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.oracle_e2m1_encode.restype = ctypes.c_uint8
+    lib.oracle_e2m1_encode.argtypes = [ctypes.c_float]
+    lib.oracle_append_kv.restype = ctypes.c_int
+    lib.oracle_append_kv.argtypes = [
+        _u16p, _u16p, _i32p, _u8p, _i32p, _i32p, _i32p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_float, _u8p]
     return lib
 
 
@@ -200,3 +208,44 @@ def e4m3_value(code: int, lib=None) -> float:
 
 def e2m1_value(nibble: int, lib=None) -> float:
     return (lib or load()).oracle_e2m1_value(nibble)
+
+
+# ------------------------------------------------------------------ append (quantise-on-write)
+def e4m3_encode(x, lib=None) -> np.ndarray:
+    """fp32 values -> e4m3 codes (nearest, ties to even, saturating, sign kept)."""
+    lib = lib or load()
+    a = np.asarray(x, dtype=np.float32).ravel()
+    return np.array([lib.oracle_e4m3_encode(float(v)) for v in a], dtype=np.uint8)
+
+
+def e2m1_encode(x, lib=None) -> np.ndarray:
+    """fp32 values -> e2m1 codes in [0, 15] (nearest, ties to even, saturating, sign kept)."""
+    lib = lib or load()
+    a = np.asarray(x, dtype=np.float32).ravel()
+    return np.array([lib.oracle_e2m1_encode(float(v)) for v in a], dtype=np.uint8)
+
+
+def append_kv(k_new, v_new, append_indptr, kv_cache, kv_indptr, kv_indices, kv_last_page_len, *,
+              num_kv_heads: int, head_dim_qk: int, head_dim_vo: int, page_size: int, kv_dtype: int,
+              k_scale: float = 1.0, v_scale: float = 1.0, sf=None, lib=None):
+    """The cache (and NVFP4 scale pool) after writing the new rows; inputs are not modified.
+
+    Returns (cache bytes, scale-pool bytes or None, rows skipped)."""
+    lib = lib or load()
+    kn = _np(k_new, np.uint16).ravel()
+    vn = _np(v_new, np.uint16).ravel()
+    ai = _np(append_indptr, np.int32)
+    cache = _np(kv_cache, np.uint8).ravel().copy()
+    ip = _np(kv_indptr, np.int32)
+    ix = _np(kv_indices, np.int32)
+    lp = _np(kv_last_page_len, np.int32)
+    sfa = _np(sf, np.uint8).ravel().copy() if sf is not None else None
+    x2 = {0: 4, 1: 2, 2: 1}[kv_dtype]
+    page_bytes = num_kv_heads * page_size * (head_dim_qk + head_dim_vo) * x2 // 2
+    num_pages = cache.size // page_bytes
+    skipped = lib.oracle_append_kv(
+        _ptr(kn, ctypes.c_uint16), _ptr(vn, ctypes.c_uint16), _ptr(ai, ctypes.c_int32),
+        _ptr(cache, ctypes.c_uint8), _ptr(ip, ctypes.c_int32), _ptr(ix, ctypes.c_int32),
+        _ptr(lp, ctypes.c_int32), ai.size - 1, num_pages, num_kv_heads, head_dim_qk, head_dim_vo,
+        page_size, kv_dtype, float(k_scale), float(v_scale), _ptr(sfa, ctypes.c_uint8))
+    return cache, sfa, skipped

@@ -285,3 +285,129 @@ int oracle_gather(const uint8_t* kv_cache, const int32_t* kv_indptr, const int32
     for (int d = 0; d < dim; ++d) dst[j * dim + d] = kv_element(&kv, b, kvh, j, is_v, d);
   return (int)kv_len;
 }
+
+/* ================================================================ append (quantise-on-write)
+ *
+ * Writes the K and V rows of new tokens (bf16) into the cache as the last tokens of each
+ * sequence, converted to the cache's element type.  The step that produces the FP8 /
+ * NVFP4 caches read above ("feat(attention): asymmetric VO-split NVFP4 paged prefill
+ * (qk=512/vo=256) for Gemma-4 on SM120/121": caches quantised from bf16 sources by an
+ * in-tree NVFP4 KV quantisation kernel; "[None][feat] Run Gemma4 head_dim 512 attention on
+ * Triton", Approach: FP8 KV with per-tensor scales).  The pages name the step but not its
+ * rounding; the reading used here (stated with the C ABI):
+ *   FP8    code = e4m3(x / s), nearest, ties to even, saturating at +-448;
+ *   NVFP4  per 16 consecutive head-dim elements of one token and head, global scale G:
+ *          amax = max |x|, sf = e4m3((amax / 6) / G), d = value(sf) * G,
+ *          code = e2m1(x / d) (nearest, ties to even, saturating at +-6), 0 when d = 0.
+ * Every arithmetic step is one fp32 operation in this order (the precision the codes are
+ * decided in); the rounding to a code is decided exactly, in double, by comparing the
+ * fp32 operand with every representable magnitude.  A code carries the operand's sign,
+ * also when it rounds to zero.
+ * ==================================================================================== */
+
+/* Nearest of the n increasing non-negative magnitudes vals[0..n-1] to a >= 0, ties to the
+ * even index (the code whose mantissa ends in 0); at or above vals[n-1]: n - 1. */
+static int nearest_code(double a, const double* vals, int n) {
+  if (a >= vals[n - 1]) return n - 1;
+  int best = 0;
+  double bd = fabs(a - vals[0]);
+  for (int c = 1; c < n; ++c) {
+    double dd = fabs(a - vals[c]);
+    if (dd < bd || (dd == bd && (c & 1) == 0)) {
+      best = c;
+      bd = dd;
+    }
+  }
+  return best;
+}
+
+static double g_e4m3_mag[127];
+static double g_e2m1_mag[8];
+static int g_tables_ready = 0;
+
+static void build_tables(void) {
+  if (g_tables_ready) return;
+  for (int c = 0; c < 127; ++c) g_e4m3_mag[c] = oracle_e4m3_value((uint8_t)c);  /* 0x7F is NaN */
+  for (int c = 0; c < 8; ++c) g_e2m1_mag[c] = oracle_e2m1_value((uint8_t)c);
+  g_tables_ready = 1;
+}
+
+uint8_t oracle_e4m3_encode(float v) {
+  build_tables();
+  int code = nearest_code(fabs((double)v), g_e4m3_mag, 127);
+  return (uint8_t)(code | (signbit(v) ? 0x80 : 0));
+}
+
+uint8_t oracle_e2m1_encode(float v) {
+  build_tables();
+  int code = nearest_code(fabs((double)v), g_e2m1_mag, 8);
+  return (uint8_t)(code | (signbit(v) ? 0x8 : 0));
+}
+
+static float bf16_float(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* Returns the number of new rows skipped because their position falls outside the
+ * sequence or their page id outside [0, num_pages). */
+int oracle_append_kv(const uint16_t* k_new, const uint16_t* v_new, const int32_t* append_indptr,
+                     uint8_t* kv_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
+                     const int32_t* kv_last_page_len, int batch, int num_pages, int Hkv, int d_qk,
+                     int d_vo, int page_size, int kv_dtype, float k_scale, float v_scale,
+                     uint8_t* sf) {
+  build_tables();
+  const int64_t x2 = kv_dtype == KV_BF16 ? 4 : (kv_dtype == KV_FP8_E4M3 ? 2 : 1);
+  const int64_t rows = (int64_t)Hkv * page_size;
+  const int64_t k_row = (int64_t)d_qk * x2 / 2, v_row = (int64_t)d_vo * x2 / 2;
+  const int64_t page_bytes = rows * (k_row + v_row);
+  const int64_t sf_page = rows * (d_qk / 16 + d_vo / 16);
+  int skipped = 0;
+  for (int b = 0; b < batch; ++b) {
+    int n = append_indptr[b + 1] - append_indptr[b];
+    int np = kv_indptr[b + 1] - kv_indptr[b];
+    int64_t kv_len = np > 0 ? (int64_t)(np - 1) * page_size + kv_last_page_len[b] : 0;
+    for (int j = 0; j < n; ++j) {
+      int64_t i = append_indptr[b] + j;      /* new row */
+      int64_t t = kv_len - n + j;            /* its position in the sequence */
+      if (t < 0 || t >= kv_len) { ++skipped; continue; }
+      int page = kv_indices[kv_indptr[b] + t / page_size];
+      if (page < 0 || page >= num_pages) { ++skipped; continue; }
+      int64_t slot = t % page_size;
+      for (int h = 0; h < Hkv; ++h)
+        for (int is_v = 0; is_v < 2; ++is_v) {
+          int dim = is_v ? d_vo : d_qk;
+          const uint16_t* src = (is_v ? v_new : k_new) + (i * Hkv + h) * dim;
+          int64_t row = (int64_t)h * page_size + slot;
+          uint8_t* dst = kv_cache + page * page_bytes + (is_v ? rows * k_row + row * v_row : row * k_row);
+          float s = is_v ? v_scale : k_scale;
+          if (kv_dtype == KV_BF16) {
+            memcpy(dst, src, (size_t)dim * 2);
+          } else if (kv_dtype == KV_FP8_E4M3) {
+            for (int d = 0; d < dim; ++d) dst[d] = oracle_e4m3_encode(bf16_float(src[d]) / s);
+          } else {
+            uint8_t* sfd = sf + page * sf_page + (is_v ? rows * (d_qk / 16) + row * (d_vo / 16) : row * (d_qk / 16));
+            for (int blk = 0; blk < dim / 16; ++blk) {
+              float x[16], amax = 0.0f;
+              for (int e = 0; e < 16; ++e) {
+                x[e] = bf16_float(src[blk * 16 + e]);
+                float a = fabsf(x[e]);
+                if (a > amax) amax = a;
+              }
+              uint8_t sfc = oracle_e4m3_encode((amax / 6.0f) / s);
+              float dd = (float)oracle_e4m3_value(sfc) * s;
+              sfd[blk] = sfc;
+              for (int e = 0; e < 16; e += 2) {
+                uint8_t lo = dd != 0.0f ? oracle_e2m1_encode(x[e] / dd) : 0;
+                uint8_t hi = dd != 0.0f ? oracle_e2m1_encode(x[e + 1] / dd) : 0;
+                dst[blk * 8 + e / 2] = (uint8_t)(lo | (hi << 4));
+              }
+            }
+          }
+        }
+    }
+  }
+  return skipped;
+}

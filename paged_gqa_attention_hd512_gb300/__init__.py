@@ -31,7 +31,8 @@ EXPORTED = ("paged_attn_decode", "paged_attn_prefill", "paged_attn_status_string
             "paged_attn_release_workspace", "paged_attn_check_device_error",
             "paged_attn_set_decode_chunk_pages", "paged_attn_last_variant",
             "paged_attn_profile_begin", "paged_attn_profile_end", "paged_attn_decode_noalloc",
-            "paged_attn_set_prefill_dequant_limit", "paged_attn_set_prefill_cta_pairs")
+            "paged_attn_set_prefill_dequant_limit", "paged_attn_set_prefill_cta_pairs",
+            "paged_attn_append_kv")
 
 _lib = None
 
@@ -64,6 +65,9 @@ def load(path: Optional[str] = None):
     lib.paged_attn_prefill.restype = i32
     lib.paged_attn_prefill.argtypes = [vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                        f32, i32, i32, i32, ctypes.POINTER(_Scales), vp, vp, vp]
+    lib.paged_attn_append_kv.restype = i32
+    lib.paged_attn_append_kv.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                         vp, vp, vp, vp]
     lib.paged_attn_status_string.restype = ctypes.c_char_p
     lib.paged_attn_status_string.argtypes = [i32]
     lib.paged_attn_release_workspace.restype = i32
@@ -199,6 +203,27 @@ def paged_attn_prefill(q: torch.Tensor, qo_indptr: torch.Tensor, kv_cache: torch
     if st != PA_OK:
         raise PagedAttnError(st, "paged_attn_prefill")
     return out, lse
+
+
+def paged_attn_append_kv(k_new: torch.Tensor, v_new: torch.Tensor, append_indptr: torch.Tensor,
+                         kv_cache: torch.Tensor, kv_indptr: torch.Tensor, kv_indices: torch.Tensor,
+                         kv_last_page_len: torch.Tensor, *, page_size: int, kv_dtype: int = PA_KV_BF16,
+                         k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                         sf: Optional[torch.Tensor] = None, num_pages: Optional[int] = None,
+                         stream=None) -> None:
+    """Write k_new [total_new, Hkv, head_dim_qk] / v_new [total_new, Hkv, head_dim_vo] (bf16)
+    as the last tokens of each sequence, converted to the cache's element type."""
+    total_new, hkv, dqk = k_new.shape
+    dvo = v_new.shape[2]
+    batch = append_indptr.numel() - 1
+    if num_pages is None:
+        num_pages = _num_pages(kv_cache, hkv, dqk, dvo, page_size, kv_dtype)
+    st = load().paged_attn_append_kv(_ptr(k_new), _ptr(v_new), _ptr(append_indptr), total_new, _ptr(kv_cache),
+                                     _ptr(kv_indptr), _ptr(kv_indices), _ptr(kv_last_page_len), batch,
+                                     num_pages, hkv, dqk, dvo, page_size, kv_dtype, _ptr(k_scale),
+                                     _ptr(v_scale), _ptr(sf), _stream(stream))
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_append_kv")
 
 
 def paged_attn_release_workspace() -> None:

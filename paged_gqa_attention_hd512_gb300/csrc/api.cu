@@ -543,6 +543,65 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   return PA_OK;
 }
 
+
+int paged_attn_append_kv(const void* k_new, const void* v_new, const int32_t* append_indptr, int total_new,
+                         void* kv_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
+                         const int32_t* kv_last_page_len, int batch, int num_pages, int num_kv_heads,
+                         int head_dim_qk, int head_dim_vo, int page_size, int kv_dtype, const float* k_scale,
+                         const float* v_scale, uint8_t* sf, void* stream) {
+  if (batch < 0 || total_new < 0 || num_pages < 1 || num_kv_heads < 1) return PA_ERR_INVALID_ARG;
+  if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3 && kv_dtype != PA_KV_NVFP4) return PA_ERR_INVALID_ARG;
+  if (!((head_dim_qk == 512 && head_dim_vo == 512) || (head_dim_qk == 512 && head_dim_vo == 256) ||
+        (head_dim_qk == 256 && head_dim_vo == 256)))
+    return PA_ERR_UNSUPPORTED;
+  if (page_size < 1 || page_size > 64 || (page_size & (page_size - 1))) return PA_ERR_UNSUPPORTED;
+  if (batch == 0 || total_new == 0) return PA_OK;
+  if (!k_new || !v_new || !append_indptr || !kv_cache || !kv_indptr || !kv_indices || !kv_last_page_len)
+    return PA_ERR_INVALID_ARG;
+  if (kv_dtype != PA_KV_BF16) {
+    if (!k_scale || !v_scale) return PA_ERR_INVALID_ARG;
+    if (!aligned(k_scale, 4) || !aligned(v_scale, 4)) return PA_ERR_ALIGNMENT;
+  }
+  if (kv_dtype == PA_KV_NVFP4 && !sf) return PA_ERR_INVALID_ARG;
+  if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(kv_cache, 16)) return PA_ERR_ALIGNMENT;
+  if (!aligned(append_indptr, 4) || !aligned(kv_indptr, 4) || !aligned(kv_indices, 4) ||
+      !aligned(kv_last_page_len, 4))
+    return PA_ERR_ALIGNMENT;
+  const uint64_t page_bytes =
+      (uint64_t)num_kv_heads * page_size * (head_dim_qk + head_dim_vo) * x2_of(kv_dtype) / 2;
+  if ((uint64_t)num_pages * page_bytes >= (1ull << 46)) return PA_ERR_INVALID_ARG;
+  int st = PA_OK;
+  char* ws = static_cast<char*>(workspace(kFixedBytes, &st));
+  if (!ws) return st;
+  AppendParams p;
+  std::memset(&p, 0, sizeof p);
+  p.k_new = static_cast<const uint16_t*>(k_new);
+  p.v_new = static_cast<const uint16_t*>(v_new);
+  p.append_indptr = append_indptr;
+  p.kv_indptr = kv_indptr;
+  p.kv_indices = kv_indices;
+  p.kv_last_page_len = kv_last_page_len;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.cache = static_cast<uint8_t*>(kv_cache);
+  p.sf = sf;
+  p.err = reinterpret_cast<int*>(ws + kErrOffset);
+  p.batch = batch;
+  p.total_new = total_new;
+  p.num_pages = num_pages;
+  p.Hkv = num_kv_heads;
+  p.d_qk = head_dim_qk;
+  p.d_vo = head_dim_vo;
+  p.page_size = page_size;
+  prof_mark(static_cast<cudaStream_t>(stream), true);
+  const cudaError_t e = launch_append_kv(kv_dtype, p, static_cast<cudaStream_t>(stream));
+  prof_mark(static_cast<cudaStream_t>(stream), false);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};
+  std::snprintf(g_variant, sizeof g_variant, "append_kv_%s", kv_names[kv_dtype]);
+  return PA_OK;
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------------------

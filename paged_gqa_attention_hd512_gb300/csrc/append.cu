@@ -1,0 +1,155 @@
+// append.cu -- write new tokens' K and V into the paged cache, converting them to the
+// cache's element type on the way (quantise-on-write).
+//
+// The step before attention: the pages' NVFP4 prefill is validated on caches written by
+// an in-tree NVFP4 KV quantisation kernel from bf16 sources ("feat(attention): asymmetric
+// VO-split NVFP4 paged prefill (qk=512/vo=256) for Gemma-4 on SM120/121", commit
+// "support-or-reject-explicitly" notes), and FP8 KV is a per-tensor-scaled e4m3 cache
+// that the attention kernels cast on load ("[None][feat] Run Gemma4 head_dim 512
+// attention on Triton", Approach).  Element formats and page layout are those the
+// attention calls read:
+//   bf16   copied;
+//   FP8    code = e4m3(x / scale), round to nearest even, saturating at +-448;
+//   NVFP4  per 16 consecutive head-dim elements of one token and head:
+//          sf = e4m3((amax / 6) / global), d = value(sf) * global,
+//          code = e2m1(x / d) (nearest even, saturating at +-6), or 0 when d is 0;
+//          two codes per byte, element 2i in the low nibble.
+// A code carries the sign of its operand, also when the magnitude rounds to zero.
+// Every operation is a correctly rounded fp32 operation in this order, so the codes are
+// a function of the inputs alone.
+//
+// One CTA per new token; each thread converts 16-element units (32 bytes of bf16), so a
+// warp reads 1 KB of consecutive input.
+#include "launch.h"
+#include "common.cuh"
+
+namespace pa {
+
+namespace {
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }
+
+// two fp32 -> two e4m3 codes (low byte: a), RNE, saturating
+__device__ __forceinline__ uint32_t f32x2_to_e4m3x2(float a, float b) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(b), "f"(a));
+  return r;
+}
+// two fp32 -> one byte of e2m1 codes (low nibble: a), RNE, saturating
+__device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float a, float b) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r)
+      : "f"(b), "f"(a));
+  return r;
+}
+// one code with the sign of v (also for results that round to zero), magnitude RNE and
+// saturating
+__device__ __forceinline__ uint32_t e4m3_code(float v) {
+  return (f32x2_to_e4m3x2(fabsf(v), 0.f) & 0x7Fu) | ((__float_as_uint(v) >> 24) & 0x80u);
+}
+__device__ __forceinline__ uint32_t e2m1_code(float v) {
+  return (f32x2_to_e2m1x2(fabsf(v), 0.f) & 0x7u) | ((__float_as_uint(v) >> 28) & 0x8u);
+}
+__device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
+  const uint32_t h2 = e4m3x2_to_f16x2(code & 0xFFu);
+  return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
+template <int KVT>
+__global__ void __launch_bounds__(256) append_kv_kernel(const AppendParams p) {
+  __shared__ int s_b;
+  const int i = blockIdx.x;  // new token
+  if (threadIdx.x == 0) {
+    int lo = 0, hi = p.batch - 1;  // last b with append_indptr[b] <= i
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (p.append_indptr[mid] <= i) lo = mid; else hi = mid - 1;
+    }
+    s_b = lo;
+  }
+  __syncthreads();
+  const int b = s_b;
+  const int n_new = p.append_indptr[b + 1] - p.append_indptr[b];
+  const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
+  const int kv_len = np > 0 ? (np - 1) * p.page_size + p.kv_last_page_len[b] : 0;
+  const int t = kv_len - n_new + (i - p.append_indptr[b]);  // position in the sequence
+  int page = -1;
+  if (t >= 0 && t < kv_len) page = p.kv_indices[p.kv_indptr[b] + t / p.page_size];
+  if (page < 0 || page >= p.num_pages) {
+    if (threadIdx.x == 0) record_error(p.err, SITE_APPEND_POS);
+    return;
+  }
+  const int slot = t % p.page_size;
+  const int ku = p.d_qk / 16, vu = p.d_vo / 16, units = p.Hkv * (ku + vu);
+  // element widths in bytes x2: bf16 4, fp8 2, nvfp4 1
+  constexpr int X2 = KVT == KV_BF16 ? 4 : (KVT == KV_FP8 ? 2 : 1);
+  const size_t rows = (size_t)p.Hkv * p.page_size;
+  const size_t k_row = (size_t)p.d_qk * X2 / 2, v_row = (size_t)p.d_vo * X2 / 2;
+  uint8_t* page_base = p.cache + (size_t)page * rows * (k_row + v_row);
+  const size_t sf_page = rows * (size_t)(ku + vu);
+  float ks = 1.f, vs = 1.f;
+  if (KVT != KV_BF16) {
+    ks = __ldg(p.k_scale);
+    vs = __ldg(p.v_scale);
+  }
+  for (int u = threadIdx.x; u < units; u += blockDim.x) {
+    const int h = u / (ku + vu), w = u % (ku + vu);
+    const bool is_k = w < ku;
+    const int blk = is_k ? w : w - ku;
+    const uint16_t* src = is_k ? p.k_new + ((size_t)i * p.Hkv + h) * p.d_qk + blk * 16
+                               : p.v_new + ((size_t)i * p.Hkv + h) * p.d_vo + blk * 16;
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
+    const uint4 c = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+    const size_t row = (size_t)h * p.page_size + slot;
+    uint8_t* dst = page_base + (is_k ? row * k_row : rows * k_row + row * v_row) + (size_t)blk * 16 * X2 / 2;
+    if constexpr (KVT == KV_BF16) {
+      reinterpret_cast<uint4*>(dst)[0] = a;
+      reinterpret_cast<uint4*>(dst)[1] = c;
+    } else {
+      const uint32_t wv[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+      float x[16];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        x[2 * k] = bf16_to_f32(wv[k] & 0xFFFFu);
+        x[2 * k + 1] = bf16_to_f32(wv[k] >> 16);
+      }
+      const float scale = is_k ? ks : vs;
+      if constexpr (KVT == KV_FP8) {
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int k = 0; k < 16; ++k) o[k >> 2] |= e4m3_code(__fdiv_rn(x[k], scale)) << (8 * (k & 3));
+        *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
+      } else {
+        float amax = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(x[k]));
+        const uint32_t sf_code = e4m3_code(__fdiv_rn(__fdiv_rn(amax, 6.f), scale));
+        const float d = __fmul_rn(e4m3_to_f32(sf_code), scale);
+        uint32_t o[2] = {0u, 0u};
+        if (d != 0.f) {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) o[k >> 3] |= e2m1_code(__fdiv_rn(x[k], d)) << (4 * (k & 7));
+        }
+        *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
+        uint8_t* sfp = p.sf + (size_t)page * sf_page + (is_k ? row * ku : rows * ku + row * vu) + blk;
+        *sfp = (uint8_t)sf_code;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_append_kv(int kvt, const AppendParams& p, cudaStream_t s) {
+  if (p.total_new == 0) return cudaSuccess;
+  const int units = p.Hkv * (p.d_qk + p.d_vo) / 16;
+  const int threads = units >= 256 ? 256 : ((units + 31) / 32) * 32;
+  if (kvt == KV_BF16) append_kv_kernel<KV_BF16><<<p.total_new, threads, 0, s>>>(p);
+  else if (kvt == KV_FP8) append_kv_kernel<KV_FP8><<<p.total_new, threads, 0, s>>>(p);
+  else if (kvt == KV_NVFP4) append_kv_kernel<KV_NVFP4><<<p.total_new, threads, 0, s>>>(p);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -21,6 +21,7 @@ enum {
   SITE_PRE_DEQ = 208,
   SITE_PRE_STG = 209,
   SITE_PRE_SF = 210,
+  SITE_APPEND_POS = 301,  // append: more new tokens than the sequence holds, or a page id out of range
 };
 
 // Decode work list entry: one page-aligned chunk of one sequence.
@@ -102,6 +103,23 @@ struct DequantParams {
   const int32_t* kv_indices;
   uint16_t* shadow;      // bf16 pages, same page index
   int batch, Hkv, page_size;
+};
+
+// New tokens' K / V (bf16) -> the paged cache, converted to the cache's element type
+// (see append.cu)
+struct AppendParams {
+  const uint16_t* k_new;  // bf16 [total_new, Hkv, d_qk]
+  const uint16_t* v_new;  // bf16 [total_new, Hkv, d_vo]
+  const int32_t* append_indptr;  // [batch + 1]
+  const int32_t* kv_indptr;
+  const int32_t* kv_indices;
+  const int32_t* kv_last_page_len;
+  const float* k_scale;  // FP8: per-tensor scale; NVFP4: global scale (device scalars)
+  const float* v_scale;
+  uint8_t* cache;        // pages in the cache's element type
+  uint8_t* sf;           // NVFP4 block-scale pool (same page indexing)
+  int* err;
+  int batch, total_new, num_pages, Hkv, d_qk, d_vo, page_size;
 };
 
 }  // namespace pa

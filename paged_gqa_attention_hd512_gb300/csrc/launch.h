@@ -41,6 +41,8 @@ cudaError_t launch_prefill_plan(const PrefillParams& p, cudaStream_t s);
 int prefill_smem_bytes(int kvt, int dqk, int dvo);
 // Two-CTA clusters of the bf16 prefill kernel that fit on the device at once.
 int prefill_pair_clusters(int dqk, int dvo);
+// New tokens' bf16 K / V -> the paged cache in its element type (quantise-on-write).
+cudaError_t launch_append_kv(int kvt, const AppendParams& p, cudaStream_t s);
 // FP8 / NVFP4 pages referenced by kv_indices -> bf16 pages of the same index.
 cudaError_t launch_prefill_dequant(int kvt, int dqk, int dvo, const DequantParams& d, int grid, cudaStream_t s);
 
