@@ -35,7 +35,7 @@ def _rank_main(rank, world, port, out):
 def test_two_gloo_ranks_take_the_slowest_time():
     world = 2
     port = _free_port()
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()  # no fork of this (threaded) process
     mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
     for r in range(world):
         slowest, value = out[r]
