@@ -149,6 +149,29 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q,
                        float* lse, void* stream);
 
 /*
+ * paged_attn_prefill_custom_mask -- paged_attn_prefill with a custom mask ("[None][feat]
+ * Run Gemma4 head_dim 512 attention on Triton", Approach: prefill is causal when no custom
+ * mask is given; the multimodal Gemma layers attend bidirectionally inside spans of the
+ * new tokens).  New token i (0 <= i < qo_len) of sequence b may attend key j
+ * (0 <= j < kv_len) only when bit mask_indptr[b] * 8 + i * kv_len + j of custom_mask is 1
+ * (bit k of a byte is its 2^k bit): each sequence's qo_len x kv_len row-major bit grid
+ * starts at byte offset mask_indptr[b] (int64, device, [batch] or more entries).  The mask
+ * narrows the causal and window rules (pass causal = 0 for a mask that replaces the causal
+ * rule); a row with no allowed key gives out = 0 and lse = -inf.  custom_mask is read only
+ * where bits of allowed-by-causal/window keys lie; mask_indptr must be 8-byte aligned.
+ * Everything else as paged_attn_prefill.
+ */
+int paged_attn_prefill_custom_mask(const void* q, const int32_t* qo_indptr, int total_q,
+                                   const void* kv_cache, const int32_t* kv_indptr,
+                                   const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                                   int batch, int num_pages, int num_qo_heads, int num_kv_heads,
+                                   int head_dim_qk, int head_dim_vo, int page_size,
+                                   float sm_scale, int window_left, int causal, int kv_dtype,
+                                   const pa_kv_scales* kv_scales, void* out, float* lse,
+                                   const uint8_t* custom_mask, const int64_t* mask_indptr,
+                                   void* stream);
+
+/*
  * paged_attn_append_kv -- write the K and V of new tokens (bf16) into the paged cache,
  * converted to the cache's element type (quantise-on-write): the step that produces the
  * FP8 / NVFP4 caches the attention calls read ("feat(attention): asymmetric VO-split NVFP4

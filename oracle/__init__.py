@@ -65,7 +65,7 @@ def _bind(lib):
         _u16p, _i32p, _u8p, _i32p, _i32p, _i32p, _u8p,
         ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_int,
-        ctypes.c_int, ctypes.c_int64, _i64p, _i32p, _i64p, _i64p, _f64p, _f64p, ctypes.c_int]
+        ctypes.c_int, ctypes.c_int64, _i64p, _i32p, _i64p, _i64p, _u8p, _i64p, _f64p, _f64p, ctypes.c_int]
     lib.oracle_merge.restype = None
     lib.oracle_merge.argtypes = [ctypes.c_int, _f64p, _f64p, ctypes.c_int, _f64p, _f64p]
     lib.oracle_gather.restype = ctypes.c_int
@@ -128,7 +128,8 @@ def default_threads() -> int:
 def rows(case, row_tok: Sequence[int], row_head: Sequence[int], key_lo=None, key_hi=None,
          threads: Optional[int] = None, lib=None):
     """fp64 attention output for the given (query token, query head) rows of ``case``
-    (a synth.Case).  Returns (out [n, d_vo], lse [n])."""
+    (a synth.Case; an optional ``mask`` / ``mask_indptr`` attribute pair is the custom
+    mask).  Returns (out [n, d_vo], lse [n])."""
     lib = lib or load()
     q = _np(case.q, np.uint16).reshape(-1)
     qo = _np(case.qo_indptr, np.int32)
@@ -141,6 +142,9 @@ def rows(case, row_tok: Sequence[int], row_head: Sequence[int], key_lo=None, key
     rh = np.ascontiguousarray(np.asarray(row_head, dtype=np.int32))
     klo = np.ascontiguousarray(np.asarray(key_lo, dtype=np.int64)) if key_lo is not None else None
     khi = np.ascontiguousarray(np.asarray(key_hi, dtype=np.int64)) if key_hi is not None else None
+    cm = getattr(case, "mask", None)
+    mask = _np(cm, np.uint8).reshape(-1) if cm is not None else None
+    mip = _np(case.mask_indptr, np.int64) if cm is not None else None
     n = rt.shape[0]
     out = np.zeros((n, case.d_vo), dtype=np.float64)
     lse = np.zeros((n,), dtype=np.float64)
@@ -150,7 +154,8 @@ def rows(case, row_tok: Sequence[int], row_head: Sequence[int], key_lo=None, key
         _ptr(sf, ctypes.c_uint8), case.batch, case.Hq, case.Hkv, case.d_qk, case.d_vo,
         case.page_size, case.kv_dtype, case.k_scale, case.v_scale, case.sm_scale,
         case.window_left, case.causal, n, _ptr(rt, ctypes.c_int64), _ptr(rh, ctypes.c_int32),
-        _ptr(klo, ctypes.c_int64), _ptr(khi, ctypes.c_int64), _ptr(out, ctypes.c_double),
+        _ptr(klo, ctypes.c_int64), _ptr(khi, ctypes.c_int64), _ptr(mask, ctypes.c_uint8),
+        _ptr(mip, ctypes.c_int64), _ptr(out, ctypes.c_double),
         _ptr(lse, ctypes.c_double), threads or default_threads())
     if rc != 0:
         raise ValueError("oracle_rows rejected its arguments")

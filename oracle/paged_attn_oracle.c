@@ -162,6 +162,12 @@ static int find_seq(const int32_t* qo_indptr, int batch, int64_t tok) {
  *  row_tok[n], row_head[n]   which rows to compute
  *  key_lo/key_hi  optional per-row restriction of keys to [key_lo, key_hi) (NULL = all);
  *                 used to form split-K partials
+ *  mask, mask_indptr  optional custom mask (NULL = none): for sequence b, query row i
+ *                 (0 <= i < qo_len) may attend key j only when bit mask_indptr[b] * 8 +
+ *                 i * kv_len + j of the byte array `mask` is 1 (bit k of a byte is its
+ *                 2^k bit); it narrows the causal / window rules, it does not replace them.
+ *                 ("[None][feat] Run Gemma4 head_dim 512 attention on Triton", Approach:
+ *                 prefill is causal when no custom mask is given.)
  *  out [n][d_vo], lse [n]    fp64 results
  * Returns 0, or -1 on a malformed argument.
  */
@@ -171,7 +177,8 @@ int oracle_rows(const uint16_t* q, const int32_t* qo_indptr, const uint8_t* kv_c
                 int d_qk, int d_vo, int page_size, int kv_dtype, double k_scale, double v_scale,
                 double sm_scale, int window_left, int causal, int64_t n_rows,
                 const int64_t* row_tok, const int32_t* row_head, const int64_t* key_lo,
-                const int64_t* key_hi, double* out, double* lse, int n_threads) {
+                const int64_t* key_hi, const uint8_t* mask, const int64_t* mask_indptr,
+                double* out, double* lse, int n_threads) {
   if (batch <= 0 || Hkv <= 0 || Hq % Hkv != 0 || page_size <= 0 || d_qk <= 0 || d_vo <= 0)
     return -1;
   if (kv_dtype == KV_NVFP4 && (sf == NULL || d_qk % 16 || d_vo % 16)) return -1;
@@ -222,6 +229,10 @@ int oracle_rows(const uint16_t* q, const int32_t* qo_indptr, const uint8_t* kv_c
         int allowed = (j >= lo && j < hi);
         if (causal && j > pos) allowed = 0;
         if (window_left >= 0 && j < pos - window_left) allowed = 0;
+        if (mask) {
+          int64_t bit = mask_indptr[b] * 8 + i * kv_len + j;
+          if (!((mask[bit >> 3] >> (bit & 7)) & 1)) allowed = 0;
+        }
         if (!allowed) { s[j] = -INFINITY; continue; }
         double dot = 0.0;
         for (int d = 0; d < d_qk; ++d) dot += oracle_bf16_value(qrow[d]) * K[j * d_qk + d];

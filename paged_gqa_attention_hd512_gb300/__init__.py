@@ -32,7 +32,7 @@ EXPORTED = ("paged_attn_decode", "paged_attn_prefill", "paged_attn_status_string
             "paged_attn_set_decode_chunk_pages", "paged_attn_last_variant",
             "paged_attn_profile_begin", "paged_attn_profile_end", "paged_attn_decode_noalloc",
             "paged_attn_set_prefill_dequant_limit", "paged_attn_set_prefill_cta_pairs",
-            "paged_attn_append_kv")
+            "paged_attn_append_kv", "paged_attn_prefill_custom_mask")
 
 _lib = None
 
@@ -68,6 +68,8 @@ def load(path: Optional[str] = None):
     lib.paged_attn_append_kv.restype = i32
     lib.paged_attn_append_kv.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                          vp, vp, vp, vp]
+    lib.paged_attn_prefill_custom_mask.restype = i32
+    lib.paged_attn_prefill_custom_mask.argtypes = list(lib.paged_attn_prefill.argtypes[:-1]) + [vp, vp, vp]
     lib.paged_attn_status_string.restype = ctypes.c_char_p
     lib.paged_attn_status_string.argtypes = [i32]
     lib.paged_attn_release_workspace.restype = i32
@@ -184,8 +186,11 @@ def paged_attn_prefill(q: torch.Tensor, qo_indptr: torch.Tensor, kv_cache: torch
                        v_scale: Optional[torch.Tensor] = None, sf: Optional[torch.Tensor] = None,
                        out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
                        num_pages: Optional[int] = None, stream=None,
-                       return_lse: bool = True) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
-    """Prefill: q [total_q, Hq, head_dim_qk] bf16 -> out [total_q, Hq, head_dim_vo] bf16."""
+                       return_lse: bool = True, custom_mask: Optional[torch.Tensor] = None,
+                       mask_indptr: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Prefill: q [total_q, Hq, head_dim_qk] bf16 -> out [total_q, Hq, head_dim_vo] bf16.
+    custom_mask (uint8 bits) with mask_indptr (int64 byte offsets per sequence) selects
+    paged_attn_prefill_custom_mask."""
     total_q, hq, dqk = q.shape
     batch = qo_indptr.numel() - 1
     if num_pages is None:
@@ -195,13 +200,17 @@ def paged_attn_prefill(q: torch.Tensor, qo_indptr: torch.Tensor, kv_cache: torch
     if lse is None and return_lse:
         lse = torch.empty(total_q, hq, dtype=torch.float32, device=q.device)
     sc = _scales(kv_dtype, k_scale, v_scale, sf)
-    st = load().paged_attn_prefill(_ptr(q), _ptr(qo_indptr), total_q, _ptr(kv_cache), _ptr(kv_indptr),
-                                   _ptr(kv_indices), _ptr(kv_last_page_len), batch, num_pages, hq,
-                                   num_kv_heads, dqk, head_dim_vo, page_size, float(sm_scale),
-                                   window_left, int(bool(causal)), kv_dtype, ctypes.byref(sc), _ptr(out),
-                                   _ptr(lse), _stream(stream))
+    args = (_ptr(q), _ptr(qo_indptr), total_q, _ptr(kv_cache), _ptr(kv_indptr), _ptr(kv_indices),
+            _ptr(kv_last_page_len), batch, num_pages, hq, num_kv_heads, dqk, head_dim_vo, page_size,
+            float(sm_scale), window_left, int(bool(causal)), kv_dtype, ctypes.byref(sc), _ptr(out), _ptr(lse))
+    if custom_mask is not None:
+        st = load().paged_attn_prefill_custom_mask(*args, _ptr(custom_mask), _ptr(mask_indptr), _stream(stream))
+        what = "paged_attn_prefill_custom_mask"
+    else:
+        st = load().paged_attn_prefill(*args, _stream(stream))
+        what = "paged_attn_prefill"
     if st != PA_OK:
-        raise PagedAttnError(st, "paged_attn_prefill")
+        raise PagedAttnError(st, what)
     return out, lse
 
 
@@ -295,6 +304,9 @@ def case_args(case) -> dict:
         kw["v_scale"] = torch.tensor([case.v_scale], dtype=torch.float32, device=dev)
         if case.kv_dtype == PA_KV_NVFP4:
             kw["sf"] = case.sf
+    if case.phase == "prefill" and getattr(case, "mask", None) is not None:
+        kw["custom_mask"] = case.mask
+        kw["mask_indptr"] = case.mask_indptr
     return kw
 
 

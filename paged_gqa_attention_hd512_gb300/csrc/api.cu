@@ -398,11 +398,16 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
   return PA_OK;
 }
 
-int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, const void* kv_cache,
-                       const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* kv_last_page_len,
-                       int batch, int num_pages, int num_qo_heads, int num_kv_heads, int head_dim_qk,
-                       int head_dim_vo, int page_size, float sm_scale, int window_left, int causal, int kv_dtype,
-                       const pa_kv_scales* kv_scales, void* out, float* lse, void* stream) {
+}  // extern "C"
+
+namespace {
+// paged_attn_prefill and paged_attn_prefill_custom_mask (mask == nullptr: none)
+int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const void* kv_cache,
+                 const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* kv_last_page_len, int batch,
+                 int num_pages, int num_qo_heads, int num_kv_heads, int head_dim_qk, int head_dim_vo,
+                 int page_size, float sm_scale, int window_left, int causal, int kv_dtype,
+                 const pa_kv_scales* kv_scales, void* out, float* lse, const uint8_t* mask,
+                 const int64_t* mask_indptr, void* stream) {
   int st = check_common(q, kv_cache, kv_indptr, kv_indices, kv_last_page_len, batch, num_pages, num_qo_heads,
                         num_kv_heads, head_dim_qk, head_dim_vo, page_size, sm_scale, window_left, kv_dtype,
                         kv_scales, out, lse);
@@ -512,6 +517,8 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   p.num_pages = num_pages;
   p.rows_per_tile = rows_per_tile;
   p.pair = pair_grid > 0 ? 1 : 0;
+  p.mask = mask;
+  p.mask_indptr = mask_indptr;
   p.max_items = (int)max_items;
   p.box_rows = page_size;
   p.swz = 7;
@@ -539,8 +546,36 @@ int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, con
   prof_mark(L.stream, false);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};
-  std::snprintf(g_variant, sizeof g_variant, "%s_%s%s", name, kv_names[kv_dtype], dequant ? "_dequant" : "");
+  std::snprintf(g_variant, sizeof g_variant, "%s_%s%s%s", name, kv_names[kv_dtype], dequant ? "_dequant" : "",
+                mask ? "_mask" : "");
   return PA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q, const void* kv_cache,
+                       const int32_t* kv_indptr, const int32_t* kv_indices, const int32_t* kv_last_page_len,
+                       int batch, int num_pages, int num_qo_heads, int num_kv_heads, int head_dim_qk,
+                       int head_dim_vo, int page_size, float sm_scale, int window_left, int causal, int kv_dtype,
+                       const pa_kv_scales* kv_scales, void* out, float* lse, void* stream) {
+  return prefill_call(q, qo_indptr, total_q, kv_cache, kv_indptr, kv_indices, kv_last_page_len, batch, num_pages,
+                      num_qo_heads, num_kv_heads, head_dim_qk, head_dim_vo, page_size, sm_scale, window_left, causal,
+                      kv_dtype, kv_scales, out, lse, nullptr, nullptr, stream);
+}
+
+int paged_attn_prefill_custom_mask(const void* q, const int32_t* qo_indptr, int total_q, const void* kv_cache,
+                                   const int32_t* kv_indptr, const int32_t* kv_indices,
+                                   const int32_t* kv_last_page_len, int batch, int num_pages, int num_qo_heads,
+                                   int num_kv_heads, int head_dim_qk, int head_dim_vo, int page_size, float sm_scale,
+                                   int window_left, int causal, int kv_dtype, const pa_kv_scales* kv_scales,
+                                   void* out, float* lse, const uint8_t* custom_mask, const int64_t* mask_indptr,
+                                   void* stream) {
+  if (!custom_mask || !mask_indptr) return PA_ERR_INVALID_ARG;
+  if (!aligned(mask_indptr, 8)) return PA_ERR_ALIGNMENT;
+  return prefill_call(q, qo_indptr, total_q, kv_cache, kv_indptr, kv_indices, kv_last_page_len, batch, num_pages,
+                      num_qo_heads, num_kv_heads, head_dim_qk, head_dim_vo, page_size, sm_scale, window_left, causal,
+                      kv_dtype, kv_scales, out, lse, custom_mask, mask_indptr, stream);
 }
 
 

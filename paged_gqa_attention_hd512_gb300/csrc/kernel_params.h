@@ -89,6 +89,10 @@ struct PrefillParams {
   int batch, total_q, Hq, Hkv, group, page_size, window_left, causal, num_pages;
   int rows_per_tile;  // query positions per 128-row tile (128 / group)
   int pair;           // 1: items span two tiles, computed by the two CTAs of a cluster
+  // optional custom mask: bit mask_indptr[b] * 8 + i * kv_len + j (bit k of a byte is
+  // its 2^k bit) lets new token i of sequence b attend key j; nullptr = none
+  const uint8_t* mask;
+  const int64_t* mask_indptr;
   int max_items;
   int box_rows;
   int swz;

@@ -271,6 +271,26 @@ __device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams
   return f;
 }
 
+// Bits [s, s + n) of a little-endian bit array (bit k of the result = bit s + k; n <= 0
+// gives 0, n is clamped to 64).  Only the bytes that hold those bits are read.
+__device__ __forceinline__ uint64_t load_mask_bits(const uint8_t* m, int64_t s, int n) {
+  if (n <= 0) return 0;
+  n = min(n, 64);
+  const int64_t b0 = s >> 3, b1 = (s + n - 1) >> 3;
+  const int sh = (int)(s & 7);
+  uint64_t lo = 0;
+  uint32_t top = 0;
+  for (int64_t b = b0; b <= b1; ++b) {
+    const uint32_t v = __ldg(m + b);
+    const int k = (int)(b - b0);
+    if (k < 8) lo |= (uint64_t)v << (8 * k);
+    else top = v;
+  }
+  uint64_t r = lo >> sh;
+  if (sh) r |= (uint64_t)top << (64 - sh);
+  return n < 64 ? r & ((1ull << n) - 1) : r;
+}
+
 // r-th item of this CTA (or CTA pair): rounds of one item per CTA (pair), alternating
 // direction, over a list sorted by descending cost.
 template <bool PAIR>
@@ -974,6 +994,10 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       const int khi = p.causal ? pos : f.kv_len - 1;
       const int klo = p.window_left >= 0 ? pos - p.window_left : 0;
       const int hq = f.kvh * g + h_local;
+      // custom mask: bit index of (this row, key 0)
+      const int64_t mbase = (p.mask != nullptr && row_ok)
+                                ? p.mask_indptr[f.b] * 8 + (int64_t)(f.q_begin + p_local) * f.kv_len
+                                : 0;
       float m_used = -INFINITY, l = 0.f;
       for (int pass = 0; pass < C::NPASS; ++pass) {
         if (reuse && pass == 1) {
@@ -1018,17 +1042,44 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
 #pragma unroll
               for (int i = 0; i < NCOL; ++i) sr[i] = __float_as_uint(__uint_as_float(sr[i]) * scale_log2);
             }
-            if (__all_sync(0xffffffffu, (lo <= 0) & (hi >= NCOL - 1))) {
-#pragma unroll
-              for (int i = 0; i < NCOL; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[i]));
-            } else {
+            // the row maximum over the visible keys of this thread's columns, masked scores
+            // set to -inf; a tile every row of the warp sees in full skips the mask
+            auto mask_and_max = [&](const uint32_t* mw, bool use_mw) {
 #pragma unroll
               for (int i = 0; i < NCOL; ++i) {
-                const bool ok = (i >= lo) & (i <= hi);
+                const bool ok = (i >= lo) & (i <= hi) & (use_mw ? ((mw[i >> 5] >> (i & 31)) & 1u) != 0u : true);
                 const float x = ok ? __uint_as_float(sr[i]) : -INFINITY;
                 sr[i] = __float_as_uint(x);
                 mx4[i & 3] = fmaxf(mx4[i & 3], x);
               }
+            };
+            auto plain_max = [&]() {
+#pragma unroll
+              for (int i = 0; i < NCOL; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[i]));
+            };
+            if (p.mask == nullptr) {
+              if (__all_sync(0xffffffffu, (lo <= 0) & (hi >= NCOL - 1))) plain_max();
+              else mask_and_max(nullptr, false);
+            } else {
+              // custom-mask bits of this row's columns (1 = may attend; all ones for rows
+              // that are not written)
+              uint32_t mw[NCOL / 32];
+#pragma unroll
+              for (int c = 0; c < NCOL / 32; ++c) mw[c] = 0xffffffffu;
+              if (row_ok) {
+                const int nvalid = max(0, min(NCOL, f.kv_len - key0));
+#pragma unroll
+                for (int c = 0; c < NCOL / 64; ++c) {
+                  const uint64_t w = load_mask_bits(p.mask, mbase + key0 + 64 * c, nvalid - 64 * c);
+                  mw[2 * c] = (uint32_t)w;
+                  mw[2 * c + 1] = (uint32_t)(w >> 32);
+                }
+              }
+              bool all_ok = true;
+#pragma unroll
+              for (int c = 0; c < NCOL / 32; ++c) all_ok &= mw[c] == 0xffffffffu;
+              if (__all_sync(0xffffffffu, (lo <= 0) & (hi >= NCOL - 1) & all_ok)) plain_max();
+              else mask_and_max(mw, true);
             }
             const float mx =
                 combine(fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])), true) * eff_scale;

@@ -208,6 +208,10 @@ class Case:
     kv_lens: List[int]
     qo_lens: List[int]
     meta: Dict = field(default_factory=dict)
+    # optional prefill custom mask: per sequence b, bit (byte offset mask_indptr[b]) * 8 +
+    # i * kv_len + j (little-endian within bytes) lets query row i attend key j
+    mask: Optional[torch.Tensor] = None
+    mask_indptr: Optional[torch.Tensor] = None
 
     @property
     def total_q(self) -> int:
@@ -226,7 +230,8 @@ class Case:
 
     def to(self, device) -> "Case":
         c = Case(**{k: getattr(self, k) for k in self.__dataclass_fields__})
-        for k in ("q", "qo_indptr", "kv_cache", "kv_indptr", "kv_indices", "kv_last_page_len", "sf"):
+        for k in ("q", "qo_indptr", "kv_cache", "kv_indptr", "kv_indices", "kv_last_page_len", "sf", "mask",
+                  "mask_indptr"):
             v = getattr(self, k)
             if v is not None:
                 setattr(c, k, v.to(device))

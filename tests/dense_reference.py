@@ -71,6 +71,12 @@ def attention_row(case, tok: int, h: int, key_range=None):
         ok &= j >= pos - case.window_left
     if key_range is not None:
         ok &= (j >= key_range[0]) & (j < key_range[1])
+    cm = getattr(case, "mask", None)
+    if cm is not None:  # custom mask: numpy's little-endian unpacking of the sequence's bits
+        m = cm.cpu().numpy() if hasattr(cm, "cpu") else np.asarray(cm)
+        off = int(np.asarray(case.mask_indptr.cpu() if hasattr(case.mask_indptr, "cpu") else case.mask_indptr)[b])
+        bits = np.unpackbits(m[off:off + (qo_len * L + 7) // 8], bitorder="little")
+        ok &= bits[i * L:(i + 1) * L].astype(bool)
     if not ok.any():
         return np.zeros(case.d_vo), -np.inf
     s = (K[ok] @ q) * case.sm_scale

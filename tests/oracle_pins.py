@@ -18,6 +18,7 @@ import torch
 import oracle
 import synth
 from dense_reference import E2M1_TABLE, attention_row, seq_kv
+from mask_cases import attach as attach_mask
 
 REL = 1e-12
 
@@ -257,6 +258,66 @@ def pin_empty_sequence(lib):
     assert np.all(out[:2] == 0.0) and np.all(np.isneginf(lse[:2]))
     o_ref, l_ref = attention_row(c, 1, 0)
     _close(out[2], o_ref, what="row after empty sequence")
+
+
+# ------------------------------------------------------------------------- custom masks
+def pin_dense_custom_mask(lib):
+    """Random, span and sparse masks against the dense reference (numpy's bit unpacking)."""
+    for n, (kind, causal) in enumerate((("random", 0), ("spans", 1), ("sparse_rows", 0), ("random", 1))):
+        c = synth.make_case("prefill", batch=2, Hq=4, Hkv=2, d_qk=32, d_vo=32, page_size=8,
+                            kv_lens=[21, 9], qo_lens=[6, 9], causal=causal, seed=40 + n)
+        attach_mask(c, kind, 70 + n)
+        _check_dense(c, lib, f"custom mask {kind} causal={causal}")
+
+
+def pin_mask_all_ones_changes_nothing(lib):
+    c = synth.make_case("prefill", batch=2, Hq=2, Hkv=1, d_qk=32, d_vo=16, page_size=4,
+                        kv_lens=[13, 6], qo_lens=[5, 6], causal=0, window_left=4, seed=45)
+    tok, head = _all_rows(c)
+    ref_o, ref_l = oracle.rows(c, tok, head, lib=lib, threads=1)
+    attach_mask(c, "all", 1)
+    o, l = oracle.rows(c, tok, head, lib=lib, threads=1)
+    assert np.array_equal(o, ref_o) and np.array_equal(l, ref_l)
+
+
+def pin_causal_mask_equals_causal(lib):
+    c = synth.make_case("prefill", batch=2, Hq=2, Hkv=1, d_qk=32, d_vo=32, page_size=8,
+                        kv_lens=[19, 8], qo_lens=[7, 8], causal=1, seed=46)
+    tok, head = _all_rows(c)
+    ref_o, ref_l = oracle.rows(c, tok, head, lib=lib, threads=1)
+    c.causal = 0
+    attach_mask(c, "causal", 2)
+    o, l = oracle.rows(c, tok, head, lib=lib, threads=1)
+    assert np.array_equal(o, ref_o) and np.array_equal(l, ref_l)
+
+
+def pin_mask_single_key(lib):
+    """One allowed key per row: the row's output is that key's value row, its lse the
+    key's scaled score (closed form)."""
+    c = synth.make_case("prefill", batch=2, Hq=2, Hkv=1, d_qk=32, d_vo=32, page_size=8,
+                        kv_lens=[17, 10], qo_lens=[4, 10], causal=0, seed=47)
+    rng = np.random.default_rng(3)
+    qo = c.qo_indptr.tolist()
+    blocks, indptr, pick = [], [0], {}
+    for b in range(c.batch):
+        ql, L = qo[b + 1] - qo[b], c.kv_lens[b]
+        g = np.zeros((ql, L), dtype=bool)
+        for i in range(ql):
+            pick[(b, i)] = int(rng.integers(0, L))
+            g[i, pick[(b, i)]] = True
+        blocks.append(np.packbits(g.ravel(), bitorder="little"))
+        indptr.append(indptr[-1] + blocks[-1].size)
+    c.mask = torch.from_numpy(np.concatenate(blocks))
+    c.mask_indptr = torch.tensor(indptr, dtype=torch.int64)
+    tok, head = _all_rows(c)
+    o, l = oracle.rows(c, tok, head, lib=lib, threads=1)
+    for r, (t, h) in enumerate(zip(tok, head)):
+        b = 0 if t < qo[1] else 1
+        j = pick[(b, int(t) - qo[b])]
+        K, V = seq_kv(c, b, int(h) // c.group)
+        q = c.q[int(t), int(h)].double().numpy()
+        _close(o[r], V[j], what="single-key output")
+        _close([l[r]], [c.sm_scale * float(K[j] @ q)], what="single-key lse")
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -37,6 +37,12 @@ MUTANTS = {
     "fp8_scale_k_for_v": ("double scale = is_v ? kv->v_scale : kv->k_scale;",
                           "double scale = kv->k_scale;"),
     "sf_block_of_32": ("int64_t sf_index = elem / 16;", "int64_t sf_index = elem / 32;"),
+    "mask_bit_order": ("if (!((mask[bit >> 3] >> (bit & 7)) & 1)) allowed = 0;",
+                       "if (!((mask[bit >> 3] >> (7 - (bit & 7))) & 1)) allowed = 0;"),
+    "mask_row_stride": ("int64_t bit = mask_indptr[b] * 8 + i * kv_len + j;",
+                        "int64_t bit = mask_indptr[b] * 8 + i * qo_len + j;"),
+    "mask_sequence_offset_ignored": ("int64_t bit = mask_indptr[b] * 8 + i * kv_len + j;",
+                                     "int64_t bit = i * kv_len + j;"),
 }
 
 
