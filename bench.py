@@ -339,9 +339,20 @@ def decode_e2e(c, kw, steps, nbytes):
     return res
 
 
-def bench_prefill(name, steps, warmup, gpu_index, pk, with_cpu=False):
+def bench_prefill(name, steps, warmup, gpu_index, pk, with_cpu=False, split_kv=True):
     import paged_gqa_attention_hd512_gb300 as pa
 
+    pa.paged_attn_set_prefill_split_kv(-1 if split_kv else 0)
+    try:
+        res = _bench_prefill(pa, name, steps, warmup, gpu_index, pk, with_cpu)
+    finally:
+        pa.paged_attn_set_prefill_split_kv(-1)
+    if not split_kv:
+        res["workload"] = name + " (split KV off)"
+    return res
+
+
+def _bench_prefill(pa, name, steps, warmup, gpu_index, pk, with_cpu):
     c = synth.workload(name, device="cuda")
     kw = pa.case_args(c)
     out = torch.empty(c.total_q, c.Hq, c.d_vo, dtype=torch.bfloat16, device="cuda")
@@ -534,6 +545,9 @@ def main():
             extra.append(bench_decode(name, max(3, args.steps // 10), args.warmup, barrier, local, pk,
                                       with_e2e=False, with_cpu=False))
         extra.append(bench_prefill("nvfp4_asym_prefill", max(3, min(50, args.steps // 40)), 3, local, pk))
+        for split_kv in (True, False):
+            extra.append(bench_prefill("prefill_extend_bf16", max(3, min(50, args.steps // 40)), 3, local, pk,
+                                       split_kv=split_kv))
         for name in APPEND_WORKLOADS:
             extra.append(bench_append(name, max(3, args.steps // 10), args.warmup, local, pk))
         line["secondary"] = extra

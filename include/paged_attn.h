@@ -242,6 +242,14 @@ int paged_attn_set_prefill_dequant_limit(long long bytes);
  * summation order.  Process-wide.  Returns PA_OK, or PA_ERR_INVALID_ARG for another mode. */
 int paged_attn_set_prefill_cta_pairs(int mode);
 
+/* Split KV for prefills whose (query tile, kv head) items are fewer than the SMs (short
+ * queries over long KV, "extend"): the device planner then cuts long KV ranges into
+ * chunks, each chunk writes an fp32 partial (normalised output, lse) to the workspace and
+ * a merge kernel combines them (lse-weighted, as split-K decode).  mode -1 (default)
+ * allows it, 0 never splits; results agree up to summation order.  Process-wide.
+ * Returns PA_OK, or PA_ERR_INVALID_ARG for another mode. */
+int paged_attn_set_prefill_split_kv(int mode);
+
 /* Name of the kernel variant the last successful call on this host thread launched
  * (for tests that must know which path ran).  Returns PA_OK; the text is truncated to
  * len-1 characters. */

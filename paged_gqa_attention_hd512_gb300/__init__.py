@@ -32,7 +32,7 @@ EXPORTED = ("paged_attn_decode", "paged_attn_prefill", "paged_attn_status_string
             "paged_attn_set_decode_chunk_pages", "paged_attn_last_variant",
             "paged_attn_profile_begin", "paged_attn_profile_end", "paged_attn_decode_noalloc",
             "paged_attn_set_prefill_dequant_limit", "paged_attn_set_prefill_cta_pairs",
-            "paged_attn_append_kv", "paged_attn_prefill_custom_mask")
+            "paged_attn_append_kv", "paged_attn_prefill_custom_mask", "paged_attn_set_prefill_split_kv")
 
 _lib = None
 
@@ -81,6 +81,8 @@ def load(path: Optional[str] = None):
     lib.paged_attn_set_prefill_dequant_limit.argtypes = [ctypes.c_longlong]
     lib.paged_attn_set_prefill_cta_pairs.restype = i32
     lib.paged_attn_set_prefill_cta_pairs.argtypes = [i32]
+    lib.paged_attn_set_prefill_split_kv.restype = i32
+    lib.paged_attn_set_prefill_split_kv.argtypes = [i32]
     lib.paged_attn_last_variant.restype = i32
     lib.paged_attn_last_variant.argtypes = [ctypes.c_char_p, i32]
     lib.paged_attn_profile_begin.restype = i32
@@ -270,6 +272,13 @@ def paged_attn_set_prefill_cta_pairs(mode: int) -> None:
     st = load().paged_attn_set_prefill_cta_pairs(mode)
     if st != PA_OK:
         raise PagedAttnError(st, "paged_attn_set_prefill_cta_pairs")
+
+
+def paged_attn_set_prefill_split_kv(mode: int) -> None:
+    """-1 (default): prefills that leave SMs idle may split long KV ranges; 0: never."""
+    st = load().paged_attn_set_prefill_split_kv(mode)
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_set_prefill_split_kv")
 
 
 def paged_attn_last_variant() -> str:

@@ -61,6 +61,8 @@ std::atomic<uint64_t> g_prefill_dequant_limit{kDefaultDequantLimit};
 // prefill with bf16 KV on CTA pairs: 1 = whenever two-CTA clusters fit, 0 = never (the
 // default: on the measured workloads one CTA per query tile is faster)
 std::atomic<int> g_prefill_pairs{0};
+// split KV for prefills that leave SMs idle: -1 = when the planner finds it useful, 0 = never
+std::atomic<int> g_prefill_split{-1};
 // two-CTA clusters of the pair kernel per device and shape (512x512, 512x256, 256x256);
 // -1 = not asked yet
 std::atomic<int> g_pair_clusters[kMaxDevices][3];
@@ -250,6 +252,12 @@ int paged_attn_set_prefill_cta_pairs(int mode) {
   return PA_OK;
 }
 
+int paged_attn_set_prefill_split_kv(int mode) {
+  if (mode < -1 || mode > 0) return PA_ERR_INVALID_ARG;
+  g_prefill_split = mode;
+  return PA_OK;
+}
+
 int paged_attn_set_decode_chunk_pages(int pages) {
   if (pages < 0) return PA_ERR_INVALID_ARG;
   g_forced_chunk_pages = pages;
@@ -433,7 +441,12 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   int pair_grid = 0;
   if (run_kvt == PA_KV_BF16 && g_prefill_pairs.load() == 1) pair_grid = 2 * std::min(sms / 2, pair_clusters(head_dim_qk, head_dim_vo));
 
-  const long max_items = ((long)total_q / rows_per_tile + batch) * num_kv_heads;
+  // split KV (short queries over long KV): when even one item per (query tile, kv head)
+  // cannot fill the SMs, the planner may split KV ranges; up to 3 x sms items and slots
+  const long tiles_bound = ((long)total_q + rows_per_tile - 1) / rows_per_tile + batch;
+  const bool split = g_prefill_split.load() != 0 && pair_grid == 0 && tiles_bound * num_kv_heads < sms;
+  const int max_slots = split ? 3 * sms : 0;
+  const long max_items = std::max(((long)total_q / rows_per_tile + batch) * num_kv_heads, (long)max_slots);
   if (max_items > (1l << 30)) return PA_ERR_INVALID_ARG;
   size_t off = kFixedBytes;
   const size_t o_hdr = off; off = align_up(off + 64, 256);
@@ -445,6 +458,9 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   const size_t o_pscr = off; off = align_up(off + (size_t)sms * reuse_tiles * 32768, 256);
   const size_t o_mscr = off; off = align_up(off + (size_t)sms * reuse_tiles * 128 * sizeof(float), 256);
   const size_t o_shadow = off; off = align_up(off + (dequant ? (size_t)num_pages * bf16_page : 0), 256);
+  const size_t o_part = off; off = align_up(off + (size_t)max_slots * 128 * head_dim_vo * sizeof(float), 256);
+  const size_t o_plse = off; off = align_up(off + (size_t)max_slots * 128 * sizeof(float), 256);
+  const size_t o_merge = off; off = align_up(off + (size_t)max_slots * sizeof(PrefillMerge), 256);
   char* ws = static_cast<char*>(workspace(off, &st));
   if (!ws) return st;
 
@@ -519,6 +535,11 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   p.pair = pair_grid > 0 ? 1 : 0;
   p.mask = mask;
   p.mask_indptr = mask_indptr;
+  p.split_target = split ? sms : 0;
+  p.part_o = reinterpret_cast<float*>(ws + o_part);
+  p.part_lse = reinterpret_cast<float*>(ws + o_plse);
+  p.merges = reinterpret_cast<PrefillMerge*>(ws + o_merge);
+  p.max_slots = max_slots;
   p.max_items = (int)max_items;
   p.box_rows = page_size;
   p.swz = 7;
@@ -545,9 +566,10 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   cudaError_t e = launch_prefill(run_kvt, head_dim_qk, head_dim_vo, L, &name);
   prof_mark(L.stream, false);
   if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (split && launch_prefill_merge(head_dim_vo, p, sms, L.stream) != cudaSuccess) return PA_ERR_CUDA;
   static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};
-  std::snprintf(g_variant, sizeof g_variant, "%s_%s%s%s", name, kv_names[kv_dtype], dequant ? "_dequant" : "",
-                mask ? "_mask" : "");
+  std::snprintf(g_variant, sizeof g_variant, "%s_%s%s%s%s", name, kv_names[kv_dtype], dequant ? "_dequant" : "",
+                mask ? "_mask" : "", split ? "_splitkv" : "");
   return PA_OK;
 }
 }  // namespace

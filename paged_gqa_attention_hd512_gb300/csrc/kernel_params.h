@@ -61,6 +61,16 @@ struct PrefillItem {
   int q_begin;  // first new-token index (within the sequence) of the tile
   int kvh;
   int cost;     // keys visited (for ordering)
+  // split KV: this item covers KV tiles [kv_t0, kv_t1) of the tile's range and writes
+  // its normalised output and lse to partial slot `slot`; slot -1: the whole range,
+  // written to the output
+  int kv_t0, kv_t1, slot;
+};
+
+// split KV: the partial slots [slot0, slot0 + parts) of one (tile, kv head), merged into
+// its output rows
+struct PrefillMerge {
+  int b, q_begin, kvh, slot0, parts;
 };
 
 struct PrefillParams {
@@ -89,6 +99,15 @@ struct PrefillParams {
   int batch, total_q, Hq, Hkv, group, page_size, window_left, causal, num_pages;
   int rows_per_tile;  // query positions per 128-row tile (128 / group)
   int pair;           // 1: items span two tiles, computed by the two CTAs of a cluster
+  // split KV (short queries over long KV): when split_target > 0 and the tiles x kv heads
+  // are fewer than split_target, the planner splits long KV ranges into chunks so that
+  // about 2 x split_target items exist; each chunk writes [128 rows][d_vo] fp32 and
+  // [128] lse to its slot, merged afterwards (hdr[1] = number of merges)
+  int split_target;
+  float* part_o;
+  float* part_lse;
+  PrefillMerge* merges;
+  int max_slots;
   // optional custom mask: bit mask_indptr[b] * 8 + i * kv_len + j (bit k of a byte is
   // its 2^k bit) lets new token i of sequence b attend key j; nullptr = none
   const uint8_t* mask;

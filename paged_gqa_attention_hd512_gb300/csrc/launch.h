@@ -38,6 +38,8 @@ int decode_tile_tokens(int kvt, int dqk);
 
 cudaError_t launch_prefill(int kvt, int dqk, int dvo, const PrefillLaunch& L, const char** variant);
 cudaError_t launch_prefill_plan(const PrefillParams& p, cudaStream_t s);
+// Split KV: merges the partial slots the plan listed (hdr[1] entries) into the output.
+cudaError_t launch_prefill_merge(int dvo, const PrefillParams& p, int grid, cudaStream_t s);
 int prefill_smem_bytes(int kvt, int dqk, int dvo);
 // Two-CTA clusters of the bf16 prefill kernel that fit on the device at once.
 int prefill_pair_clusters(int dqk, int dvo);

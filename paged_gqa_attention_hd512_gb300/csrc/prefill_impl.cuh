@@ -131,6 +131,20 @@ __device__ __forceinline__ int prefill_tile_cost(const PrefillParams& p, int kv_
   return hi / 128 - lo / 128 + 1;
 }
 
+// First KV tile and number of KV tiles of the item starting at new-token q_begin (the
+// range prefill_item_info computes); nt 0 when no key is visible.
+__device__ __forceinline__ void prefill_tile_range(const PrefillParams& p, int kv_len, int qo_len, int q_begin,
+                                                   int& jlo, int& nt) {
+  const int n_pos = min(p.rows_per_tile * (p.pair ? 2 : 1), qo_len - q_begin);
+  const int pos0 = kv_len - qo_len + q_begin;
+  int hi = p.causal ? min(kv_len - 1, pos0 + n_pos - 1) : kv_len - 1;
+  int lo = p.window_left >= 0 ? max(0, pos0 - p.window_left) : 0;
+  hi = max(hi, 0);
+  lo = min(lo, hi);
+  jlo = lo / 128;
+  nt = hi / 128 - jlo + 1;
+}
+
 #ifdef PA_PREFILL_PLAN
 // Per-sequence tile offsets (exclusive scan over ceil(qo_len / P)), then a cost histogram
 // and a scatter over all tiles in parallel.
@@ -185,6 +199,63 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p) {
     const int kv_len = np > 0 ? (np - 1) * ps + p.kv_last_page_len[b] : 0;
     cost = prefill_tile_cost(p, kv_len, qo_len, q0);
   };
+  // split KV: fewer tiles x kv heads than split_target (short queries over long KV).  The
+  // tile list is short, so one thread lays the items out tile by tile: every (tile, kv
+  // head) whose range exceeds `chunk` KV tiles becomes ceil(range / chunk) items over
+  // consecutive chunks, each with its own partial slot, plus one merge entry; chunk is
+  // chosen so that about 2 x split_target items exist.
+  if (p.split_target > 0 && n_tiles * p.Hkv < p.split_target) {
+    if (tid == 0) {
+      long long total = 0;
+      for (int t = 0; t < n_tiles; ++t) {
+        int b, q0, cost;
+        tile_of(t, b, q0, cost);
+        total += cost;
+      }
+      const int chunk = max(4, (int)((total * p.Hkv + 2ll * p.split_target - 1) / (2ll * p.split_target)));
+      int n_items = 0, n_slots = 0, n_merge = 0;
+      for (int t = 0; t < n_tiles; ++t) {
+        int b, q0, cost;
+        tile_of(t, b, q0, cost);
+        const int qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
+        const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
+        const int kv_len = np > 0 ? (np - 1) * p.page_size + p.kv_last_page_len[b] : 0;
+        int jlo, nt;
+        prefill_tile_range(p, kv_len, qo_len, q0, jlo, nt);
+        int parts = max(1, (nt + chunk - 1) / chunk);
+        // stay inside the host's bounds (cannot trigger with chunk as chosen above)
+        if (n_items + parts * p.Hkv > p.max_items || n_slots + parts * p.Hkv > p.max_slots) parts = 1;
+        const int step = (nt + parts - 1) / parts;
+        for (int k = 0; k < p.Hkv; ++k) {
+          if (n_items + parts > p.max_items) break;
+          if (parts > 1) {
+            PrefillMerge m;
+            m.b = b;
+            m.q_begin = q0;
+            m.kvh = k;
+            m.slot0 = n_slots;
+            m.parts = parts;
+            p.merges[n_merge++] = m;
+          }
+          for (int s2 = 0; s2 < parts; ++s2) {
+            PrefillItem it;
+            it.b = b;
+            it.q_begin = q0;
+            it.kvh = k;
+            it.kv_t0 = jlo + s2 * step;
+            it.kv_t1 = min(jlo + nt, jlo + (s2 + 1) * step);
+            it.cost = it.kv_t1 - it.kv_t0;
+            it.slot = parts > 1 ? n_slots + s2 : -1;
+            p.items[n_items++] = it;
+          }
+          if (parts > 1) n_slots += parts;
+        }
+      }
+      p.hdr[0] = n_items;
+      p.hdr[1] = n_merge;
+    }
+    return;
+  }
   for (int t = tid; t < n_tiles; t += blockDim.x) {
     int b, q0, cost;
     tile_of(t, b, q0, cost);
@@ -233,16 +304,63 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p) {
       it.q_begin = q0;
       it.kvh = k;
       it.cost = cost;
+      it.kv_t0 = 0;
+      it.kv_t1 = 0;
+      it.slot = -1;
       p.items[slot * p.Hkv + k] = it;
     }
   }
-  if (tid == 0) p.hdr[0] = min(n_tiles * p.Hkv, p.max_items);
+  if (tid == 0) {
+    p.hdr[0] = min(n_tiles * p.Hkv, p.max_items);
+    p.hdr[1] = 0;
+  }
+}
+
+// Split KV: each merge entry's output rows = the partials of its slots weighted by
+// exp(lse_s - lse), lse = ln sum_s exp(lse_s) (the split-K merge of "Run Gemma4 head_dim
+// 512 attention on Triton", Not covered / Test Coverage: split-K).  A warp per row.
+template <int DVO>
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams p) {
+  const int n = p.hdr[1];
+  const int g = p.group;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int u = blockIdx.x; u < n; u += gridDim.x) {
+    const PrefillMerge m = p.merges[u];
+    const int qo_len = p.qo_indptr[m.b + 1] - p.qo_indptr[m.b];
+    const int n_pos = min(p.rows_per_tile, qo_len - m.q_begin);
+    const int q_row0 = p.qo_indptr[m.b] + m.q_begin;
+    for (int r = warp; r < n_pos * g; r += blockDim.x >> 5) {
+      float M = -INFINITY;
+      for (int s2 = 0; s2 < m.parts; ++s2) M = fmaxf(M, p.part_lse[(size_t)(m.slot0 + s2) * 128 + r]);
+      float L = 0.f;
+      if (M != -INFINITY)
+        for (int s2 = 0; s2 < m.parts; ++s2) L += expf(p.part_lse[(size_t)(m.slot0 + s2) * 128 + r] - M);
+      const float lse = M == -INFINITY ? -INFINITY : M + logf(L);
+      const size_t orow = ((size_t)(q_row0 + r / g) * p.Hq + m.kvh * g + r % g) * DVO;
+      for (int d = lane * 4; d < DVO; d += 128) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (M != -INFINITY)
+          for (int s2 = 0; s2 < m.parts; ++s2) {
+            const size_t base = (size_t)(m.slot0 + s2) * 128 + r;
+            const float w = expf(p.part_lse[base] - lse);
+            const float4 v = *reinterpret_cast<const float4*>(p.part_o + base * DVO + d);
+            acc.x += w * v.x;
+            acc.y += w * v.y;
+            acc.z += w * v.z;
+            acc.w += w * v.w;
+          }
+        *reinterpret_cast<uint2*>(p.out + orow + d) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+      }
+      if (lane == 0 && p.lse) p.lse[(size_t)(q_row0 + r / g) * p.Hq + m.kvh * g + r % g] = lse;
+    }
+  }
 }
 #endif  // PA_PREFILL_PLAN
 
 // Everything one role needs to know about a work item.
 struct PrefillItemInfo {
   int b, kvh, q_begin, n_pos, qo_len, kv_len, q_row0, pos0, jlo, nt, ip0, np;
+  int slot;  // split KV: partial slot of this item, -1 when it writes the output
 };
 
 // `rank`: which tile of a CTA pair's item this CTA computes (0 without pairs).  Both CTAs
@@ -268,6 +386,12 @@ __device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams
   lo = min(lo, hi);
   f.jlo = lo / 128;
   f.nt = hi / 128 - f.jlo + 1;
+  f.slot = item.slot;
+  if (item.kv_t1 > item.kv_t0) {  // split KV: one chunk of the range
+    const int t0 = max(f.jlo, item.kv_t0), t1 = min(f.jlo + f.nt, item.kv_t1);
+    f.jlo = t0;
+    f.nt = max(1, t1 - t0);
+  }
   return f;
 }
 
@@ -1168,28 +1292,47 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
         tc_fence_after();
         const float inv = lt > 0.f ? v_scale / lt : 0.f;
         uint16_t* orow = p.out + ((size_t)(f.q_row0 + p_local) * p.Hq + hq) * DVO + pass * C::DVP + ocol0;
+        const float row_lse = lt > 0.f ? (m_used + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+        if (f.slot >= 0) {
+          // split KV: this chunk's normalised rows (fp32) and lse into its partial slot
+          float* prow = p.part_o + ((size_t)f.slot * 128 + row) * DVO + pass * C::DVP + ocol0;
 #pragma unroll 1
-        for (int c = 0; c < OCOL / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(lane_base + C::TM_O + ocol0 + 32 * c, ov);
-          tc_wait_ld();
-          uint32_t pkd[16];
+          for (int c = 0; c < OCOL / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(lane_base + C::TM_O + ocol0 + 32 * c, ov);
+            tc_wait_ld();
+            if (row_ok) {
+              float4* dst = reinterpret_cast<float4*>(prow + 32 * c);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pkd[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              st_global_stream_v4(dst + i, make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]));
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
+                                     __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
+            }
           }
+          if (pass == C::NPASS - 1 && row_ok && wg == 0) p.part_lse[(size_t)f.slot * 128 + row] = row_lse;
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < OCOL / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld32(lane_base + C::TM_O + ocol0 + 32 * c, ov);
+            tc_wait_ld();
+            uint32_t pkd[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              pkd[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                st_global_stream_v4(dst + i, make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]));
+            }
+          }
+          if (pass == C::NPASS - 1 && row_ok && p.lse && wg == 0)
+            p.lse[(size_t)(f.q_row0 + p_local) * p.Hq + hq] = row_lse;
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) arrive_lead(o_free);
-        if (pass == C::NPASS - 1 && row_ok && p.lse && wg == 0)
-          p.lse[(size_t)(f.q_row0 + p_local) * p.Hq + hq] =
-              lt > 0.f ? (m_used + log2f(lt)) * 0.69314718055994531f : -INFINITY;
       }
     }
   }

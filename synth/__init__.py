@@ -398,6 +398,10 @@ WORKLOADS = {
     "nvfp4_asym_prefill": dict(
         phase="prefill", batch=8, Hq=16, Hkv=2, d_qk=512, d_vo=256, page_size=32,
         kv_lens=[1024] * 8, qo_lens=[1024] * 8, kv_dtype=KV_NVFP4, seed=1005),
+    # a few new tokens per sequence over a long cached prefix ("extend")
+    "prefill_extend_bf16": dict(
+        phase="prefill", batch=4, Hq=24, Hkv=4, d_qk=512, d_vo=512, page_size=64,
+        kv_lens=[16384] * 4, qo_lens=[32] * 4, kv_dtype=KV_BF16, seed=1006),
     "sliding_decode_d256": dict(
         phase="decode", batch=256, Hq=32, Hkv=16, d_qk=256, d_vo=256, page_size=16,
         kv_lens=[8192] * 256, kv_dtype=KV_BF16, window_left=1023, seed=1005),

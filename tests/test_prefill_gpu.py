@@ -43,13 +43,23 @@ def _id(c):
             f"-qo{'_'.join(map(str, c[6]))}-c{c[7]}-w{c[8]}")
 
 
-@pytest.fixture(params=["pairs", "single"])
+def _variant():
+    """The variant of the last call without the split-KV mark (which small cases get)."""
+    return pa.paged_attn_last_variant().replace("_splitkv", "")
+
+
+@pytest.fixture(params=["pairs", "single", "single_nosplit"])
 def cta_mode(request):
-    """bf16 prefill on one CTA per query tile (the default) and on CTA pairs."""
+    """bf16 prefill on one CTA per query tile (the default; small cases split long KV
+    ranges), on one CTA per tile without splitting, and on CTA pairs."""
     ensure_built()
     pa.paged_attn_set_prefill_cta_pairs(1 if request.param == "pairs" else -1)
+    pa.paged_attn_set_prefill_split_kv(0 if request.param == "single_nosplit" else -1)
     yield "_pair" if request.param == "pairs" else ""
+    if request.param != "single":
+        assert "_splitkv" not in pa.paged_attn_last_variant()
     pa.paged_attn_set_prefill_cta_pairs(-1)
+    pa.paged_attn_set_prefill_split_kv(-1)
 
 
 @pytest.mark.parametrize("c", CASES, ids=[_id(c) for c in CASES])
@@ -58,7 +68,7 @@ def test_prefill_parity(c, cta_mode):
     case = synth.make_case("prefill", batch=len(kv), Hq=hq, Hkv=hkv, d_qk=dqk, d_vo=dvo, page_size=ps,
                            kv_lens=kv, qo_lens=qo, causal=causal, window_left=win, seed=500 + len(kv))
     check_full(case, _id(c) + cta_mode)
-    assert pa.paged_attn_last_variant() == f"prefill_{dqk}x{dvo}{cta_mode}_bf16"
+    assert _variant() == f"prefill_{dqk}x{dvo}{cta_mode}_bf16"
 
 
 @pytest.mark.parametrize("q_gain", [8.0, 32.0])
@@ -78,6 +88,10 @@ def test_prefill_cta_pairs_setter_rejects_other_modes():  # noqa: D103
         with pytest.raises(pa.PagedAttnError) as e:
             pa.paged_attn_set_prefill_cta_pairs(bad)
         assert e.value.status == pa.PA_ERR_INVALID_ARG
+    for bad in (1, -2):
+        with pytest.raises(pa.PagedAttnError) as e:
+            pa.paged_attn_set_prefill_split_kv(bad)
+        assert e.value.status == pa.PA_ERR_INVALID_ARG
 
 
 def test_prefill_pairs_on_the_dequantised_copy(cta_mode, _dequant_limit):
@@ -86,7 +100,7 @@ def test_prefill_pairs_on_the_dequantised_copy(cta_mode, _dequant_limit):
     case = synth.make_case("prefill", batch=2, Hq=16, Hkv=2, d_qk=512, d_vo=256, page_size=32,
                            kv_lens=[300, 100], qo_lens=[300, 100], kv_dtype=synth.KV_NVFP4, seed=602)
     check_full(case, "nvfp4 copy" + cta_mode)
-    assert pa.paged_attn_last_variant() == f"prefill_512x256{cta_mode}_nvfp4_dequant"
+    assert _variant() == f"prefill_512x256{cta_mode}_nvfp4_dequant"
 
 
 def test_prefill_small_pages_are_refused():  # noqa: D103
@@ -132,4 +146,4 @@ def test_prefill_parity_quantised(c, mode, _dequant_limit):
     check_full(case, _qid(c) + "-" + mode)
     names = {synth.KV_FP8: "fp8", synth.KV_NVFP4: "nvfp4"}
     suffix = "_dequant" if mode == "dequant" else ""
-    assert pa.paged_attn_last_variant() == f"prefill_{dqk}x{dvo}_{names[dt]}{suffix}"
+    assert _variant() == f"prefill_{dqk}x{dvo}_{names[dt]}{suffix}"
