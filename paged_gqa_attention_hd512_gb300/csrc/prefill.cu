@@ -96,13 +96,6 @@ cudaError_t launch_prefill_plan(const PrefillParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_merge(int dvo, const PrefillParams& p, int grid, cudaStream_t s) {
-  if (dvo == 512) prefill_merge_kernel<512><<<grid, 256, 0, s>>>(p);
-  else if (dvo == 256) prefill_merge_kernel<256><<<grid, 256, 0, s>>>(p);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
-}
-
 template <int KVT>
 static int smem_bytes(int dqk, int dvo) {
   if (dqk == 512 && dvo == 512) return PrefillCfg<512, 512, KVT>::ALLOC;

@@ -316,45 +316,6 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p) {
   }
 }
 
-// Split KV: each merge entry's output rows = the partials of its slots weighted by
-// exp(lse_s - lse), lse = ln sum_s exp(lse_s) (the split-K merge of "Run Gemma4 head_dim
-// 512 attention on Triton", Not covered / Test Coverage: split-K).  A warp per row.
-template <int DVO>
-__global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams p) {
-  const int n = p.hdr[1];
-  const int g = p.group;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int u = blockIdx.x; u < n; u += gridDim.x) {
-    const PrefillMerge m = p.merges[u];
-    const int qo_len = p.qo_indptr[m.b + 1] - p.qo_indptr[m.b];
-    const int n_pos = min(p.rows_per_tile, qo_len - m.q_begin);
-    const int q_row0 = p.qo_indptr[m.b] + m.q_begin;
-    for (int r = warp; r < n_pos * g; r += blockDim.x >> 5) {
-      float M = -INFINITY;
-      for (int s2 = 0; s2 < m.parts; ++s2) M = fmaxf(M, p.part_lse[(size_t)(m.slot0 + s2) * 128 + r]);
-      float L = 0.f;
-      if (M != -INFINITY)
-        for (int s2 = 0; s2 < m.parts; ++s2) L += expf(p.part_lse[(size_t)(m.slot0 + s2) * 128 + r] - M);
-      const float lse = M == -INFINITY ? -INFINITY : M + logf(L);
-      const size_t orow = ((size_t)(q_row0 + r / g) * p.Hq + m.kvh * g + r % g) * DVO;
-      for (int d = lane * 4; d < DVO; d += 128) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (M != -INFINITY)
-          for (int s2 = 0; s2 < m.parts; ++s2) {
-            const size_t base = (size_t)(m.slot0 + s2) * 128 + r;
-            const float w = expf(p.part_lse[base] - lse);
-            const float4 v = *reinterpret_cast<const float4*>(p.part_o + base * DVO + d);
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
-          }
-        *reinterpret_cast<uint2*>(p.out + orow + d) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
-      }
-      if (lane == 0 && p.lse) p.lse[(size_t)(q_row0 + r / g) * p.Hq + m.kvh * g + r % g] = lse;
-    }
-  }
-}
 #endif  // PA_PREFILL_PLAN
 
 // Everything one role needs to know about a work item.
