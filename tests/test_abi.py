@@ -96,3 +96,44 @@ def test_binding_refuses_cpu_tensors(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(RuntimeError):
         pa.load(str(tmp_path / "nope.so"))
+
+
+def test_prefill_custom_mask_rejects_bad_arguments(lib):
+    sc = pa._Scales(None, None, None)
+    args = (FAKE, FAKE, 10, FAKE, FAKE, FAKE, FAKE, 1, 4, 8, 1, 512, 512, 16, 0.04, -1, 1, 0, ctypes.byref(sc),
+            FAKE, None)
+    assert lib.paged_attn_prefill_custom_mask(*args, None, FAKE, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.paged_attn_prefill_custom_mask(*args, FAKE, None, None) == pa.PA_ERR_INVALID_ARG
+    assert lib.paged_attn_prefill_custom_mask(*args, FAKE, FAKE + 4, None) == pa.PA_ERR_ALIGNMENT
+
+
+def _append(lib, **over):
+    a = dict(k=FAKE, v=FAKE, ai=FAKE, total=8, cache=FAKE, ip=FAKE, ind=FAKE, last=FAKE, batch=2, num_pages=4,
+             hkv=2, dqk=512, dvo=256, ps=16, dt=0, ks=None, vs=None, sf=None)
+    a.update(over)
+    return lib.paged_attn_append_kv(a["k"], a["v"], a["ai"], a["total"], a["cache"], a["ip"], a["ind"], a["last"],
+                                    a["batch"], a["num_pages"], a["hkv"], a["dqk"], a["dvo"], a["ps"], a["dt"],
+                                    a["ks"], a["vs"], a["sf"], None)
+
+
+def test_append_rejects_bad_arguments(lib):
+    assert _append(lib, batch=0) == pa.PA_OK and _append(lib, total=0) == pa.PA_OK  # nothing to write
+    assert _append(lib, k=None) == pa.PA_ERR_INVALID_ARG
+    assert _append(lib, ai=None) == pa.PA_ERR_INVALID_ARG
+    assert _append(lib, total=-1) == pa.PA_ERR_INVALID_ARG
+    assert _append(lib, num_pages=0) == pa.PA_ERR_INVALID_ARG
+    assert _append(lib, dqk=256, dvo=512) == pa.PA_ERR_UNSUPPORTED
+    assert _append(lib, ps=24) == pa.PA_ERR_UNSUPPORTED
+    assert _append(lib, dt=5) == pa.PA_ERR_INVALID_ARG
+    assert _append(lib, dt=1) == pa.PA_ERR_INVALID_ARG  # FP8 without scales
+    assert _append(lib, dt=2, ks=FAKE, vs=FAKE) == pa.PA_ERR_INVALID_ARG  # NVFP4 without a scale pool
+    assert _append(lib, dt=1, ks=FAKE + 2, vs=FAKE) == pa.PA_ERR_ALIGNMENT
+    assert _append(lib, k=FAKE + 8) == pa.PA_ERR_ALIGNMENT
+    assert _append(lib, cache=FAKE + 8) == pa.PA_ERR_ALIGNMENT
+
+
+def test_mode_setters_reject_other_values(lib):
+    assert lib.paged_attn_set_prefill_cta_pairs(2) == pa.PA_ERR_INVALID_ARG
+    assert lib.paged_attn_set_prefill_split_kv(1) == pa.PA_ERR_INVALID_ARG
+    assert lib.paged_attn_set_prefill_cta_pairs(-1) == pa.PA_OK
+    assert lib.paged_attn_set_prefill_split_kv(-1) == pa.PA_OK
