@@ -91,12 +91,40 @@ def peaks():
     return p, src
 
 
-def sources_digest(names) -> str:
+def code_tokens(text: str) -> str:
+    """C / CUDA source without comments, whitespace runs collapsed: what the compiler sees.
+    String and character literals are kept as they are."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def sources_digest(names, read=None) -> str:
+    """Digest of the kernel sources' code (comments and layout do not count), used to tell
+    whether a recorded ncu capture was taken on the current kernel."""
     h = hashlib.sha256()
     for n in names:
         path = os.path.join(ROOT, "paged_gqa_attention_hd512_gb300", "csrc", n)
-        if os.path.exists(path):
-            h.update(open(path, "rb").read())
+        text = read(n) if read else (open(path).read() if os.path.exists(path) else None)
+        if text is not None:
+            h.update(code_tokens(text).encode())
     return h.hexdigest()[:16]
 
 

@@ -9,22 +9,28 @@
 // one kv head (P = 128 / g), so every K/V tile loaded into shared memory serves all g
 // query heads that read it.  Warp roles:
 //   warp 0      producer: TMA loads of the Q tile (once per item) and, for bf16 KV, of K/V
-//               chunks ([128 keys][64 head-dim], 128B-swizzled) into a ring of 16 KB slots
-//               (V rows past the end of the sequence are zeroed before release); for FP8 /
-//               NVFP4 KV, of the packed chunks and block scales into staging rings
-//   warp 1      MMA issuer (the warp polls, lane 0 issues): S = Q K^T into TMEM (M 128,
-//               N 128, K 16 steps), O += P V with P read from TMEM (M 128, N 128 per pair
-//               of V chunks)
-//   warps 4-7   softmax + epilogue: thread r owns row r (TMEM lane r): masks, online
-//               softmax in base 2 with lazy rescaling, writes P into TMEM, and at the end
-//               normalises O and stores bf16 rows and lse
-//   warps 8-11  (FP8 / NVFP4 KV only) converters: staged chunks -> the MMA ring
+//               chunks ([128 keys][128 head-dim], two 128B-swizzled 16 KB blocks) into a
+//               ring of 32 KB slots (V rows past the end of the sequence are zeroed before
+//               release); for FP8 / NVFP4 KV converted in the kernel, of the packed chunks
+//               and block scales into staging rings
+//   warp 1      MMA issuer (lane 0 issues): S = Q K^T into TMEM (M 128, N 128, K 16
+//               steps), O += P V with P read from TMEM (M 128, N 128 per V chunk)
+//   warp 2      gate: polls the mbarriers and meets the MMA warp at named barriers
+//   warp 3      (head_dim_vo 512, bf16) the first pass's P tiles into the P slots
+//   warps 4-11  softmax + epilogue (two warpgroups, half of the keys each; warps 4-7 alone
+//               when 8-11 convert FP8 / NVFP4): thread r owns row r (TMEM lane r): causal,
+//               window and custom masks, online softmax in base 2 with lazy rescaling, P
+//               into TMEM, at the end O / l as bf16 rows and lse (or, for a chunk of a
+//               split KV range, fp32 rows and lse into a partial slot)
+//   warps 8-11  (FP8 / NVFP4 KV converted in the kernel) converters: staged chunks -> ring
 // TMEM (512 columns): two S buffers [0, 128) and [128, 256), used by alternate KV steps,
 // each holding its step's P once the softmax has read S, and O [256, 512).  With two S
 // buffers the QK of the next step runs while the softmax works on this one.  A 128 x 512
 // fp32 O tile would fill all of TMEM, so head_dim_vo 512 is computed in two passes of 256
-// columns over the same KV range (S is recomputed; the softmax statistics of both passes
-// are identical).
+// columns over the same KV range: the second reads the first pass's P tiles back from a
+// per-CTA scratch (items of up to 64 KV tiles) or recomputes S (longer items).
+// With PAIR, two CTAs of a cluster share every MMA (cta_group::2, M 256), each loading
+// half of every K/V tile (see PrefillCfg).
 #pragma once
 
 #include "common.cuh"

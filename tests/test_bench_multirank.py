@@ -57,3 +57,13 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setattr("sys.argv", ["bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1"])
     assert bench.main() == 0
     assert capsys.readouterr().out == ""
+
+
+def test_source_digest_ignores_comments_not_code():
+    base = 'int f(int x) { return x + 1; }  // add one\n/* block */ const char* s = "a // b";\n'
+    same = '// header\nint f(int x) {\n  return x + 1;  /* changed comment */\n}\nconst char* s = "a // b";\n'
+    other = 'int f(int x) { return x + 2; }\nconst char* s = "a // b";\n'
+    lit = 'int f(int x) { return x + 1; }\nconst char* s = "a // c";\n'
+    d = lambda t: bench.sources_digest(["x.cu"], read=lambda n: t)
+    assert d(base) == d(same)
+    assert d(base) != d(other) and d(base) != d(lit)
