@@ -137,7 +137,12 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
  * converted to a bf16 copy in the library workspace (num_pages * num_kv_heads *
  * page_size * (head_dim_qk + head_dim_vo) * 2 bytes) when that fits the limit set by
  * paged_attn_set_prefill_dequant_limit (default 4 GiB), else converted inside the
- * kernel on every read; both give the same values (the conversions are exact).
+ * kernel on every read; both give the same values (the conversions are exact).  When the
+ * (query tile, kv head) items are fewer than the SMs (a few new tokens over a long
+ * prefix), the device planner may split long KV ranges into chunks whose fp32 partials a
+ * merge kernel combines (paged_attn_set_prefill_split_kv); the workspace then also holds
+ * 3 x SMs partial slots of 128 x head_dim_vo floats.  Everything runs on `stream` with no
+ * host synchronisation.
  * Returns as paged_attn_decode.
  */
 int paged_attn_prefill(const void* q, const int32_t* qo_indptr, int total_q,
