@@ -37,6 +37,39 @@ import synth  # noqa: E402
 
 MAIN = "gqa_decode_bf16"
 PREFILL = "causal_prefill_bf16"
+# the configurations the numbers are quoted on (synth.WORKLOADS holds their recipes)
+DESCRIBE = {
+    "tiny_mqa_decode": "tiny decode: batch 2, MQA 8 q / 1 kv heads, head_dim 512, bf16, page_size 16, "
+                       "kv_len 37 and 64, shuffled pages, no window",
+    "gqa_decode_bf16": "bf16 GQA decode: batch 64, 24 q / 4 kv heads, head_dim 512, page_size 64, "
+                       "kv_len uniform in [1024, 8192], shuffled pages, split-K",
+    "fp8_decode": "FP8 KV decode: batch 128, 12 q / 4 kv heads, head_dim 512, e4m3 KV with per-tensor fp32 "
+                  "scales, page_size 16, kv_len 32768, bf16 q and output",
+    "causal_prefill_bf16": "causal paged prefill bf16: new-token lengths 2048 / 3000 / 4096 / 6272, no cached "
+                           "prefix, 24 q / 4 kv heads, head_dim 512, page_size 64, shuffled pages",
+    "nvfp4_asym_prefill": "asymmetric NVFP4 causal prefill: qk 512 / vo 256, 16 q / 2 kv heads, 8 x 1024 "
+                          "tokens, NVFP4 KV (e2m1, e4m3 scale per 16, fp32 global), page_size 32",
+    "sliding_decode_d256": "sliding-window decode: head_dim 256, window_left 1023, 32 q / 16 kv heads, "
+                           "batch 256, kv_len 8192, bf16 KV, page_size 16",
+    "prefill_extend_bf16": "extend prefill: 4 x 32 new tokens over 16384 cached keys, 24 q / 4 kv heads, "
+                           "head_dim 512, page_size 64, bf16",
+}
+
+
+def rank_world():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def bench_case(name, device="cuda"):
+    """This rank's shard of the global batch (the whole workload on one GPU)."""
+    rank, world = rank_world()
+    return synth.workload_shard(name, rank, world, device=device)
+
+
+def prefill_launches(variant: str) -> int:
+    """Kernels one prefill call launches: planner and prefill, plus the FP8 / NVFP4 page
+    conversion and the split-KV merge when the variant names them."""
+    return 2 + ("_dequant" in variant) + ("_splitkv" in variant)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DECODE_SOURCES = ("decode_impl.cuh", "common.cuh", "decode_inst.cuh", "kernel_params.h")
 PREFILL_SOURCES = ("prefill_impl.cuh", "common.cuh", "kernel_params.h")
@@ -296,7 +329,7 @@ def oracle_sample_rate(host_case, budget_s: float, kind: str):
 def bench_decode(name, steps, warmup, barrier, gpu_index, pk, with_e2e=True, with_cpu=True):
     import paged_gqa_attention_hd512_gb300 as pa
 
-    c = synth.workload(name, device="cuda")
+    c = bench_case(name)
     kw = pa.case_args(c)
     out = torch.empty(c.batch, c.Hq, c.d_vo, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(c.batch, c.Hq, dtype=torch.float32, device="cuda")
@@ -316,9 +349,10 @@ def bench_decode(name, steps, warmup, barrier, gpu_index, pk, with_e2e=True, wit
         n_k, k_ms = pa.paged_attn_profile_end()
     clocks = clk.summary()
     variant = pa.paged_attn_last_variant()
-    res = {"workload": name, "ms_per_step": ms / steps, "value": nbytes / (ms / steps * 1e-3) / 1e9,
-           "unit": "GB/s", "bytes_per_step": nbytes, "clocks": clocks, "variant": variant,
-           "gpu_launches": 3 * steps}
+    res = {"workload": name, "config": {"workload": DESCRIBE.get(name, name), "name": name},
+           "ms_per_step": ms / steps, "value": nbytes / (ms / steps * 1e-3) / 1e9,
+           "unit": "GB/s", "bytes_per_step": nbytes, "steps": steps, "clocks": clocks, "variant": variant,
+           "gpu_launches": 2 * steps}
     kern_ms = k_ms / max(1, n_k)
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
     digest = sources_digest(DECODE_SOURCES)
@@ -330,7 +364,7 @@ def bench_decode(name, steps, warmup, barrier, gpu_index, pk, with_e2e=True, wit
         res["e2e"] = decode_e2e(c, kw, max(3, min(steps, 10)), nbytes)
     if with_cpu:
         host = c.to("cpu")
-        rate, dt, desc, threads = oracle_sample_rate(host, 20.0, "decode")
+        rate, dt, desc, threads = oracle_sample_rate(host, 15.0, "decode")
         res["cpu_baseline"] = {"value": rate, "unit": "GB/s", "cores": threads, "kind": "oracle",
                                "sample": desc, "seconds": dt}
     del c
@@ -367,12 +401,12 @@ def decode_e2e(c, kw, steps, nbytes):
     return res
 
 
-def bench_prefill(name, steps, warmup, gpu_index, pk, with_cpu=False, split_kv=True):
+def bench_prefill(name, steps, warmup, gpu_index, pk, with_cpu=False, split_kv=True, with_e2e=False):
     import paged_gqa_attention_hd512_gb300 as pa
 
     pa.paged_attn_set_prefill_split_kv(-1 if split_kv else 0)
     try:
-        res = _bench_prefill(pa, name, steps, warmup, gpu_index, pk, with_cpu)
+        res = _bench_prefill(pa, name, steps, warmup, gpu_index, pk, with_cpu, with_e2e)
     finally:
         pa.paged_attn_set_prefill_split_kv(-1)
     if not split_kv:
@@ -380,8 +414,43 @@ def bench_prefill(name, steps, warmup, gpu_index, pk, with_cpu=False, split_kv=T
     return res
 
 
-def _bench_prefill(pa, name, steps, warmup, gpu_index, pk, with_cpu):
-    c = synth.workload(name, device="cuda")
+def prefill_e2e(c, kw, steps, flops):
+    """Same metric through the C ABI from pinned host buffers: q, the page table and the
+    cache copied in, out and lse copied back, inside the timed region."""
+    import paged_gqa_attention_hd512_gb300 as pa
+
+    names = ["q", "qo_indptr", "kv_cache", "kv_indptr", "kv_indices", "kv_last_page_len"]
+    if c.sf is not None:
+        names.append("sf")
+    host = {n: getattr(c, n).cpu().pin_memory() for n in names}
+    dev = {n: torch.empty_like(getattr(c, n)) for n in names}
+    kw = dict(kw)
+    out_h = torch.empty(c.total_q, c.Hq, c.d_vo, dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty(c.total_q, c.Hq, dtype=torch.float32).pin_memory()
+    out = torch.empty(c.total_q, c.Hq, c.d_vo, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(c.total_q, c.Hq, dtype=torch.float32, device="cuda")
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    if "sf" in dev:
+        kw["sf"] = dev["sf"]
+
+    def step():
+        for n in names:
+            dev[n].copy_(host[n], non_blocking=True)
+        pa.paged_attn_prefill(dev["q"], dev["qo_indptr"], dev["kv_cache"], dev["kv_indptr"], dev["kv_indices"],
+                              dev["kv_last_page_len"], causal=bool(c.causal), out=out, lse=lse, **kw)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+
+    ms = time_region(step, steps, 2)
+    res = {"value": flops / (ms / steps * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps}
+    del dev, host
+    return res
+
+
+def _bench_prefill(pa, name, steps, warmup, gpu_index, pk, with_cpu, with_e2e):
+    c = bench_case(name)
     kw = pa.case_args(c)
     out = torch.empty(c.total_q, c.Hq, c.d_vo, dtype=torch.bfloat16, device="cuda")
     lse = torch.empty(c.total_q, c.Hq, dtype=torch.float32, device="cuda")
@@ -420,16 +489,20 @@ def _bench_prefill(pa, name, steps, warmup, gpu_index, pk, with_cpu):
     kern_ms = k_ms / max(1, n_k)
     achieved = flops / (kern_ms * 1e-3) / 1e12
     digest = sources_digest(PREFILL_SOURCES)
-    res = {"workload": name, "ms_per_step": ms, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-           "flops_per_step": flops, "variant": pa.paged_attn_last_variant(), "clocks": clk.summary(),
-           "l2": "flushed between steps (256 MiB write)", "gpu_launches": 2 * steps,
+    variant = pa.paged_attn_last_variant()
+    res = {"workload": name, "config": {"workload": DESCRIBE.get(name, name), "name": name},
+           "ms_per_step": ms, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "flops_per_step": flops, "steps": steps, "variant": variant, "clocks": clk.summary(),
+           "l2": "flushed between steps (256 MiB write)", "gpu_launches": prefill_launches(variant) * steps,
            "roofline": {"bound": "tensor", "achieved": achieved, "peak": pk[0]["bf16_tflops"], "unit": "TFLOP/s",
                         "frac": achieved / pk[0]["bf16_tflops"],
                         "traffic": traffic_record("prefill_kernel", name, digest), "kernel": "prefill_kernel",
                         "kernel_ms": kern_ms, "launches_timed": n_k, "peak_source": f"{pk[1]} bf16_tflops (burst)",
                         "source_digest": digest}}
+    if with_e2e:
+        res["e2e"] = prefill_e2e(c, kw, max(3, min(steps, 10)), flops)
     if with_cpu:
-        rate, dt, desc, threads = oracle_sample_rate(c.to("cpu"), 20.0, "prefill")
+        rate, dt, desc, threads = oracle_sample_rate(c.to("cpu"), 15.0, "prefill")
         res["cpu_baseline"] = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
                                "sample": desc, "seconds": dt}
     del c, flush
@@ -512,7 +585,8 @@ def main():
     ap.add_argument("--all", action="store_true", help="also time every other workload")
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle cpu_baseline leg")
-    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e leg")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer e2e legs")
+    ap.add_argument("--no-secondary", action="store_true", help="time only the main decode and prefill lines")
     ap.add_argument("--workload", default=MAIN, help="decode workload of the main line")
     ap.add_argument("--prefill-only", action="store_true", help="time only the prefill workload (profiling)")
     ap.add_argument("--prefill-workload", default=PREFILL, help="prefill workload of --prefill-only")
@@ -543,8 +617,9 @@ def main():
         barrier()
     torch.cuda.set_device(local)
     pk = peaks()
+    psteps = max(5, min(50, args.steps // 2))
     if args.prefill_only:
-        res = bench_prefill(args.prefill_workload, max(3, min(50, args.steps // 40)), args.warmup, local, pk)
+        res = bench_prefill(args.prefill_workload, psteps, args.warmup, local, pk)
         if rank == 0:
             print(json.dumps({"prefill": res}), flush=True)
         return 0
@@ -557,27 +632,30 @@ def main():
         "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded Irwin-Hall(4) standard-normal draws; seeded random page order)",
-        "config": {"workload": "bf16 GQA decode: batch 64, 24 q / 4 kv heads, head_dim 512, page_size 64, "
-                               "kv_len uniform in [1024, 8192], shuffled pages, split-K",
-                   "name": args.workload, "l2": "inputs (2.4 GB of KV) larger than L2, no flush",
-                   "parallelism": f"{world} independent replica(s), no collective"},
+        "config": {"workload": DESCRIBE.get(args.workload, args.workload),
+                   "name": args.workload, "l2": "inputs (2.6 GB of KV) larger than L2, no flush",
+                   "parallelism": (f"global batch of {world} x the workload's batch, split by sequence over "
+                                   f"{world} rank(s) (one shard each), no collective")},
         "e2e": main_res.get("e2e"), "roofline": main_res["roofline"], "cpu_baseline": main_res.get("cpu_baseline"),
         "clocks": main_res["clocks"], "gpu_launches": main_res["gpu_launches"], "variant": main_res["variant"],
     }
     if not args.no_prefill:
-        line["prefill"] = bench_prefill(PREFILL, max(3, min(50, args.steps // 40)), 3, local, pk,
-                                        with_cpu=(rank == 0 and args.all))
-    if args.all:
+        line["prefill"] = bench_prefill(PREFILL, psteps, 3, local, pk, with_cpu=(rank == 0 and not args.no_cpu),
+                                        with_e2e=not args.no_e2e)
+    if not args.no_secondary:
+        # the other configurations the metric covers; --all adds the extend prefill and
+        # the append kernel
         extra = []
         for name in ("tiny_mqa_decode", "fp8_decode", "sliding_decode_d256"):
-            extra.append(bench_decode(name, max(3, args.steps // 10), args.warmup, barrier, local, pk,
-                                      with_e2e=False, with_cpu=False))
-        extra.append(bench_prefill("nvfp4_asym_prefill", max(3, min(50, args.steps // 40)), 3, local, pk))
-        for split_kv in (True, False):
-            extra.append(bench_prefill("prefill_extend_bf16", max(3, min(50, args.steps // 40)), 3, local, pk,
-                                       split_kv=split_kv))
-        for name in APPEND_WORKLOADS:
-            extra.append(bench_append(name, max(3, args.steps // 10), args.warmup, local, pk))
+            extra.append(bench_decode(name, args.steps, args.warmup, barrier, local, pk, with_e2e=False,
+                                      with_cpu=False))
+        if not args.no_prefill:
+            extra.append(bench_prefill("nvfp4_asym_prefill", psteps, 3, local, pk))
+        if args.all:
+            for split_kv in (True, False):
+                extra.append(bench_prefill("prefill_extend_bf16", psteps, 3, local, pk, split_kv=split_kv))
+            for name in APPEND_WORKLOADS:
+                extra.append(bench_append(name, max(3, args.steps // 10), args.warmup, local, pk))
         line["secondary"] = extra
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -638,8 +716,7 @@ def reference_arm(args, world):
             "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": tot_t / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "bf16 GQA decode: batch 64, 24 q / 4 kv heads, head_dim 512, page_size 64, "
-                                   "kv_len uniform in [1024, 8192], shuffled pages", "name": MAIN},
+            "config": {"workload": DESCRIBE[MAIN], "name": MAIN},
             "cpu_baseline": {"kind": "oracle", "cores": threads, "sample": sample, "value": value, "unit": "GB/s"},
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)

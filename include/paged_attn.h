@@ -108,13 +108,17 @@ typedef struct {
  * bf16; lse [batch, num_qo_heads] fp32 or NULL.  Every query head of one kv head is
  * served by the same CTA (groups up to 16, padded inside the kernel).  The KV length of
  * each sequence is cut into page-aligned chunks on the device; chunks of one sequence
- * write partial (O, m, l) that a merge kernel combines.
+ * write partial (O, m, l) to the workspace that a merge kernel combines by their lse
+ * weights.
  *
  * Supported: (head_dim_qk, head_dim_vo) in {(512,512), (512,256), (256,256)};
  * num_qo_heads / num_kv_heads in [1, 16]; page_size in {1,2,4,8,16,32,64};
  * kv_dtype any pa_kv_dtype.  window_left = -1 disables the sliding window.
- * Returns PA_OK, or PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED / PA_ERR_ALIGNMENT /
- * PA_ERR_SMEM / PA_ERR_CUDA; nothing is launched on error.
+ * Returns PA_OK, or PA_ERR_INVALID_ARG (a null required pointer, batch < 0,
+ * num_pages < 1, num_qo_heads not a multiple of num_kv_heads, a non-finite sm_scale,
+ * window_left < -1, an unknown kv_dtype, missing scales), PA_ERR_UNSUPPORTED (a group
+ * num_qo_heads / num_kv_heads above 16, another head-dim pair, another page size),
+ * PA_ERR_ALIGNMENT, PA_ERR_SMEM or PA_ERR_CUDA; nothing is launched on error.
  */
 int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_indptr,
                       const int32_t* kv_indices, const int32_t* kv_last_page_len, int batch,
@@ -225,10 +229,19 @@ const char* paged_attn_status_string(int status);
  * PA_ERR_CUDA.  The next call allocates it again. */
 int paged_attn_release_workspace(void);
 
-/* Synchronises the current device, then reports and clears the device error word that
- * kernels set when a bounded wait gives up: *code = 0 (none) or the wait site id.
+/* Synchronises the current device, then reports and clears the device error words that
+ * kernels set when a bounded wait gives up (the workspace's and, once
+ * paged_attn_decode_noalloc has run on the device, the one in its fixed array):
+ * *code = 0 (none) or the wait site id (the workspace's first when both are set).
  * Returns PA_OK, PA_ERR_DEVICE when a wait gave up, PA_ERR_CUDA on a CUDA error. */
 int paged_attn_check_device_error(int* code);
+
+/* Test hook: stores `code` in a device error word of the current device (blocking):
+ * target 0 = the workspace's (allocating the workspace if there is none), 1 = the one in
+ * paged_attn_decode_noalloc's fixed array.  Lets a test check that
+ * paged_attn_check_device_error reports and clears each word without making a kernel
+ * wait time out.  Returns PA_OK, PA_ERR_INVALID_ARG or PA_ERR_CUDA. */
+int paged_attn_debug_set_error_word(int target, int code);
 
 /* Test hook for split-K: force every decode chunk to `pages` pages (0 = automatic).
  * The device still widens chunks when the workspace bound requires it.  Process-wide. */
@@ -280,12 +293,12 @@ int paged_attn_last_variant(char* buf, int len);
  * keeps it inside the array.
  *
  * The first call on a device resolves the array's device address (with that device
- * current) and caches it; make that first call before any stream capture.  Every call
- * shares the one array and it keeps the last call's contents (the call clears the
- * part that must start at zero), so calls that overlap on the GPU -- on different
- * streams, or from different threads -- race; serialise them.  A bounded wait that
- * gives up is recorded in the array's first word and is not reported by
- * paged_attn_check_device_error.
+ * current), caches it and zeroes the array's error word (a blocking cudaMemset); make
+ * that first call before any stream capture.  Every call shares the one array and it
+ * keeps the last call's contents (the planner kernel of each call rewrites the work
+ * list, and every partial is written before it is read), so calls that overlap on the
+ * GPU -- on different streams, or from different threads -- race; serialise them.  A bounded wait that gives up is recorded
+ * in the array's error word, which paged_attn_check_device_error reports and clears.
  *
  * Arguments, layouts and the supported set are those of paged_attn_decode.
  */

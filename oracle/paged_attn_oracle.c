@@ -33,7 +33,7 @@
  *    consecutive head-dim elements of one token; commit "support-or-reject-explicitly":
  *    the reference consumes the exact same quantised bytes as the kernel.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings taken where the pages are silent:
  *  - lse uses the natural log of the scaled scores.
  *  - window: a query at pos sees keys [pos - window_left, pos]; -1 means no window.
  *  - causal alignment is bottom-right: pos = kv_len - qo_len + i.

@@ -32,7 +32,8 @@ EXPORTED = ("paged_attn_decode", "paged_attn_prefill", "paged_attn_status_string
             "paged_attn_set_decode_chunk_pages", "paged_attn_last_variant",
             "paged_attn_profile_begin", "paged_attn_profile_end", "paged_attn_decode_noalloc",
             "paged_attn_set_prefill_dequant_limit", "paged_attn_set_prefill_cta_pairs",
-            "paged_attn_append_kv", "paged_attn_prefill_custom_mask", "paged_attn_set_prefill_split_kv")
+            "paged_attn_append_kv", "paged_attn_prefill_custom_mask", "paged_attn_set_prefill_split_kv",
+            "paged_attn_debug_set_error_word")
 
 _lib = None
 
@@ -75,6 +76,8 @@ def load(path: Optional[str] = None):
     lib.paged_attn_release_workspace.restype = i32
     lib.paged_attn_check_device_error.restype = i32
     lib.paged_attn_check_device_error.argtypes = [ctypes.POINTER(ctypes.c_int)]
+    lib.paged_attn_debug_set_error_word.restype = i32
+    lib.paged_attn_debug_set_error_word.argtypes = [i32, i32]
     lib.paged_attn_set_decode_chunk_pages.restype = i32
     lib.paged_attn_set_decode_chunk_pages.argtypes = [i32]
     lib.paged_attn_set_prefill_dequant_limit.restype = i32
@@ -250,6 +253,14 @@ def paged_attn_check_device_error() -> int:
     if st not in (PA_OK, PA_ERR_DEVICE):
         raise PagedAttnError(st, "paged_attn_check_device_error")
     return code.value
+
+
+def paged_attn_debug_set_error_word(target: int, code: int) -> None:
+    """Test hook: store ``code`` in the workspace's (0) or the no-alloc array's (1) device
+    error word."""
+    st = load().paged_attn_debug_set_error_word(target, code)
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_debug_set_error_word")
 
 
 def paged_attn_set_decode_chunk_pages(pages: int) -> None:

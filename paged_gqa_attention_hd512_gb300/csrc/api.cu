@@ -217,6 +217,63 @@ bool make_kv_maps(CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tsfk, CUtensorM
 }  // namespace
 }  // namespace pa
 
+// ---------------------------------------------------------------------------------------
+// paged_attn_decode_noalloc's scratch: the decode call for callers that cannot allocate
+// device memory (an engine plugin handed a fixed pool, a memory-budgeted service, code
+// that must not trigger cudaMalloc's implicit device synchronisation mid-step) uses this
+// statically sized device array instead of the grow-only workspace; it calls no
+// cudaMalloc, cudaFree or other allocating routine.
+//
+// In host code `g_pa_noalloc_scratch` names only a host-side stand-in of the device
+// array: handing it to a kernel would fault or, where the GPU can reach host memory,
+// silently use the wrong memory.  Its device address comes from cudaGetSymbolAddress,
+// resolved once per device (with that device current) by the first call on that device,
+// which also zeroes the array's error word; that first call should therefore come before
+// any stream capture.
+static __device__ __align__(256) uint8_t g_pa_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+namespace pa {
+namespace {
+void* g_noalloc_ptr[kMaxDevices] = {};
+std::mutex g_noalloc_mutex;
+
+void* noalloc_scratch(int* status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *status = PA_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_pa_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      *status = PA_ERR_CUDA;
+      return nullptr;
+    }
+    // the error word starts at zero; afterwards only paged_attn_check_device_error clears it
+    if (cudaMemset(static_cast<char*>(p) + kErrOffset, 0, sizeof(int)) != cudaSuccess) {
+      cudaGetLastError();
+      *status = PA_ERR_CUDA;
+      return nullptr;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+// Reads and clears one device error word (blocking); returns its value, or -1 on a CUDA error.
+int take_error_word(void* base) {
+  int v = 0;
+  char* e = static_cast<char*>(base) + kErrOffset;
+  if (cudaMemcpy(&v, e, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return -1;
+  if (v != 0 && cudaMemset(e, 0, sizeof v) != cudaSuccess) return -1;
+  return v;
+}
+}  // namespace
+}  // namespace pa
+
 using namespace pa;
 
 extern "C" {
@@ -311,14 +368,35 @@ int paged_attn_check_device_error(int* code) {
   if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_ws_mutex);
-  if (!g_ws[dev].base) return PA_OK;
+  // the workspace's error word and, once paged_attn_decode_noalloc has run on this
+  // device, the one in its fixed array; both are cleared, the first nonzero is reported
   int v = 0;
-  char* e = static_cast<char*>(g_ws[dev].base) + kErrOffset;
-  if (cudaMemcpy(&v, e, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return PA_ERR_CUDA;
-  if (v != 0 && cudaMemset(e, 0, sizeof v) != cudaSuccess) return PA_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    if (g_ws[dev].base) v = take_error_word(g_ws[dev].base);
+  }
+  if (v < 0) return PA_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev]) {
+      const int w = take_error_word(g_noalloc_ptr[dev]);
+      if (w < 0) return PA_ERR_CUDA;
+      if (v == 0) v = w;
+    }
+  }
   if (code) *code = v;
   return v ? PA_ERR_DEVICE : PA_OK;
+}
+
+int paged_attn_debug_set_error_word(int target, int code) {
+  if (target != 0 && target != 1) return PA_ERR_INVALID_ARG;
+  int st = PA_OK;
+  void* base = target == 0 ? workspace(kFixedBytes, &st) : noalloc_scratch(&st);
+  if (!base) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaMemcpy(static_cast<char*>(base) + kErrOffset, &code, sizeof code, cudaMemcpyHostToDevice) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
 }
 
 int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
@@ -648,7 +726,6 @@ int paged_attn_append_kv(const void* k_new, const void* v_new, const int32_t* ap
   p.num_pages = num_pages;
   p.Hkv = num_kv_heads;
   p.d_qk = head_dim_qk;
-  p.d_vo = head_dim_vo;
   p.page_size = page_size;
   prof_mark(static_cast<cudaStream_t>(stream), true);
   const cudaError_t e = launch_append_kv(kv_dtype, p, static_cast<cudaStream_t>(stream));
@@ -660,47 +737,6 @@ int paged_attn_append_kv(const void* k_new, const void* v_new, const int32_t* ap
 }
 
 }  // extern "C"
-
-// ---------------------------------------------------------------------------------------
-// paged_attn_decode_noalloc: the decode call for callers that cannot allocate device
-// memory (an engine plugin handed a fixed pool, a memory-budgeted service, code that must
-// not trigger cudaMalloc's implicit device synchronisation mid-step).  Its scratch is the
-// statically sized device array below instead of the grow-only workspace; it calls no
-// cudaMalloc, cudaFree or other allocating routine.
-//
-// In host code `g_pa_noalloc_scratch` names only a host-side stand-in of the device
-// array: handing it to a kernel would fault or, where the GPU can reach host memory,
-// silently use the wrong memory.  Its device address comes from cudaGetSymbolAddress,
-// resolved once per device (with that device current) by the first call on that device,
-// which should therefore come before any stream capture.
-static __device__ __align__(256) uint8_t g_pa_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
-
-namespace pa {
-namespace {
-void* g_noalloc_ptr[kMaxDevices] = {};
-std::mutex g_noalloc_mutex;
-
-void* noalloc_scratch(int* status) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    *status = PA_ERR_CUDA;
-    return nullptr;
-  }
-  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_pa_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      cudaGetLastError();
-      *status = PA_ERR_CUDA;
-      return nullptr;
-    }
-    g_noalloc_ptr[dev] = p;
-  }
-  return g_noalloc_ptr[dev];
-}
-}  // namespace
-}  // namespace pa
 
 extern "C" int paged_attn_decode_noalloc(const void* q, const void* kv_cache, const int32_t* kv_indptr,
                                          const int32_t* kv_indices, const int32_t* kv_last_page_len, int batch,
@@ -754,9 +790,9 @@ extern "C" int paged_attn_decode_noalloc(const void* q, const void* kv_cache, co
     return PA_ERR_CUDA;
   L.grid = grid;
   L.stream = static_cast<cudaStream_t>(stream);
-  // the error word is the only scratch that must start at zero (the planner rewrites
-  // the work list and every partial is written before it is read)
-  if (cudaMemsetAsync(ws + kErrOffset, 0, sizeof(int), L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  // nothing else must start at zero: the error word was zeroed at set-up and is cleared
+  // only by paged_attn_check_device_error, the planner rewrites the work list, and every
+  // partial is written before it is read
 
   DecodeParams& p = L.p;
   p.q = static_cast<const uint16_t*>(q);
@@ -789,9 +825,11 @@ extern "C" int paged_attn_decode_noalloc(const void* q, const void* kv_cache, co
   if (launch_decode_plan(p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
   const char* name = "?";
   cudaError_t e;
+  prof_mark(L.stream, true);
   if (kv_dtype == PA_KV_BF16) e = launch_decode_bf16(head_dim_qk, head_dim_vo, hp, L, &name);
   else if (kv_dtype == PA_KV_FP8_E4M3) e = launch_decode_fp8(head_dim_qk, head_dim_vo, hp, L, &name);
   else e = launch_decode_nvfp4(head_dim_qk, head_dim_vo, hp, L, &name);
+  prof_mark(L.stream, false);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   if (launch_decode_merge(head_dim_vo, p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
   static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};

@@ -10,8 +10,8 @@ cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t s) {
 }
 
 cudaError_t launch_decode_merge(int dvo, const DecodeParams& p, cudaStream_t s) {
-  const long rows = (long)p.batch * p.Hq;
-  const int blocks = (int)((rows * 32 + 255) / 256);
+  const long warps = (long)p.batch * p.Hq * (dvo / 128);
+  const int blocks = (int)((warps * 32 + 255) / 256);
   if (blocks == 0) return cudaSuccess;
   if (dvo == 512) decode_merge_kernel<512><<<blocks, 256, 0, s>>>(p);
   else decode_merge_kernel<256><<<blocks, 256, 0, s>>>(p);

@@ -156,53 +156,66 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
 
 // ----------------------------------------------------------------------------- merge
 // out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  lse = ln2 * (M + log2 L).
+// One warp per (sequence, query head, 128 output columns): lane s of the warp reads the
+// (m, l) of partial s (32 at a time) and forms its weight once; every lane then owns 4
+// columns and issues the loads of 8 partials before it sums them, so the warp waits on
+// L2 once per 8 partials rather than once per partial.
 template <int DVO>
 __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeParams p) {
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  constexpr int NQ = DVO / 128;  // column quarters (warps) per row
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  if (warp >= p.batch * p.Hq) return;
-  const int b = warp / p.Hq, hq = warp % p.Hq;
+  if (gw >= p.batch * p.Hq * NQ) return;
+  const int row = gw / NQ, qc = gw % NQ;
+  const int b = row / p.Hq, hq = row % p.Hq;
   const int2 si = p.seq_info[b];
   if (si.y == 1) return;  // the decode kernel wrote this row directly
-  constexpr int PER = DVO / 32;
-  uint16_t* orow = p.out + ((size_t)b * p.Hq + hq) * DVO;
+  uint2* orow = reinterpret_cast<uint2*>(p.out + (size_t)row * DVO + qc * 128) + lane;
   if (si.y == 0) {  // no visible key
-    for (int i = 0; i < PER; ++i) orow[lane + 32 * i] = 0;
-    if (p.lse && lane == 0) p.lse[(size_t)b * p.Hq + hq] = -INFINITY;
+    *orow = make_uint2(0, 0);
+    if (p.lse && qc == 0 && lane == 0) p.lse[row] = -INFINITY;
     return;
   }
+  const float2* ml = p.ws_ml + (size_t)si.x * p.Hq + hq;  // partial s at ml[s * Hq]
   float M = -INFINITY;
-  for (int s = 0; s < si.y; ++s) M = fmaxf(M, p.ws_ml[(size_t)(si.x + s) * p.Hq + hq].x);
-  float acc[PER];
+  for (int s = lane; s < si.y; s += 32) M = fmaxf(M, ml[(size_t)s * p.Hq].x);
 #pragma unroll
-  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float L = 0.f;
-  for (int s = 0; s < si.y; ++s) {
-    const size_t row = (size_t)(si.x + s) * p.Hq + hq;
-    const float2 ml = p.ws_ml[row];
-    if (ml.x == -INFINITY) continue;
-    const float w = fast_exp2(ml.x - M);
-    L += w * ml.y;
-    const float4* src = reinterpret_cast<const float4*>(p.ws_o + row * DVO);
+  const float4* src = reinterpret_cast<const float4*>(p.ws_o + ((size_t)si.x * p.Hq + hq) * DVO + qc * 128) + lane;
+  const size_t step = (size_t)p.Hq * DVO / 4;  // float4s between consecutive partials
+  for (int s0 = 0; s0 < si.y; s0 += 32) {
+    // this lane's partial s0 + lane: weight 2^(m - M) (0 for an empty partial)
+    float w = 0.f;
+    if (s0 + lane < si.y) {
+      const float2 v = ml[(size_t)(s0 + lane) * p.Hq];
+      w = v.x == -INFINITY ? 0.f : fast_exp2(v.x - M);
+      L += w * v.y;
+    }
+    const int n = min(32, si.y - s0);
+    for (int k0 = 0; k0 < n; k0 += 8) {
+      float4 v[8];
 #pragma unroll
-    for (int i = 0; i < PER / 4; ++i) {
-      float4 v = src[lane + 32 * i];
-      acc[4 * i + 0] += w * v.x;
-      acc[4 * i + 1] += w * v.y;
-      acc[4 * i + 2] += w * v.z;
-      acc[4 * i + 3] += w * v.w;
+      for (int k = 0; k < 8; ++k)
+        if (k0 + k < n) v[k] = src[(size_t)(s0 + k0 + k) * step];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w, (k0 + k) & 31);
+        if (k0 + k < n) {
+          acc.x += wk * v[k].x;
+          acc.y += wk * v[k].y;
+          acc.z += wk * v[k].z;
+          acc.w += wk * v[k].w;
+        }
+      }
     }
   }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-  for (int i = 0; i < PER / 4; ++i) {
-    uint2 packed;
-    packed.x = pack_bf16x2(acc[4 * i + 0] * inv, acc[4 * i + 1] * inv);
-    packed.y = pack_bf16x2(acc[4 * i + 2] * inv, acc[4 * i + 3] * inv);
-    reinterpret_cast<uint2*>(orow)[lane + 32 * i] = packed;
-  }
-  if (p.lse && lane == 0)
-    p.lse[(size_t)b * p.Hq + hq] = (L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  *orow = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (p.lse && qc == 0 && lane == 0) p.lse[row] = (L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
 }
 
 }  // namespace pa

@@ -34,7 +34,11 @@ KV_BF16, KV_FP8, KV_NVFP4 = 0, 1, 2
 KV_DTYPE_NAMES = {KV_BF16: "bf16", KV_FP8: "fp8_e4m3", KV_NVFP4: "nvfp4"}
 
 # tensor ids of the independent draws
-TID_Q, TID_K, TID_V, TID_LEN, TID_PERM = 1, 2, 3, 4, 5
+TID_Q, TID_K, TID_V, TID_LEN, TID_PERM, TID_OUTLIER = 1, 2, 3, 4, 5, 6
+
+# heavy tails: magnitude of the planted K / V outliers (in units of the draws' standard
+# deviation), which the bounded Irwin-Hall(4) draws never reach (|x| <= 3.46)
+OUTLIER_SIGMA = 8.0
 
 # standard deviation of the sum of four uniform integers on [0, 65535]
 _IH_SD = math.sqrt((65536.0 ** 2 - 1.0) / 3.0)
@@ -250,9 +254,23 @@ def _page_table(seed: int, kv_lens: List[int], page_size: int):
             torch.tensor(last, dtype=torch.int32), total)
 
 
+def with_outliers(x: torch.Tensor, seed: int, tid: int, start: int, every: int) -> torch.Tensor:
+    """x (bf16 draws of elements start, start + 1, ...) with element i replaced by
+    +-OUTLIER_SIGMA where a seeded hash of i is 0 modulo ``every`` (one element in
+    ``every`` on average, sign from another bit of the hash)."""
+    idx = torch.arange(start, start + x.numel(), dtype=torch.int64, device=x.device)
+    h1, _ = uniform_u32(seed, TID_OUTLIER * 16 + tid, idx)
+    hit = (h1 % every) == 0
+    sign = torch.where((h1 >> 31) & 1 == 1, -1.0, 1.0).to(torch.bfloat16)
+    flat = torch.where(hit, sign * OUTLIER_SIGMA, x.reshape(-1))
+    return flat.view(x.shape)
+
+
 def _fill_kv(case_shape, seed, kv_dtype, device, chunk_pages=None, poison=True, kv_lens=None,
-             indices=None, indptr=None):
-    """Build cache bytes, NVFP4 scale pool and the fp32 K/V scales for a page pool."""
+             indices=None, indptr=None, outlier_every=0):
+    """Build cache bytes, NVFP4 scale pool and the fp32 K/V scales for a page pool.
+    outlier_every > 0 plants +-OUTLIER_SIGMA values in K and V before quantisation (about
+    one element in outlier_every), for heavy-tailed inputs."""
     num_pages, Hkv, ps, dqk, dvo = case_shape
     k_row = Hkv * ps * dqk
     v_row = Hkv * ps * dvo
@@ -260,7 +278,10 @@ def _fill_kv(case_shape, seed, kv_dtype, device, chunk_pages=None, poison=True, 
         chunk_pages = max(1, (1 << 27) // max(1, k_row + v_row))
 
     def draw(tid, p0, p1, row):
-        return normal_bf16(seed, tid, p0 * row, (p1 - p0) * row, device).view(p1 - p0, row)
+        x = normal_bf16(seed, tid, p0 * row, (p1 - p0) * row, device)
+        if outlier_every > 0:
+            x = with_outliers(x, seed, tid, p0 * row, outlier_every)
+        return x.view(p1 - p0, row)
 
     k_scale = v_scale = 1.0
     sf = None
@@ -340,9 +361,10 @@ def make_case(phase: str, *, batch: int, Hq: int, Hkv: int, d_qk: int, d_vo: int
               page_size: int, kv_lens: List[int], qo_lens: Optional[List[int]] = None,
               kv_dtype: int = KV_BF16, sm_scale: Optional[float] = None, window_left: int = -1,
               causal: int = 1, seed: int = 1234, device="cpu", poison: bool = True,
-              extra_pages: int = 0) -> Case:
+              extra_pages: int = 0, outlier_every: int = 0) -> Case:
     """Build one call's inputs.  ``phase`` is "decode" (one query token per sequence) or
-    "prefill" (``qo_lens`` new tokens per sequence, the last ``qo_len`` of ``kv_len``)."""
+    "prefill" (``qo_lens`` new tokens per sequence, the last ``qo_len`` of ``kv_len``).
+    ``outlier_every`` > 0 gives K and V heavy tails (see with_outliers)."""
     assert len(kv_lens) == batch
     if phase == "decode":
         qo_lens = [1] * batch
@@ -355,7 +377,8 @@ def make_case(phase: str, *, batch: int, Hq: int, Hkv: int, d_qk: int, d_vo: int
         # unused physical pages at the end of the pool (never referenced)
         pass
     cache, sf, ks, vs = _fill_kv((num_pages, Hkv, page_size, d_qk, d_vo), seed, kv_dtype, device,
-                                 poison=poison, kv_lens=kv_lens, indices=indices, indptr=indptr)
+                                 poison=poison, kv_lens=kv_lens, indices=indices, indptr=indptr,
+                                 outlier_every=outlier_every)
     total_q = sum(qo_lens)
     q = normal_bf16(seed, TID_Q, 0, total_q * Hq * d_qk, device).view(total_q, Hq, d_qk)
     qo_indptr = [0]
@@ -391,6 +414,10 @@ WORKLOADS = {
     "fp8_decode": dict(
         phase="decode", batch=128, Hq=12, Hkv=4, d_qk=512, d_vo=512, page_size=16,
         kv_lens=[32768] * 128, kv_dtype=KV_FP8, seed=1003),
+    # the first 16 sequences of the FP8 decode workload (2.1 GB of KV, above L2): profiling captures
+    "fp8_decode_small": dict(
+        phase="decode", batch=16, Hq=12, Hkv=4, d_qk=512, d_vo=512, page_size=16,
+        kv_lens=[32768] * 16, kv_dtype=KV_FP8, seed=1003),
     "causal_prefill_bf16": dict(
         phase="prefill", batch=4, Hq=24, Hkv=4, d_qk=512, d_vo=512, page_size=64,
         kv_lens=[2048, 3000, 4096, 6272], qo_lens=[2048, 3000, 4096, 6272],
@@ -413,6 +440,70 @@ def workload(name: str, device="cpu", poison: bool = True) -> Case:
     if w["kv_lens"] is None:
         w["kv_lens"] = _cfg2_lens(w["batch"])
     return make_case(device=device, poison=poison, **w)
+
+
+# --------------------------------------------------------------------------------------
+# batch partitions across ranks (sequences are independent: no exchange between shards)
+# --------------------------------------------------------------------------------------
+def shard_sequences(batch: int, rank: int, world: int) -> range:
+    """Global sequence ids of shard ``rank`` when a batch of ``batch`` sequences is cut
+    into ``world`` contiguous shards whose sizes differ by at most one."""
+    assert 0 <= rank < world
+    base, extra = divmod(batch, world)
+    start = rank * base + min(rank, extra)
+    return range(start, start + base + (1 if rank < extra else 0))
+
+
+def workload_shard(name: str, rank: int, world: int, device="cpu", poison: bool = True) -> Case:
+    """Shard ``rank`` of a global batch of ``world`` x batch sequences of workload ``name``
+    (weak scaling: every shard has the workload's batch).  Sequence lengths are those of
+    the global sequence ids; each shard has its own page pool and draws its values under
+    its own seed (rank 0 under the workload's seed, so shard 0 of any world is the
+    single-GPU workload)."""
+    w = dict(WORKLOADS[name])
+    ids = shard_sequences(w["batch"] * world, rank, world)
+    if w["kv_lens"] is None:
+        w["kv_lens"] = [randint(w["seed"], TID_LEN, b, 1024, 8192) for b in ids]
+    w["seed"] = w["seed"] + 100003 * rank
+    return make_case(device=device, poison=poison, **w)
+
+
+def concat_cases(cases: List[Case]) -> Case:
+    """One host case holding every sequence of ``cases`` in order (page pools appended,
+    page ids and query rows offset); the cases must share shapes, dtype and scales."""
+    c0 = cases[0]
+    for c in cases[1:]:
+        for k in ("phase", "Hq", "Hkv", "d_qk", "d_vo", "page_size", "kv_dtype", "sm_scale", "window_left",
+                  "causal", "k_scale", "v_scale"):
+            assert getattr(c, k) == getattr(c0, k), k
+    ind, ip, qo, last, q, cache, sf = [], [0], [0], [], [], [], []
+    page0 = 0
+    for c in cases:
+        c = c.to("cpu")
+        ind.append(c.kv_indices + page0)
+        for x in (c.kv_indptr[1:] - c.kv_indptr[:-1]).tolist():
+            ip.append(ip[-1] + int(x))
+        for x in (c.qo_indptr[1:] - c.qo_indptr[:-1]).tolist():
+            qo.append(qo[-1] + int(x))
+        last.append(c.kv_last_page_len)
+        q.append(c.q)
+        cache.append(c.kv_cache)
+        if c.sf is not None:
+            sf.append(c.sf)
+        page0 += c.num_pages
+    out = Case(**{k: getattr(c0, k) for k in c0.__dataclass_fields__})
+    out.batch = sum(c.batch for c in cases)
+    out.num_pages = page0
+    out.q = torch.cat(q)
+    out.qo_indptr = torch.tensor(qo, dtype=torch.int32)
+    out.kv_cache = torch.cat(cache)
+    out.kv_indptr = torch.tensor(ip, dtype=torch.int32)
+    out.kv_indices = torch.cat(ind).to(torch.int32)
+    out.kv_last_page_len = torch.cat(last)
+    out.sf = torch.cat(sf) if sf else None
+    out.kv_lens = [L for c in cases for L in c.kv_lens]
+    out.qo_lens = [L for c in cases for L in c.qo_lens]
+    return out
 
 
 def workload_kv_lens(name: str) -> List[int]:

@@ -137,3 +137,33 @@ def test_mode_setters_reject_other_values(lib):
     assert lib.paged_attn_set_prefill_split_kv(1) == pa.PA_ERR_INVALID_ARG
     assert lib.paged_attn_set_prefill_cta_pairs(-1) == pa.PA_OK
     assert lib.paged_attn_set_prefill_split_kv(-1) == pa.PA_OK
+
+
+def _decode_noalloc(lib, **over):
+    a = dict(q=FAKE, kv=FAKE, ip=FAKE, ind=FAKE, last=FAKE, batch=2, num_pages=4, hq=8, hkv=1,
+             dqk=512, dvo=512, ps=16, scale=0.04, win=-1, dt=0, out=FAKE, lse=None)
+    a.update(over)
+    sc = pa._Scales(None, None, None)
+    return lib.paged_attn_decode_noalloc(a["q"], a["kv"], a["ip"], a["ind"], a["last"], a["batch"],
+                                         a["num_pages"], a["hq"], a["hkv"], a["dqk"], a["dvo"], a["ps"],
+                                         a["scale"], a["win"], a["dt"], ctypes.byref(sc), a["out"], a["lse"], None)
+
+
+def test_decode_noalloc_rejects_bad_arguments(lib):
+    assert _decode_noalloc(lib, batch=0) == pa.PA_OK  # nothing to do
+    assert _decode_noalloc(lib, q=None) == pa.PA_ERR_INVALID_ARG
+    assert _decode_noalloc(lib, out=None) == pa.PA_ERR_INVALID_ARG
+    assert _decode_noalloc(lib, kv=None) == pa.PA_ERR_INVALID_ARG
+    assert _decode_noalloc(lib, hq=7, hkv=2) == pa.PA_ERR_INVALID_ARG
+    assert _decode_noalloc(lib, hq=34, hkv=2) == pa.PA_ERR_UNSUPPORTED  # group 17
+    assert _decode_noalloc(lib, ps=3) == pa.PA_ERR_UNSUPPORTED
+    assert _decode_noalloc(lib, q=FAKE + 8) == pa.PA_ERR_ALIGNMENT
+    assert _decode_noalloc(lib, out=FAKE + 4) == pa.PA_ERR_ALIGNMENT
+    assert _decode_noalloc(lib, lse=FAKE + 2) == pa.PA_ERR_ALIGNMENT
+    assert _decode_noalloc(lib, dt=2) == pa.PA_ERR_INVALID_ARG  # NVFP4 without scales
+    assert _decode_noalloc(lib, win=-3) == pa.PA_ERR_INVALID_ARG
+
+
+def test_debug_error_hook_rejects_unknown_target(lib):
+    assert lib.paged_attn_debug_set_error_word(2, 5) == pa.PA_ERR_INVALID_ARG
+    assert lib.paged_attn_debug_set_error_word(-1, 5) == pa.PA_ERR_INVALID_ARG

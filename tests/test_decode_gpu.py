@@ -133,3 +133,15 @@ def test_synth_cpu_and_gpu_inputs_are_identical():
         assert a.k_scale == b.k_scale and a.v_scale == b.v_scale
         if dt == NVFP4:
             assert torch.equal(a.sf, b.sf.cpu())
+
+
+@pytest.mark.parametrize("dt", [BF16, FP8, NVFP4])
+def test_decode_heavy_tailed_kv(dt):
+    """K and V with +-8 sigma outliers (one element in 16 on average), which the bounded
+    synthetic draws never reach: the FP8 per-tensor scale and the NVFP4 global and block
+    scales are set by the tails, most values sit far below them."""
+    case = synth.make_case("decode", batch=4, Hq=12, Hkv=4, d_qk=512, d_vo=512, page_size=16,
+                           kv_lens=[300, 17, 129, 64], kv_dtype=dt, seed=47, outlier_every=16)
+    check_full(case, "heavy tails")
+    pa.paged_attn_set_decode_chunk_pages(2)
+    check_full(case, "heavy tails, split")

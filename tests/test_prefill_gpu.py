@@ -147,3 +147,16 @@ def test_prefill_parity_quantised(c, mode, _dequant_limit):
     names = {synth.KV_FP8: "fp8", synth.KV_NVFP4: "nvfp4"}
     suffix = "_dequant" if mode == "dequant" else ""
     assert _variant() == f"prefill_{dqk}x{dvo}_{names[dt]}{suffix}"
+
+
+@pytest.mark.parametrize("dt,mode", [(BF16, "dequant"), (synth.KV_FP8, "dequant"), (synth.KV_FP8, "in_kernel"),
+                                     (synth.KV_NVFP4, "dequant"), (synth.KV_NVFP4, "in_kernel")])
+def test_prefill_heavy_tailed_kv(dt, mode, _dequant_limit):
+    """K and V with +-8 sigma outliers (one element in 16 on average): the FP8 per-tensor
+    scale and the NVFP4 global and block scales are set by the tails (FP8 / NVFP4 through
+    the bf16 copy and converted inside the kernel)."""
+    ensure_built()
+    pa.paged_attn_set_prefill_dequant_limit(-1 if mode == "dequant" else 0)
+    case = synth.make_case("prefill", batch=2, Hq=16, Hkv=2, d_qk=512, d_vo=512, page_size=16,
+                           kv_lens=[300, 129], qo_lens=[300, 129], kv_dtype=dt, seed=48, outlier_every=16)
+    check_full(case, f"heavy tails {mode}")
