@@ -149,6 +149,25 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t row
   return r == CUDA_SUCCESS;
 }
 
+// 4-D byte tensor [pages][segments][rows][128 B] over rows of row_bytes = segments x 128 B
+// (the segment dimension steps 128 bytes inside a row); boxes of [1][segments][box_rows]
+// [128 B]: every segment of box_rows consecutive rows of one page in one load.
+bool make_map_rows(CUtensorMap* m, const void* base, uint64_t row_bytes, uint64_t rows, uint64_t pages,
+                   uint64_t page_stride, uint32_t box_rows, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const uint64_t segs = row_bytes / 128;
+  cuuint64_t dims[4] = {128, rows, segs, pages};
+  cuuint64_t strides[3] = {row_bytes, 128, page_stride};
+  cuuint32_t box[4] = {128, box_rows, (cuuint32_t)segs, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 int x2_of(int kvt) { return kvt == KV_BF16 ? 4 : (kvt == KV_FP8 ? 2 : 1); }
@@ -203,6 +222,29 @@ bool make_kv_maps(CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tsfk, CUtensorM
   const uint8_t* base = static_cast<const uint8_t*>(kv_cache);
   if (!make_map(tk, base, k_row, rows, num_pages, page_bytes, box_inner, box_rows, swz)) return false;
   if (!make_map(tv, base + rows * k_row, v_row, rows, num_pages, page_bytes, box_inner, box_rows, swz)) return false;
+  if (kvt == KV_NVFP4) {
+    const uint64_t sk = dqk / 16, sv = dvo / 16, sf_page = rows * (sk + sv);
+    if (!make_map(tsfk, sf, sk, rows, num_pages, sf_page, (uint32_t)sk, box_rows, false)) return false;
+    if (!make_map(tsfv, sf + rows * sk, sv, rows, num_pages, sf_page, (uint32_t)sv, box_rows, false)) return false;
+  } else {
+    *tsfk = *tk;
+    *tsfv = *tv;
+  }
+  return true;
+}
+
+// Decode: K and V maps whose boxes hold every 128-byte segment of box_rows rows of one
+// page (one load per page piece), NVFP4 scale maps as for the prefill.
+bool make_decode_maps(CUtensorMap* tk, CUtensorMap* tv, CUtensorMap* tsfk, CUtensorMap* tsfv, const void* kv_cache,
+                      const uint8_t* sf, int num_pages, int Hkv, int dqk, int dvo, int ps, int kvt, int box_rows,
+                      bool swz) {
+  const int x2 = x2_of(kvt);
+  const uint64_t k_row = (uint64_t)dqk * x2 / 2, v_row = (uint64_t)dvo * x2 / 2;
+  const uint64_t rows = (uint64_t)Hkv * ps;
+  const uint64_t page_bytes = rows * (k_row + v_row);
+  const uint8_t* base = static_cast<const uint8_t*>(kv_cache);
+  if (!make_map_rows(tk, base, k_row, rows, num_pages, page_bytes, box_rows, swz)) return false;
+  if (!make_map_rows(tv, base + rows * k_row, v_row, rows, num_pages, page_bytes, box_rows, swz)) return false;
   if (kvt == KV_NVFP4) {
     const uint64_t sk = dqk / 16, sv = dvo / 16, sf_page = rows * (sk + sv);
     if (!make_map(tsfk, sf, sk, rows, num_pages, sf_page, (uint32_t)sk, box_rows, false)) return false;
@@ -422,8 +464,8 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
   const int T = decode_tile_tokens(kv_dtype, head_dim_qk);
   const int box_rows = page_size < T ? page_size : T;
   const bool swz = page_size >= 8;
-  if (!make_kv_maps(&L.tk, &L.tv, &L.tsfk, &L.tsfv, kv_cache, kv_scales ? kv_scales->sf : nullptr, num_pages,
-                    num_kv_heads, head_dim_qk, head_dim_vo, page_size, kv_dtype, box_rows, swz))
+  if (!make_decode_maps(&L.tk, &L.tv, &L.tsfk, &L.tsfv, kv_cache, kv_scales ? kv_scales->sf : nullptr, num_pages,
+                        num_kv_heads, head_dim_qk, head_dim_vo, page_size, kv_dtype, box_rows, swz))
     return PA_ERR_CUDA;
 
   const int grid = sms;
@@ -464,6 +506,7 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
   p.target_chunks = target;
   p.forced_chunk_pages = forced;
   p.box_rows = box_rows;
+  p.box_shift = __builtin_ctz((unsigned)box_rows);
   p.swz = swz ? 7 : 0;
   p.sm_scale = sm_scale;
   L.grid = grid;
@@ -590,6 +633,8 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   p.k_scale = kv_dtype != PA_KV_BF16 ? kv_scales->k_scale : nullptr;
   p.v_scale = kv_dtype != PA_KV_BF16 ? kv_scales->v_scale : nullptr;
   p.kv_cache = static_cast<const uint8_t*>(kv_cache);
+  p.kv_bf16 = static_cast<const uint8_t*>(kv_read);
+  p.kv_bf16_page_bytes = (long long)bf16_page;
   p.sf = kv_scales ? kv_scales->sf : nullptr;
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
@@ -785,8 +830,8 @@ extern "C" int paged_attn_decode_noalloc(const void* q, const void* kv_cache, co
   const int T = decode_tile_tokens(kv_dtype, head_dim_qk);
   const int box_rows = page_size < T ? page_size : T;
   const bool swz = page_size >= 8;
-  if (!make_kv_maps(&L.tk, &L.tv, &L.tsfk, &L.tsfv, kv_cache, kv_scales ? kv_scales->sf : nullptr, num_pages,
-                    num_kv_heads, head_dim_qk, head_dim_vo, page_size, kv_dtype, box_rows, swz))
+  if (!make_decode_maps(&L.tk, &L.tv, &L.tsfk, &L.tsfv, kv_cache, kv_scales ? kv_scales->sf : nullptr, num_pages,
+                        num_kv_heads, head_dim_qk, head_dim_vo, page_size, kv_dtype, box_rows, swz))
     return PA_ERR_CUDA;
   L.grid = grid;
   L.stream = static_cast<cudaStream_t>(stream);
@@ -819,6 +864,7 @@ extern "C" int paged_attn_decode_noalloc(const void* q, const void* kv_cache, co
   p.target_chunks = (int)target;
   p.forced_chunk_pages = forced;
   p.box_rows = box_rows;
+  p.box_shift = __builtin_ctz((unsigned)box_rows);
   p.swz = swz ? 7 : 0;
   p.sm_scale = sm_scale;
 

@@ -222,12 +222,15 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeParams p) {
 
 namespace pa {
 
-// Byte address inside a K or V tile: row t, byte offset bo within the row.  Rows are
-// split into 128-byte segments stored [segment][row][128 B]; with swizzling the 16-byte
-// chunks of a row are permuted by (row & 7), exactly as the 128B-swizzled TMA writes them.
-template <int T>
-__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int t, int bo, int swz) {
-  return base + (uint32_t)((bo >> 7) * (T * 128) + t * 128 + ((((bo >> 4) & 7) ^ (t & swz)) << 4));
+// Byte address inside a K or V tile: row t, byte offset bo within the row.  A tile is a
+// run of pieces of box_rows = 2^lbr rows (one page, or part of one); each piece is one TMA
+// box stored [128-byte segment][row][128 B], SEGS segments per row.  With swizzling the
+// 16-byte chunks of a row are permuted by (row & 7), exactly as the 128B-swizzled TMA
+// writes them (box_rows is then a multiple of 8, so the row's phase is t & 7).
+template <int SEGS>
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int t, int bo, int swz, int lbr) {
+  const int piece = t >> lbr, r = t & ((1 << lbr) - 1);
+  return base + (uint32_t)(((piece * SEGS + (bo >> 7)) << (lbr + 7)) + r * 128 + ((((bo >> 4) & 7) ^ (t & swz)) << 4));
 }
 
 // First of the two consecutive head-dim indices held by B-fragment register `half` of
@@ -336,12 +339,9 @@ __global__ void __launch_bounds__(288, 1)
           const int tok = tok0 + k * br;
           const int page = p.kv_indices[ip0 + tok / ps];
           const int row = kvh * ps + tok % ps;
-#pragma unroll
-          for (int sg = 0; sg < C::K_SEGS; ++sg)
-            tma_load_3d(kbase + sg * (T * 128) + k * br * 128, &tm_k, sg * 128, row, page, &full[s]);
-#pragma unroll
-          for (int sg = 0; sg < C::V_SEGS; ++sg)
-            tma_load_3d(vbase + sg * (T * 128) + k * br * 128, &tm_v, sg * 128, row, page, &full[s]);
+          // the piece's rows of every 128-byte segment in one box ([segment][row][128 B])
+          tma_load_4d(kbase + k * br * C::K_ROW, &tm_k, 0, row, 0, page, &full[s]);
+          tma_load_4d(vbase + k * br * C::V_ROW, &tm_v, 0, row, 0, page, &full[s]);
           if constexpr (KVT == KV_NVFP4) {
             tma_load_3d(sfkbase + k * br * C::SFK_ROW, &tm_sfk, 0, row, page, &full[s]);
             tma_load_3d(sfvbase + k * br * C::SFV_ROW, &tm_sfv, 0, row, page, &full[s]);
@@ -360,6 +360,7 @@ __global__ void __launch_bounds__(288, 1)
   const int dqk0 = dq * C::DQW;  // QK^T head-dim slice of this warp
   const int dv0 = cw * C::DVW;   // output columns of this warp
   const int swz = p.swz;
+  const int lbr = p.box_shift;
   const int gsz = p.group;
   const float kscale = BF ? 1.f : __ldg(p.k_scale);
   const float vscale = BF ? 1.f : __ldg(p.v_scale);
@@ -467,8 +468,8 @@ __global__ void __launch_bounds__(288, 1)
         for (int idx = threadIdx.x; idx < nrow * C::V_SEGS * 8; idx += 256) {
           const int r = n_valid + idx / (C::V_SEGS * 8);
           const int rem = idx % (C::V_SEGS * 8);
-          *reinterpret_cast<uint4*>(vp + (rem >> 3) * (T * 128) + r * 128 + (rem & 7) * 16) =
-              make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vp + ((((r >> lbr) * C::V_SEGS + (rem >> 3)) << (lbr + 7)) +
+                                          (r & ((1 << lbr) - 1)) * 128 + (rem & 7) * 16)) = make_uint4(0, 0, 0, 0);
         }
         if constexpr (KVT == KV_NVFP4) {
           uint8_t* sv = kp + C::K_TILE + C::V_TILE + C::SFK_TILE;
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(288, 1)
           uint32_t a0, a1, a2, a3;
           const int t = t0 + mr + 8 * (mat & 1);
           const int d = dqk0 + 16 * ks + 8 * (mat >> 1);
-          ldsm_x4(tile_addr<T>(kbase, t, 2 * d, swz), a0, a1, a2, a3);
+          ldsm_x4(tile_addr<C::K_SEGS>(kbase, t, 2 * d, swz, lbr), a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) mma16816<true>(sacc[nt], a0, a1, a2, a3, qf[ks][nt][0], qf[ks][nt][1]);
         }
@@ -500,7 +501,7 @@ __global__ void __launch_bounds__(288, 1)
           uint32_t R[4];
           const int t = t0 + mr + 8 * (mat & 1);
           const int d = dqk0 + 32 * kg + 16 * (mat >> 1);
-          ldsm_x4(tile_addr<T>(kbase, t, d, swz), R[0], R[1], R[2], R[3]);
+          ldsm_x4(tile_addr<C::K_SEGS>(kbase, t, d, swz, lbr), R[0], R[1], R[2], R[3]);
 #pragma unroll
           for (int sub = 0; sub < 2; ++sub) {
             const uint32_t ra = R[2 * sub], rb = R[2 * sub + 1];
@@ -517,7 +518,7 @@ __global__ void __launch_bounds__(288, 1)
           uint32_t R[4];
           const int t = t0 + mr + 8 * (mat & 1);
           const int d = dqk0 + 64 * kg + 32 * (mat >> 1);
-          ldsm_x4(tile_addr<T>(kbase, t, d >> 1, swz), R[0], R[1], R[2], R[3]);
+          ldsm_x4(tile_addr<C::K_SEGS>(kbase, t, d >> 1, swz, lbr), R[0], R[1], R[2], R[3]);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {  // head-dim halves: +0 (R0, R1), +32 (R2, R3)
             const int blk = (dqk0 + 64 * kg + 32 * hh + 8 * tig) >> 4;
@@ -626,7 +627,7 @@ __global__ void __launch_bounds__(288, 1)
             uint32_t a0, a1, a2, a3;
             const int t = tb + mr + 8 * (mat >> 1);
             const int d = dv0 + 16 * i + 8 * (mat & 1);
-            ldsm_x4_t(tile_addr<T>(vbase, t, 2 * d, swz), a0, a1, a2, a3);
+            ldsm_x4_t(tile_addr<C::V_SEGS>(vbase, t, 2 * d, swz, lbr), a0, a1, a2, a3);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) mma16816<true>(o[i][nt], a0, a1, a2, a3, pb[nt][0], pb[nt][1]);
           }
@@ -636,7 +637,7 @@ __global__ void __launch_bounds__(288, 1)
             uint32_t R[4];
             const int t = tb + mr + 8 * (mat & 1);
             const int d = dv0 + 32 * ip + 16 * (mat >> 1);
-            ldsm_x4_t(tile_addr<T>(vbase, t, d, swz), R[0], R[1], R[2], R[3]);
+            ldsm_x4_t(tile_addr<C::V_SEGS>(vbase, t, d, swz, lbr), R[0], R[1], R[2], R[3]);
 #pragma unroll
             for (int sub = 0; sub < 2; ++sub) {
               const uint32_t ra = R[2 * sub], rb = R[2 * sub + 1];
@@ -652,9 +653,9 @@ __global__ void __launch_bounds__(288, 1)
           const int t = tb + mr + 8 * (mat & 1);
           const int d = dv0 + 32 * (mat >> 1);
           if constexpr (C::DVW == 64) {
-            ldsm_x4_t(tile_addr<T>(vbase, t, d >> 1, swz), R[0], R[1], R[2], R[3]);
+            ldsm_x4_t(tile_addr<C::V_SEGS>(vbase, t, d >> 1, swz, lbr), R[0], R[1], R[2], R[3]);
           } else {
-            ldsm_x2_t(tile_addr<T>(vbase, t, (dv0 >> 1), swz), R[0], R[1]);
+            ldsm_x2_t(tile_addr<C::V_SEGS>(vbase, t, (dv0 >> 1), swz, lbr), R[0], R[1]);
             R[2] = R[3] = 0;
           }
 #pragma unroll

@@ -50,8 +50,9 @@ struct DecodeParams {
   float2* ws_ml;      // [max_chunks][Hq] {running max (log2 units), running sum}
   int batch, Hq, Hkv, group, page_size, window_left;
   int max_chunks, target_chunks, forced_chunk_pages;
-  int box_rows;  // rows per TMA box: min(page_size, tile tokens)
-  int swz;       // 7 when the K/V smem tiles are 128B-swizzled, 0 when not
+  int box_rows;   // rows per TMA box: min(page_size, tile tokens), a power of two
+  int box_shift;  // log2(box_rows)
+  int swz;        // 7 when the K/V smem tiles are 128B-swizzled, 0 when not
   float sm_scale;
 };
 
@@ -82,6 +83,10 @@ struct PrefillParams {
   const float* k_scale;
   const float* v_scale;
   const uint8_t* kv_cache;  // for the plain-load (dequantising) producer
+  // the bf16 pages the tensor maps read (the cache itself, or its bf16 copy), for L2
+  // prefetches ahead of the TMA loads
+  const uint8_t* kv_bf16;
+  long long kv_bf16_page_bytes;
   const uint8_t* sf;
   uint16_t* out;  // bf16 [total_q, Hq, d_vo]
   float* lse;
