@@ -633,8 +633,6 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   p.k_scale = kv_dtype != PA_KV_BF16 ? kv_scales->k_scale : nullptr;
   p.v_scale = kv_dtype != PA_KV_BF16 ? kv_scales->v_scale : nullptr;
   p.kv_cache = static_cast<const uint8_t*>(kv_cache);
-  p.kv_bf16 = static_cast<const uint8_t*>(kv_read);
-  p.kv_bf16_page_bytes = (long long)bf16_page;
   p.sf = kv_scales ? kv_scales->sf : nullptr;
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;
@@ -670,8 +668,9 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   L.grid = pair_grid > 0 ? pair_grid : sms;
   L.stream = static_cast<cudaStream_t>(stream);
 
+  DequantParams d;
+  std::memset(&d, 0, sizeof d);
   if (dequant) {
-    DequantParams d;
     d.cache = static_cast<const uint8_t*>(kv_cache);
     d.sf = kv_scales->sf;
     d.kv_indptr = kv_indptr;
@@ -680,10 +679,9 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
     d.batch = batch;
     d.Hkv = num_kv_heads;
     d.page_size = page_size;
-    if (launch_prefill_dequant(kv_dtype, head_dim_qk, head_dim_vo, d, 4 * sms, L.stream) != cudaSuccess)
-      return PA_ERR_CUDA;
   }
-  if (launch_prefill_plan(p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_prefill_prep(kv_dtype, head_dim_qk, head_dim_vo, dequant, p, d, sms, L.stream) != cudaSuccess)
+    return PA_ERR_CUDA;
   const char* name = "?";
   prof_mark(L.stream, true);
   cudaError_t e = launch_prefill(run_kvt, head_dim_qk, head_dim_vo, L, &name);
@@ -771,6 +769,7 @@ int paged_attn_append_kv(const void* k_new, const void* v_new, const int32_t* ap
   p.num_pages = num_pages;
   p.Hkv = num_kv_heads;
   p.d_qk = head_dim_qk;
+  p.d_vo = head_dim_vo;
   p.page_size = page_size;
   prof_mark(static_cast<cudaStream_t>(stream), true);
   const cudaError_t e = launch_append_kv(kv_dtype, p, static_cast<cudaStream_t>(stream));

@@ -13,9 +13,9 @@ cudaError_t launch_decode_merge(int dvo, const DecodeParams& p, cudaStream_t s) 
   const long warps = (long)p.batch * p.Hq * (dvo / 128);
   const int blocks = (int)((warps * 32 + 255) / 256);
   if (blocks == 0) return cudaSuccess;
-  if (dvo == 512) decode_merge_kernel<512><<<blocks, 256, 0, s>>>(p);
-  else decode_merge_kernel<256><<<blocks, 256, 0, s>>>(p);
-  return cudaGetLastError();
+  // a programmatic dependent of the decode kernel
+  if (dvo == 512) return launch_pdl(decode_merge_kernel<512>, dim3(blocks), dim3(256), 0, s, 1, p);
+  return launch_pdl(decode_merge_kernel<256>, dim3(blocks), dim3(256), 0, s, 1, p);
 }
 
 int decode_smem_bytes(int kvt, int dqk, int dvo, int hp) {

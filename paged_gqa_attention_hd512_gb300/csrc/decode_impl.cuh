@@ -73,6 +73,7 @@ struct DecodeSmem {
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
   __shared__ int s_red[32];
   __shared__ int s_carry;
+  grid_dep_launch();  // the decode kernel may start its set-up (it waits for this grid)
   const int tid = threadIdx.x;
   const int ps = p.page_size;
   // pass 1: total visible pages
@@ -163,6 +164,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
 template <int DVO>
 __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeParams p) {
   constexpr int NQ = DVO / 128;  // column quarters (warps) per row
+  grid_dep_wait();  // the decode kernel's partials are complete
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (gw >= p.batch * p.Hq * NQ) return;
@@ -304,6 +306,7 @@ __global__ void __launch_bounds__(288, 1)
     fence_mbar_init();
   }
   __syncthreads();
+  grid_dep_wait();  // the planner of this call is complete
   const int n_items = p.hdr[0] * p.Hkv;
   const int ps = p.page_size;
 

@@ -14,8 +14,8 @@ static cudaError_t run_decode(const DecodeLaunch& L) {
   auto kern = decode_kernel<KVT, DQK, DVO, HP>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::ALLOC);
   if (e != cudaSuccess) return e;
-  kern<<<L.grid, 288, Sm::ALLOC, L.stream>>>(L.tk, L.tv, L.tsfk, L.tsfv, L.p);
-  return cudaGetLastError();
+  // a programmatic dependent of the planner
+  return launch_pdl(kern, dim3(L.grid), dim3(288), Sm::ALLOC, L.stream, 1, L.tk, L.tv, L.tsfk, L.tsfv, L.p);
 }
 
 template <int KVT>

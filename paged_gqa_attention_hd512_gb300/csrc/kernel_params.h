@@ -83,10 +83,6 @@ struct PrefillParams {
   const float* k_scale;
   const float* v_scale;
   const uint8_t* kv_cache;  // for the plain-load (dequantising) producer
-  // the bf16 pages the tensor maps read (the cache itself, or its bf16 copy), for L2
-  // prefetches ahead of the TMA loads
-  const uint8_t* kv_bf16;
-  long long kv_bf16_page_bytes;
   const uint8_t* sf;
   uint16_t* out;  // bf16 [total_q, Hq, d_vo]
   float* lse;

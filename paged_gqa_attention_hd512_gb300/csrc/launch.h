@@ -24,6 +24,34 @@ struct PrefillLaunch {
   cudaStream_t stream;
 };
 
+// Launch `kern` on `stream` with programmatic stream serialization: it may begin while
+// the preceding kernel on the stream finishes (the kernel itself waits for that one
+// before it touches global memory, see grid_dep_wait in common.cuh).
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster_x,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // Each returns cudaSuccess or the launch error; `variant` receives a static name.
 // Returns cudaErrorInvalidValue for a shape that has no instantiation.
 cudaError_t launch_decode_bf16(int dqk, int dvo, int hp, const DecodeLaunch& L, const char** variant);
@@ -37,7 +65,10 @@ int decode_smem_bytes(int kvt, int dqk, int dvo, int hp);
 int decode_tile_tokens(int kvt, int dqk);
 
 cudaError_t launch_prefill(int kvt, int dqk, int dvo, const PrefillLaunch& L, const char** variant);
-cudaError_t launch_prefill_plan(const PrefillParams& p, cudaStream_t s);
+// The prefill's planner (block 0) and, for FP8 / NVFP4 pages converted to a bf16 copy
+// (dequant true), the conversion (the other blocks), in one launch.
+cudaError_t launch_prefill_prep(int kvt, int dqk, int dvo, bool dequant, const PrefillParams& p,
+                                const DequantParams& d, int sms, cudaStream_t s);
 // Split KV: merges the partial slots the plan listed (hdr[1] entries) into the output.
 cudaError_t launch_prefill_merge(int dvo, const PrefillParams& p, int grid, cudaStream_t s);
 int prefill_smem_bytes(int kvt, int dqk, int dvo);
@@ -45,7 +76,5 @@ int prefill_smem_bytes(int kvt, int dqk, int dvo);
 int prefill_pair_clusters(int dqk, int dvo);
 // New tokens' bf16 K / V -> the paged cache in its element type (quantise-on-write).
 cudaError_t launch_append_kv(int kvt, const AppendParams& p, cudaStream_t s);
-// FP8 / NVFP4 pages referenced by kv_indices -> bf16 pages of the same index.
-cudaError_t launch_prefill_dequant(int kvt, int dqk, int dvo, const DequantParams& d, int grid, cudaStream_t s);
 
 }  // namespace pa

@@ -1,9 +1,47 @@
-// prefill.cu -- instantiates the tcgen05 prefill kernel and its planner.
+// prefill.cu -- instantiates the tcgen05 prefill kernel and its preparation kernel
+// (planner, plus the bf16 copy of FP8 / NVFP4 pages).
 #define PA_PREFILL_PLAN 1
 #include "launch.h"
+#include "prefill_dequant.cuh"
 #include "prefill_impl.cuh"
 
 namespace pa {
+
+// Block 0 plans the work items; blocks 1.. (FP8 / NVFP4 pages converted to a bf16 copy)
+// convert the pages.  The prefill kernel that follows is launched as its programmatic
+// dependent and waits for the whole grid before it reads either result.
+template <int KVT, int DQK, int DVO>
+__global__ void __launch_bounds__(1024) prefill_prep_kernel(const PrefillParams p, const DequantParams d) {
+  grid_dep_launch();
+  if (blockIdx.x == 0) {
+    prefill_plan_body(p);
+    return;
+  }
+  if constexpr (KVT != KV_BF16) prefill_dequant_body<KVT, DQK, DVO>(d, blockIdx.x - 1, gridDim.x - 1);
+}
+
+template <int KVT>
+static cudaError_t run_prep(int dqk, int dvo, int grid, const PrefillParams& p, const DequantParams& d,
+                            cudaStream_t s) {
+  if (dqk == 512 && dvo == 512) prefill_prep_kernel<KVT, 512, 512><<<grid, 1024, 0, s>>>(p, d);
+  else if (dqk == 512 && dvo == 256) prefill_prep_kernel<KVT, 512, 256><<<grid, 1024, 0, s>>>(p, d);
+  else if (dqk == 256 && dvo == 256) prefill_prep_kernel<KVT, 256, 256><<<grid, 1024, 0, s>>>(p, d);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_prep(int kvt, int dqk, int dvo, bool dequant, const PrefillParams& p,
+                                const DequantParams& d, int sms, cudaStream_t s) {
+  if (!dequant) {
+    prefill_prep_kernel<KV_BF16, 512, 512><<<1, 1024, 0, s>>>(p, d);
+    return cudaGetLastError();
+  }
+  // two 1024-thread blocks per SM convert, all resident at once
+  const int grid = 1 + 2 * sms;
+  if (kvt == KV_FP8) return run_prep<KV_FP8>(dqk, dvo, grid, p, d, s);
+  if (kvt == KV_NVFP4) return run_prep<KV_NVFP4>(dqk, dvo, grid, p, d, s);
+  return cudaErrorInvalidValue;
+}
 
 template <int KVT, int DQK, int DVO, bool PAIR>
 static cudaError_t run_prefill(const PrefillLaunch& L) {
@@ -11,25 +49,10 @@ static cudaError_t run_prefill(const PrefillLaunch& L) {
   auto kern = prefill_kernel<KVT, DQK, DVO, PAIR>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC);
   if (e != cudaSuccess) return e;
-  if constexpr (PAIR) {
-    // clusters of two CTAs (one per SM of a pair)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(L.grid);
-    cfg.blockDim = dim3(C::THREADS);
-    cfg.dynamicSmemBytes = C::ALLOC;
-    cfg.stream = L.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, L.tq, L.tk, L.tv, L.tsfk, L.tsfv, L.tp, L.p);
-  } else {
-    kern<<<L.grid, C::THREADS, C::ALLOC, L.stream>>>(L.tq, L.tk, L.tv, L.tsfk, L.tsfv, L.tp, L.p);
-    return cudaGetLastError();
-  }
+  // a programmatic dependent of the preparation kernel (pairs: clusters of two CTAs, one
+  // per SM of a pair)
+  return launch_pdl(kern, dim3(L.grid), dim3(C::THREADS), C::ALLOC, L.stream, PAIR ? 2 : 1, L.tq, L.tk, L.tv,
+                    L.tsfk, L.tsfv, L.tp, L.p);
 }
 
 template <int KVT, bool PAIR>
@@ -89,11 +112,6 @@ cudaError_t launch_prefill(int kvt, int dqk, int dvo, const PrefillLaunch& L, co
   if (kvt == KV_FP8) return dispatch_prefill<KV_FP8, false>(dqk, dvo, L, variant);
   if (kvt == KV_NVFP4) return dispatch_prefill<KV_NVFP4, false>(dqk, dvo, L, variant);
   return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_prefill_plan(const PrefillParams& p, cudaStream_t s) {
-  prefill_plan_kernel<<<1, 1024, 0, s>>>(p);
-  return cudaGetLastError();
 }
 
 template <int KVT>

@@ -153,8 +153,8 @@ __device__ __forceinline__ void prefill_tile_range(const PrefillParams& p, int k
 
 #ifdef PA_PREFILL_PLAN
 // Per-sequence tile offsets (exclusive scan over ceil(qo_len / P)), then a cost histogram
-// and a scatter over all tiles in parallel.
-__global__ void __launch_bounds__(1024) prefill_plan_kernel(PrefillParams p) {
+// and a scatter over all tiles in parallel.  Run by one block of 1024 threads.
+__device__ __forceinline__ void prefill_plan_body(const PrefillParams& p) {
   __shared__ int hist[kPlanBuckets];
   __shared__ int s_red[32];
   __shared__ int s_carry;
@@ -484,6 +484,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
   else __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  grid_dep_wait();  // the planner (and the page conversion) of this call are complete
   const int n_items = min(p.hdr[0], p.max_items);
   const int ps = p.page_size, g = p.group;
   // head_dim_vo 512 (bf16 KV): the second pass reads P of the first from global scratch
@@ -661,7 +662,8 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
                              lead(&pslot_full[s]), pol_p);
           } else {
             mbar_arrive_expect_tx(&pslot_full[s], (uint32_t)C::CHUNK);
-            bulk_load_g2s(q_s + s * C::CHUNK, pscr + (size_t)j * C::CHUNK, (uint32_t)C::CHUNK, &pslot_full[s]);
+            bulk_load_g2s_hint(q_s + s * C::CHUNK, pscr + (size_t)j * C::CHUNK, (uint32_t)C::CHUNK, &pslot_full[s],
+                               pol_p);
           }
         }
         __syncwarp();
@@ -1073,6 +1075,9 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     int it_local = 0;
     uint8_t* pscr = p.p_scratch + (size_t)blockIdx.x * p.reuse_tiles * C::CHUNK;
     float* mscr = p.m_scratch + (size_t)blockIdx.x * p.reuse_tiles * 128;
+    // the first pass's P tiles are read back by the second pass of the same item: keep
+    // them in L2 ahead of streaming data; the second pass reads them with evict-first
+    const uint64_t pol_keep = l2_policy_evict_last();
     for (int r = 0;; ++r, ++it_local) {
       const int it = prefill_item_at<C::PAIR>(r);
       if (it >= n_items) break;
@@ -1229,7 +1234,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
               for (int k = 0; k < NCOL / 16; ++k) {
                 const uint32_t* a = pk + 8 * k + (odd ? 4 : 0);
                 const uint32_t* b = pk + 8 * k + (odd ? 0 : 4);
-                st_global_v8(prow + (k >> 2) * C::HALF + (((k & 3) ^ ((row & 7) >> 1)) << 5), a, b);
+                st_global_v8_hint(prow + (k >> 2) * C::HALF + (((k & 3) ^ ((row & 7) >> 1)) << 5), a, b, pol_keep);
               }
               mscr[jt * 128 + row] = resc ? alpha : 1.f;
             }

@@ -19,6 +19,7 @@ namespace {
 template <int DVO>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams p) {
   constexpr int G4 = DVO / 128;  // float4 groups per lane
+  grid_dep_wait();  // the prefill kernel's partial slots are complete
   const int n = p.hdr[1];
   const int g = p.group;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -68,10 +69,9 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams 
 
 cudaError_t launch_prefill_merge(int dvo, const PrefillParams& p, int grid, cudaStream_t s) {
   const dim3 g(grid, 16);
-  if (dvo == 512) prefill_merge_kernel<512><<<g, 256, 0, s>>>(p);
-  else if (dvo == 256) prefill_merge_kernel<256><<<g, 256, 0, s>>>(p);
-  else return cudaErrorInvalidValue;
-  return cudaGetLastError();
+  if (dvo == 512) return launch_pdl(prefill_merge_kernel<512>, g, dim3(256), 0, s, 1, p);
+  if (dvo == 256) return launch_pdl(prefill_merge_kernel<256>, g, dim3(256), 0, s, 1, p);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

@@ -85,6 +85,21 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
+// One 32-byte global store with an L2 cache policy: a[0..3] then b[0..3] (p 32-byte aligned).
+__device__ __forceinline__ void st_global_v8_hint(void* p, const uint32_t* a, const uint32_t* b, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p), "r"(a[0]), "r"(a[1]),
+               "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "l"(pol)
+               : "memory");
+}
+// One contiguous global -> shared bulk copy with an L2 cache policy (16-byte aligned, size
+// a multiple of 16), completing on `bar`.
+__device__ __forceinline__ void bulk_load_g2s_hint(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                   uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
 // One 32-byte global store: a[0..3] then b[0..3] (p 32-byte aligned).
 __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* a, const uint32_t* b) {
   asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a[0]), "r"(a[1]), "r"(a[2]),
