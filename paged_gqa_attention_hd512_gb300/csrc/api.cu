@@ -544,8 +544,10 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   if (!qo_indptr || total_q < 0) return PA_ERR_INVALID_ARG;
   if (!aligned(qo_indptr, 4)) return PA_ERR_ALIGNMENT;
   if (batch == 0 || total_q == 0) return PA_OK;
-  // K/V tiles are 128B-swizzled TMA boxes of page_size rows: they need whole 8-row atoms
-  if (page_size < 8) return PA_ERR_UNSUPPORTED;
+  // K/V tiles are 128B-swizzled TMA boxes of page_size rows, which need whole 8-row atoms:
+  // pages of 1, 2 or 4 tokens are read from a bf16 copy that pads each page to 8 rows
+  const bool pad = page_size < 8;
+  const int rows_copy = pad ? 8 : page_size;
   const int group = num_qo_heads / num_kv_heads;
   const int rows_per_tile = 128 / group;
   int smem_optin = 0;
@@ -554,13 +556,15 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   // FP8 / NVFP4: convert the referenced pages once into a bf16 copy and run the bf16
   // kernel on it, when the copy fits the limit; else convert inside the kernel
   const bool quant = kv_dtype != PA_KV_BF16;
-  const uint64_t bf16_page = (uint64_t)num_kv_heads * page_size * (head_dim_qk + head_dim_vo) * 2;
-  const bool dequant = quant && (uint64_t)num_pages * bf16_page <= g_prefill_dequant_limit.load();
+  const uint64_t bf16_page = (uint64_t)num_kv_heads * rows_copy * (head_dim_qk + head_dim_vo) * 2;
+  const bool dequant = (quant || pad) && (uint64_t)num_pages * bf16_page <= g_prefill_dequant_limit.load();
+  if (pad && !dequant) return PA_ERR_UNSUPPORTED;  // the padded copy would exceed the limit
   const int run_kvt = dequant ? (int)PA_KV_BF16 : kv_dtype;
   if (prefill_smem_bytes(run_kvt, head_dim_qk, head_dim_vo) > smem_optin) return PA_ERR_SMEM;
   // bf16 kernel (or the bf16 copy): CTA pairs share each MMA and each K/V tile
   int pair_grid = 0;
-  if (run_kvt == PA_KV_BF16 && g_prefill_pairs.load() == 1) pair_grid = 2 * std::min(sms / 2, pair_clusters(head_dim_qk, head_dim_vo));
+  if (run_kvt == PA_KV_BF16 && !pad && g_prefill_pairs.load() == 1)
+    pair_grid = 2 * std::min(sms / 2, pair_clusters(head_dim_qk, head_dim_vo));
 
   // split KV (short queries over long KV): when even one item per (query tile, kv head)
   // cannot fill the SMs, the planner may split KV ranges; up to 3 x sms items and slots
@@ -594,7 +598,7 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   const void* kv_read = dequant ? static_cast<const void*>(ws + o_shadow) : kv_cache;
   const bool packed = run_kvt != PA_KV_BF16;
   if (!make_kv_maps(&L.tk, &L.tv, &L.tsfk, &L.tsfv, kv_read, packed ? kv_scales->sf : nullptr, num_pages,
-                    num_kv_heads, head_dim_qk, head_dim_vo, page_size, run_kvt, page_size, !packed,
+                    num_kv_heads, head_dim_qk, head_dim_vo, rows_copy, run_kvt, rows_copy, !packed,
                     packed ? (run_kvt == KV_FP8 ? 64u : 32u) : 128u))
     return PA_ERR_CUDA;
   // Q as [total_q][Hq][d_qk] bf16 bytes: boxes of [rows_per_tile][group][128 B]
@@ -662,7 +666,8 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   p.merges = reinterpret_cast<PrefillMerge*>(ws + o_merge);
   p.max_slots = max_slots;
   p.max_items = (int)max_items;
-  p.box_rows = page_size;
+  p.box_rows = rows_copy;
+  p.tile_tok = 128 / rows_copy * page_size;
   p.swz = 7;
   p.sm_scale = sm_scale;
   L.grid = pair_grid > 0 ? pair_grid : sms;
@@ -672,15 +677,17 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   std::memset(&d, 0, sizeof d);
   if (dequant) {
     d.cache = static_cast<const uint8_t*>(kv_cache);
-    d.sf = kv_scales->sf;
+    d.sf = kv_scales ? kv_scales->sf : nullptr;
     d.kv_indptr = kv_indptr;
     d.kv_indices = kv_indices;
     d.shadow = reinterpret_cast<uint16_t*>(ws + o_shadow);
     d.batch = batch;
     d.Hkv = num_kv_heads;
     d.page_size = page_size;
+    d.out_rows = rows_copy;
   }
-  if (launch_prefill_prep(kv_dtype, head_dim_qk, head_dim_vo, dequant, p, d, sms, L.stream) != cudaSuccess)
+  if (launch_prefill_prep(kv_dtype, head_dim_qk, head_dim_vo, pad ? 2 : (dequant ? 1 : 0), p, d, sms, L.stream) !=
+      cudaSuccess)
     return PA_ERR_CUDA;
   const char* name = "?";
   prof_mark(L.stream, true);
@@ -689,8 +696,8 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   if (e != cudaSuccess) return PA_ERR_CUDA;
   if (split && launch_prefill_merge(head_dim_vo, p, sms, L.stream) != cudaSuccess) return PA_ERR_CUDA;
   static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};
-  std::snprintf(g_variant, sizeof g_variant, "%s_%s%s%s%s", name, kv_names[kv_dtype], dequant ? "_dequant" : "",
-                mask ? "_mask" : "", split ? "_splitkv" : "");
+  std::snprintf(g_variant, sizeof g_variant, "%s_%s%s%s%s", name, kv_names[kv_dtype],
+                pad ? "_padded" : (dequant ? "_dequant" : ""), mask ? "_mask" : "", split ? "_splitkv" : "");
   return PA_OK;
 }
 }  // namespace

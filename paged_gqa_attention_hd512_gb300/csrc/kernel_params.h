@@ -114,19 +114,26 @@ struct PrefillParams {
   const uint8_t* mask;
   const int64_t* mask_indptr;
   int max_items;
+  // rows one page occupies in the K/V tiles the kernel reads: page_size, or 8 for pages
+  // of 1, 2 or 4 tokens read from a copy that pads every page to 8 rows (rows past the
+  // page's tokens are zero); a 128-row KV tile then holds 128 / box_rows pages, i.e.
+  // tile_tok = 128 / box_rows * page_size tokens
   int box_rows;
+  int tile_tok;
   int swz;
   float sm_scale;
 };
 
-// FP8 / NVFP4 pages -> bf16 copy for the prefill (see prefill_dequant.cu)
+// Pages -> bf16 copy for the prefill (see prefill_dequant.cuh): FP8 / NVFP4 pages
+// converted, and pages of fewer than 8 tokens (any dtype) padded to 8 rows per kv head
 struct DequantParams {
-  const uint8_t* cache;  // packed pages
+  const uint8_t* cache;  // the caller's pages
   const uint8_t* sf;     // NVFP4 block-scale pool (same page indexing)
   const int32_t* kv_indptr;
   const int32_t* kv_indices;
   uint16_t* shadow;      // bf16 pages, same page index
   int batch, Hkv, page_size;
+  int out_rows;          // rows per kv head in a copy page: page_size, or 8 when padding
 };
 
 // New tokens' K / V (bf16) -> the paged cache, converted to the cache's element type

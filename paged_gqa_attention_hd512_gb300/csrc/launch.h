@@ -65,9 +65,10 @@ int decode_smem_bytes(int kvt, int dqk, int dvo, int hp);
 int decode_tile_tokens(int kvt, int dqk);
 
 cudaError_t launch_prefill(int kvt, int dqk, int dvo, const PrefillLaunch& L, const char** variant);
-// The prefill's planner (block 0) and, for FP8 / NVFP4 pages converted to a bf16 copy
-// (dequant true), the conversion (the other blocks), in one launch.
-cudaError_t launch_prefill_prep(int kvt, int dqk, int dvo, bool dequant, const PrefillParams& p,
+// The prefill's planner (block 0) and, when the kernel reads a bf16 copy of the pages,
+// the copy (the other blocks), in one launch.  copy: 0 none, 1 FP8 / NVFP4 pages
+// converted, 2 pages of fewer than 8 tokens padded to 8 rows (any dtype, converted).
+cudaError_t launch_prefill_prep(int kvt, int dqk, int dvo, int copy, const PrefillParams& p,
                                 const DequantParams& d, int sms, cudaStream_t s);
 // Split KV: merges the partial slots the plan listed (hdr[1] entries) into the output.
 cudaError_t launch_prefill_merge(int dvo, const PrefillParams& p, int grid, cudaStream_t s);

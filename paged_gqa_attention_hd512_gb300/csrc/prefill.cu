@@ -7,39 +7,43 @@
 
 namespace pa {
 
-// Block 0 plans the work items; blocks 1.. (FP8 / NVFP4 pages converted to a bf16 copy)
-// convert the pages.  The prefill kernel that follows is launched as its programmatic
-// dependent and waits for the whole grid before it reads either result.
-template <int KVT, int DQK, int DVO>
+// Block 0 plans the work items; blocks 1.. (COPY: FP8 / NVFP4 pages converted to a bf16
+// copy, or pages of fewer than 8 tokens padded in one) write the copy.  The prefill
+// kernel that follows is launched as its programmatic dependent and waits for the whole
+// grid before it reads either result.
+template <int KVT, int DQK, int DVO, bool COPY, bool PAD>
 __global__ void __launch_bounds__(1024) prefill_prep_kernel(const PrefillParams p, const DequantParams d) {
   grid_dep_launch();
   if (blockIdx.x == 0) {
     prefill_plan_body(p);
     return;
   }
-  if constexpr (KVT != KV_BF16) prefill_dequant_body<KVT, DQK, DVO>(d, blockIdx.x - 1, gridDim.x - 1);
+  if constexpr (COPY) prefill_dequant_body<KVT, DQK, DVO, PAD>(d, blockIdx.x - 1, gridDim.x - 1);
 }
 
-template <int KVT>
+template <int KVT, bool PAD>
 static cudaError_t run_prep(int dqk, int dvo, int grid, const PrefillParams& p, const DequantParams& d,
                             cudaStream_t s) {
-  if (dqk == 512 && dvo == 512) prefill_prep_kernel<KVT, 512, 512><<<grid, 1024, 0, s>>>(p, d);
-  else if (dqk == 512 && dvo == 256) prefill_prep_kernel<KVT, 512, 256><<<grid, 1024, 0, s>>>(p, d);
-  else if (dqk == 256 && dvo == 256) prefill_prep_kernel<KVT, 256, 256><<<grid, 1024, 0, s>>>(p, d);
+  if (dqk == 512 && dvo == 512) prefill_prep_kernel<KVT, 512, 512, true, PAD><<<grid, 1024, 0, s>>>(p, d);
+  else if (dqk == 512 && dvo == 256) prefill_prep_kernel<KVT, 512, 256, true, PAD><<<grid, 1024, 0, s>>>(p, d);
+  else if (dqk == 256 && dvo == 256) prefill_prep_kernel<KVT, 256, 256, true, PAD><<<grid, 1024, 0, s>>>(p, d);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
 
-cudaError_t launch_prefill_prep(int kvt, int dqk, int dvo, bool dequant, const PrefillParams& p,
+cudaError_t launch_prefill_prep(int kvt, int dqk, int dvo, int copy, const PrefillParams& p,
                                 const DequantParams& d, int sms, cudaStream_t s) {
-  if (!dequant) {
-    prefill_prep_kernel<KV_BF16, 512, 512><<<1, 1024, 0, s>>>(p, d);
+  if (copy == 0) {
+    prefill_prep_kernel<KV_BF16, 512, 512, false, false><<<1, 1024, 0, s>>>(p, d);
     return cudaGetLastError();
   }
-  // two 1024-thread blocks per SM convert, all resident at once
+  // two 1024-thread blocks per SM write the copy, all resident at once
   const int grid = 1 + 2 * sms;
-  if (kvt == KV_FP8) return run_prep<KV_FP8>(dqk, dvo, grid, p, d, s);
-  if (kvt == KV_NVFP4) return run_prep<KV_NVFP4>(dqk, dvo, grid, p, d, s);
+  const bool pad = copy == 2;
+  if (kvt == KV_BF16) return pad ? run_prep<KV_BF16, true>(dqk, dvo, grid, p, d, s) : cudaErrorInvalidValue;
+  if (kvt == KV_FP8) return pad ? run_prep<KV_FP8, true>(dqk, dvo, grid, p, d, s) : run_prep<KV_FP8, false>(dqk, dvo, grid, p, d, s);
+  if (kvt == KV_NVFP4)
+    return pad ? run_prep<KV_NVFP4, true>(dqk, dvo, grid, p, d, s) : run_prep<KV_NVFP4, false>(dqk, dvo, grid, p, d, s);
   return cudaErrorInvalidValue;
 }
 

@@ -134,7 +134,7 @@ __device__ __forceinline__ int prefill_tile_cost(const PrefillParams& p, int kv_
   const int hi = p.causal ? min(kv_len - 1, pos0 + n_pos - 1) : kv_len - 1;
   const int lo = p.window_left >= 0 ? max(0, pos0 - p.window_left) : 0;
   if (hi < lo || hi < 0) return 0;
-  return hi / 128 - lo / 128 + 1;
+  return hi / p.tile_tok - lo / p.tile_tok + 1;
 }
 
 // First KV tile and number of KV tiles of the item starting at new-token q_begin (the
@@ -147,8 +147,8 @@ __device__ __forceinline__ void prefill_tile_range(const PrefillParams& p, int k
   int lo = p.window_left >= 0 ? max(0, pos0 - p.window_left) : 0;
   hi = max(hi, 0);
   lo = min(lo, hi);
-  jlo = lo / 128;
-  nt = hi / 128 - jlo + 1;
+  jlo = lo / p.tile_tok;
+  nt = hi / p.tile_tok - jlo + 1;
 }
 
 #ifdef PA_PREFILL_PLAN
@@ -351,8 +351,8 @@ __device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams
   int lo = p.window_left >= 0 ? max(0, ipos0 - p.window_left) : 0;
   hi = max(hi, 0);  // at least one tile: rows without a visible key come out as 0 / -inf
   lo = min(lo, hi);
-  f.jlo = lo / 128;
-  f.nt = hi / 128 - f.jlo + 1;
+  f.jlo = lo / p.tile_tok;
+  f.nt = hi / p.tile_tok - f.jlo + 1;
   f.slot = item.slot;
   if (item.kv_t1 > item.kv_t0) {  // split KV: one chunk of the range
     const int t0 = max(f.jlo, item.kv_t0), t1 = min(f.jlo + f.nt, item.kv_t1);
@@ -523,26 +523,30 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       }
       // steps that compute S: both passes, or only the first when the second reuses P
       const int steps = reuse ? f.nt : C::NPASS * f.nt;
-      const int page_tok_cap = f.np * ps;
+      // a KV tile is ppt pages of rpp rows each (rpp = page_size, or 8 for the padded copy
+      // of smaller pages: then only the first page_size rows of a page are tokens)
+      const int rpp = p.box_rows, ppt = 128 / rpp;
       // page ids of a step's KV tile, one per lane (lane < pieces); loaded a few steps
       // ahead so the producer never waits on them
       auto step_pages = [&](int st) -> int {
         if (st < 0 || st >= C::NPASS * f.nt) return 0;
-        const int key0 = (f.jlo + st % f.nt) * 128;
-        const int pieces = max(0, min(128, page_tok_cap - key0)) / ps;
-        return (lane < pieces) ? __ldg(p.kv_indices + f.ip0 + key0 / ps + lane) : 0;
+        const int pg0 = (f.jlo + st % f.nt) * ppt;
+        const int pieces = max(0, min(ppt, f.np - pg0));
+        return (lane < pieces) ? __ldg(p.kv_indices + f.ip0 + pg0 + lane) : 0;
       };
       // the K or V chunks of step st into the ring
       auto emit = [&](bool is_k, int st, int my_page) {
         const int pass = st / f.nt, jt = st % f.nt;
-        const int key0 = (f.jlo + jt) * 128;
-        const int valid = max(0, min(128, f.kv_len - key0));
+        // tile rows before the first that holds no token of the sequence
+        const int rem = max(0, f.kv_len - (f.jlo + jt) * p.tile_tok);
+        const int valid = min(128, rem / ps * rpp + rem % ps);
         if constexpr (C::PAIR) {
           if (is_k) {
             // this CTA's 64 keys of the tile (B rows of its half of N), in chunks of 256
             // dims: four [64 keys][64 dims] blocks per page piece
-            const int h0 = key0 + 64 * (int)rank;
-            const int pieces = max(0, min(64, page_tok_cap - h0)) / ps;
+            // (pairs read the caller's pages: a tile is 128 tokens)
+            const int h0 = (f.jlo + jt) * 128 + 64 * (int)rank;
+            const int pieces = max(0, min(64, f.np * ps - h0)) / ps;
             const int pg0 = 64 * (int)rank / ps;
             for (int c = 0; c < C::NKC; ++c, ++rc) {
               const int slot = rc % NSLOT;
@@ -561,14 +565,13 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
             return;
           }
         }
-        const int load_rows = max(0, min(128, page_tok_cap - key0));
-        const int pieces = load_rows / ps;
+        const int pieces = max(0, min(ppt, f.np - (f.jlo + jt) * ppt));
         const int nch = is_k ? C::NQC : C::NVS_P;
         for (int c = 0; c < nch; ++c, ++rc) {
           const int slot = rc % NSLOT;
           mbar_wait<C::PAIR>(&kv_empty[slot], ((rc / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
           const uint32_t dst = ring + slot * C::CHUNK;
-          const uint32_t bytes = (uint32_t)(2 * pieces * ps * 128);
+          const uint32_t bytes = (uint32_t)(2 * pieces * rpp * 128);
           const bool fix = !is_k && valid < 128;  // V rows past the sequence must be zeroed
           // pairs: the chunk completes on the first CTA's barrier (the zeroing path on this
           // CTA's aux first)
@@ -587,11 +590,11 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
             if (lane == 0)
               for (int h = 0; h < 2; ++h) {
                 if (remote)
-                  tma_load_3d_pair(dst + h * C::HALF + pc * ps * 128, &tm_v, col + h * 128, f.kvh * ps, page, fb,
+                  tma_load_3d_pair(dst + h * C::HALF + pc * rpp * 128, &tm_v, col + h * 128, f.kvh * rpp, page, fb,
                                    pol_kv);
                 else
-                  tma_load_3d_hint(dst + h * C::HALF + pc * ps * 128, is_k ? &tm_k : &tm_v, col + h * 128,
-                                   f.kvh * ps, page, bar, pol_kv);
+                  tma_load_3d_hint(dst + h * C::HALF + pc * rpp * 128, is_k ? &tm_k : &tm_v, col + h * 128,
+                                   f.kvh * rpp, page, bar, pol_kv);
               }
           }
           if (fix) {
@@ -1138,6 +1141,11 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
 #pragma unroll
               for (int i = 0; i < NCOL; ++i) sr[i] = __float_as_uint(__uint_as_float(sr[i]) * scale_log2);
             }
+            // pages of fewer than 8 tokens, read from their copy padded to 8 rows: column i
+            // of this thread is token tok0 + (i / 8) * page_size + i % 8 when i % 8 <
+            // page_size and padding otherwise (at most 8 * 4 tokens per thread)
+            const bool padded = p.box_rows != ps;
+            const int tok0 = padded ? (f.jlo + jt) * p.tile_tok + (col0 >> 3) * ps : 0;
             // the row maximum over the visible keys of this thread's columns, masked scores
             // set to -inf; a tile every row of the warp sees in full skips the mask
             auto mask_and_max = [&](const uint32_t* mw, bool use_mw) {
@@ -1153,7 +1161,19 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
 #pragma unroll
               for (int i = 0; i < NCOL; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], __uint_as_float(sr[i]));
             };
-            if (p.mask == nullptr) {
+            if (padded) {
+              const int thi = min(khi, f.kv_len - 1) - tok0, tlo = klo - tok0;
+              uint64_t mb = ~0ull;  // custom-mask bits of tokens tok0 .. tok0 + 63 of this row
+              if (p.mask != nullptr && row_ok) mb = load_mask_bits(p.mask, mbase + tok0, min(64, f.kv_len - tok0));
+#pragma unroll
+              for (int i = 0; i < NCOL; ++i) {
+                const int r = i & 7, t = (i >> 3) * ps + r;
+                const bool ok = (r < ps) & (t >= tlo) & (t <= thi) & (((mb >> (t & 63)) & 1ull) != 0ull);
+                const float x = ok ? __uint_as_float(sr[i]) : -INFINITY;
+                sr[i] = __float_as_uint(x);
+                mx4[i & 3] = fmaxf(mx4[i & 3], x);
+              }
+            } else if (p.mask == nullptr) {
               if (__all_sync(0xffffffffu, (lo <= 0) & (hi >= NCOL - 1))) plain_max();
               else mask_and_max(nullptr, false);
             } else {

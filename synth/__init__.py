@@ -429,6 +429,11 @@ WORKLOADS = {
     "prefill_extend_bf16": dict(
         phase="prefill", batch=4, Hq=24, Hkv=4, d_qk=512, d_vo=512, page_size=64,
         kv_lens=[16384] * 4, qo_lens=[32] * 4, kv_dtype=KV_BF16, seed=1006),
+    # the first 32 sequences of the sliding-window decode (4.3 GB of cache, 0.54 GB of it
+    # in the windows, above L2): profiling captures
+    "sliding_decode_d256_small": dict(
+        phase="decode", batch=32, Hq=32, Hkv=16, d_qk=256, d_vo=256, page_size=16,
+        kv_lens=[8192] * 32, kv_dtype=KV_BF16, window_left=1023, seed=1005),
     "sliding_decode_d256": dict(
         phase="decode", batch=256, Hq=32, Hkv=16, d_qk=256, d_vo=256, page_size=16,
         kv_lens=[8192] * 256, kv_dtype=KV_BF16, window_left=1023, seed=1005),

@@ -103,8 +103,46 @@ def test_prefill_pairs_on_the_dequantised_copy(cta_mode, _dequant_limit):
     assert _variant() == f"prefill_512x256{cta_mode}_nvfp4_dequant"
 
 
-def test_prefill_small_pages_are_refused():  # noqa: D103
+SMALL_PAGE_CASES = [
+    # (dtype, dqk, dvo, Hq, Hkv, page_size, kv_lens, qo_lens, causal, window)
+    (BF16, 512, 512, 8, 2, 1, [130, 33], [130, 33], 1, -1),
+    (BF16, 512, 512, 24, 4, 2, [300, 129, 1], [300, 129, 1], 1, -1),
+    (BF16, 512, 256, 16, 2, 4, [260, 64], [200, 64], 1, 63),
+    (BF16, 256, 256, 8, 8, 4, [190, 17], [190, 17], 0, -1),
+    (BF16, 512, 512, 8, 2, 2, [700, 333], [260, 333], 1, -1),
+    (synth.KV_FP8, 512, 512, 12, 4, 2, [150, 40], [150, 40], 1, -1),
+    (synth.KV_NVFP4, 512, 256, 16, 2, 4, [300, 100], [300, 100], 1, -1),
+    (synth.KV_NVFP4, 512, 512, 8, 1, 1, [70], [70], 1, 20),
+]
+
+
+def _sid(c):
+    return {BF16: "bf16", synth.KV_FP8: "fp8", synth.KV_NVFP4: "nvfp4"}[c[0]] + "-" + _id(c[1:])
+
+
+@pytest.mark.parametrize("split", [True, False])
+@pytest.mark.parametrize("c", SMALL_PAGE_CASES, ids=[_sid(c) for c in SMALL_PAGE_CASES])
+def test_prefill_small_pages(c, split):
+    """Pages of 1, 2 and 4 tokens: the prefill reads a bf16 copy that pads each page to
+    8 rows per kv head (the padding is masked); every KV dtype, windows, a cached prefix,
+    non-causal rows, with and without split KV."""
     ensure_built()
+    pa.paged_attn_set_prefill_split_kv(-1 if split else 0)
+    try:
+        dt, dqk, dvo, hq, hkv, ps, kv, qo, causal, win = c
+        case = synth.make_case("prefill", batch=len(kv), Hq=hq, Hkv=hkv, d_qk=dqk, d_vo=dvo, page_size=ps,
+                               kv_lens=kv, qo_lens=qo, kv_dtype=dt, causal=causal, window_left=win,
+                               seed=640 + ps + len(kv))
+        check_full(case, _sid(c))
+        names = {BF16: "bf16", synth.KV_FP8: "fp8", synth.KV_NVFP4: "nvfp4"}
+        assert _variant() == f"prefill_{dqk}x{dvo}_{names[dt]}_padded"
+    finally:
+        pa.paged_attn_set_prefill_split_kv(-1)
+
+
+def test_prefill_small_pages_beyond_the_copy_limit_are_refused(_dequant_limit):  # noqa: D103
+    ensure_built()
+    pa.paged_attn_set_prefill_dequant_limit(0)
     case = synth.make_case("prefill", batch=1, Hq=8, Hkv=1, d_qk=512, d_vo=512, page_size=4,
                            kv_lens=[20], qo_lens=[20], seed=9).to("cuda")
     with pytest.raises(pa.PagedAttnError) as e:

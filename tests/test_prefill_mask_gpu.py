@@ -19,6 +19,10 @@ CASES = [
     ("spans", synth.KV_BF16, 256, 256, 12, 4, 8, [150, 40], [150, 40], 0, -1),
     ("random", synth.KV_FP8, 512, 512, 8, 2, 16, [200, 77], [200, 77], 0, -1),
     ("spans", synth.KV_NVFP4, 512, 256, 16, 2, 32, [256, 100], [256, 100], 1, -1),
+    # pages of fewer than 8 tokens (read from the padded copy)
+    ("random", synth.KV_BF16, 512, 512, 8, 2, 2, [300, 130], [300, 70], 0, -1),
+    ("spans", synth.KV_NVFP4, 512, 256, 16, 2, 4, [256, 100], [256, 100], 1, -1),
+    ("sparse_rows", synth.KV_BF16, 256, 256, 12, 4, 1, [150, 40], [150, 40], 0, 30),
 ]
 
 
