@@ -136,12 +136,15 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
  * bf16; lse [total_q, num_qo_heads] fp32 or NULL.  QK^T and PV run as tcgen05 MMAs with
  * TMEM accumulators; for head_dim_vo = 512 the VO dimension is processed in two halves
  * (the second reuses the first's softmax probabilities from a workspace scratch).
- * Shapes and dtypes as for decode; group size up to 16; page_size >= 8 (smaller pages
- * return PA_ERR_UNSUPPORTED).  FP8 / NVFP4 KV: the pages kv_indices references are first
- * converted to a bf16 copy in the library workspace (num_pages * num_kv_heads *
- * page_size * (head_dim_qk + head_dim_vo) * 2 bytes) when that fits the limit set by
- * paged_attn_set_prefill_dequant_limit (default 4 GiB), else converted inside the
- * kernel on every read; both give the same values (the conversions are exact).  When the
+ * Shapes and dtypes as for decode; group size up to 16.  FP8 / NVFP4 KV: the pages
+ * kv_indices references are first converted to a bf16 copy in the library workspace
+ * (num_pages * num_kv_heads * page_size * (head_dim_qk + head_dim_vo) * 2 bytes) when
+ * that fits the limit set by paged_attn_set_prefill_dequant_limit (default 4 GiB), else
+ * converted inside the kernel on every read; both give the same values (the conversions
+ * are exact).  Page sizes 1, 2 and 4 (any dtype): the pages are read from a bf16 copy
+ * that pads each page to 8 rows per kv head (num_pages * num_kv_heads * 8 *
+ * (head_dim_qk + head_dim_vo) * 2 bytes), under the same limit; beyond it the call
+ * returns PA_ERR_UNSUPPORTED.  When the
  * (query tile, kv head) items are fewer than the SMs (a few new tokens over a long
  * prefix), the device planner may split long KV ranges into chunks whose fp32 partials a
  * merge kernel combines (paged_attn_set_prefill_split_kv); the workspace then also holds
