@@ -154,19 +154,35 @@ __device__ __forceinline__ void prefill_tile_range(const PrefillParams& p, int k
 #ifdef PA_PREFILL_PLAN
 // Per-sequence tile offsets (exclusive scan over ceil(qo_len / P)), then a cost histogram
 // and a scatter over all tiles in parallel.  Run by one block of 1024 threads.
+// Batches of up to kPlanCache sequences keep their tile offsets and lengths in shared
+// memory, so the per-tile lookups below are shared-memory reads, not chains of dependent
+// global loads.
+constexpr int kPlanCache = 2048;
+
 __device__ __forceinline__ void prefill_plan_body(const PrefillParams& p) {
   __shared__ int hist[kPlanBuckets];
   __shared__ int s_red[32];
   __shared__ int s_carry;
+  __shared__ int c_off[kPlanCache + 1], c_qo[kPlanCache], c_kv[kPlanCache];
   const int tid = threadIdx.x;
   for (int i = tid; i < kPlanBuckets; i += blockDim.x) hist[i] = 0;
   if (tid == 0) s_carry = 0;
   __syncthreads();
   const int P = p.rows_per_tile * (p.pair ? 2 : 1), ps = p.page_size;  // positions per item
-  int* off = p.tile_off;  // [batch + 1]
+  const bool cached = p.batch <= kPlanCache;
+  int* off = cached ? c_off : p.tile_off;  // [batch + 1]
   for (int base = 0; base < p.batch; base += blockDim.x) {
     const int b = base + tid;
-    const int n = b < p.batch ? (p.qo_indptr[b + 1] - p.qo_indptr[b] + P - 1) / P : 0;
+    int qo_len = 0;
+    if (b < p.batch) {
+      qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
+      if (cached) {
+        const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
+        c_qo[b] = qo_len;
+        c_kv[b] = np > 0 ? (np - 1) * ps + p.kv_last_page_len[b] : 0;
+      }
+    }
+    const int n = (qo_len + P - 1) / P;
     int v = n;
     for (int o = 1; o < 32; o <<= 1) {
       const int t = __shfl_up_sync(0xffffffffu, v, o);
@@ -200,9 +216,15 @@ __device__ __forceinline__ void prefill_plan_body(const PrefillParams& p) {
     }
     b = lo;
     q0 = (t - off[b]) * P;
-    const int qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
-    const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
-    const int kv_len = np > 0 ? (np - 1) * ps + p.kv_last_page_len[b] : 0;
+    int qo_len, kv_len;
+    if (cached) {
+      qo_len = c_qo[b];
+      kv_len = c_kv[b];
+    } else {
+      qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
+      const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
+      kv_len = np > 0 ? (np - 1) * ps + p.kv_last_page_len[b] : 0;
+    }
     cost = prefill_tile_cost(p, kv_len, qo_len, q0);
   };
   // split KV: fewer tiles x kv heads than split_target (short queries over long KV).  The
@@ -223,9 +245,15 @@ __device__ __forceinline__ void prefill_plan_body(const PrefillParams& p) {
       for (int t = 0; t < n_tiles; ++t) {
         int b, q0, cost;
         tile_of(t, b, q0, cost);
-        const int qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
-        const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
-        const int kv_len = np > 0 ? (np - 1) * p.page_size + p.kv_last_page_len[b] : 0;
+        int qo_len, kv_len;
+        if (cached) {
+          qo_len = c_qo[b];
+          kv_len = c_kv[b];
+        } else {
+          qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
+          const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
+          kv_len = np > 0 ? (np - 1) * p.page_size + p.kv_last_page_len[b] : 0;
+        }
         int jlo, nt;
         prefill_tile_range(p, kv_len, qo_len, q0, jlo, nt);
         int parts = max(1, (nt + chunk - 1) / chunk);
