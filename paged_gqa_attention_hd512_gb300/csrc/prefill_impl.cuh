@@ -644,16 +644,15 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
           }
         }
       };
+      // chunks in the MMA thread's order: K of step 0, then per step k: K of k + 1, V of k
       int pg_a = step_pages(0), pg_b = step_pages(1);
-      // chunks in the MMA thread's order: steps in pairs, K of both, then V of both
-      for (int k = 0; k < steps; k += 2) {
-        const int pg_c = step_pages(k + 2), pg_d = step_pages(k + 3);
-        for (int part = 0; part < 4; ++part) {
-          const int st = k + (part & 1);
-          if (st < steps) emit(part < 2, st, (part & 1) ? pg_b : pg_a);
-        }
-        pg_a = pg_c;
-        pg_b = pg_d;
+      emit(true, 0, pg_a);
+      for (int k = 0; k < steps; ++k) {
+        const int pg_c = step_pages(k + 2);
+        if (k + 1 < steps) emit(true, k + 1, pg_b);
+        emit(false, k, pg_a);
+        pg_a = pg_b;
+        pg_b = pg_c;
       }
       if (reuse) {
         // second pass: V of the upper output half (the P tiles come from warp 3)
@@ -738,18 +737,19 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
           const int pieces = max(0, min(128, page_tok_cap - key0)) / ps;
           return (lane < pieces) ? __ldg(p.kv_indices + f.ip0 + key0 / ps + lane) : 0;
         };
-        int pg_a = step_pages(0), pg_b = step_pages(1);
-        for (int k = 0; k < steps; k += 2) {
-          const int pg_c = step_pages(k + 2), pg_d = step_pages(k + 3);
-          for (int part = 0; part < 4; ++part) {
-            const bool is_k = part < 2;
-            const int st = k + (part & 1);
-            if (st >= steps) continue;
+        // per iteration k: K of step k + 1 (pages pg_b), V of step k (pages pg_a)
+        int pg_a = 0, pg_b = step_pages(0);
+        for (int k = -1; k < steps; ++k) {
+          const int pg_c = step_pages(k + 2);
+          for (int part = 0; part < 2; ++part) {
+            const bool is_k = part == 0;
+            const int st = is_k ? k + 1 : k;
+            if (st < 0 || st >= steps) continue;
             const int pass = st / f.nt, jt = st % f.nt;
             const int key0 = (f.jlo + jt) * 128;
             const int valid = max(0, min(128, f.kv_len - key0));
             const int pieces = max(0, min(128, page_tok_cap - key0)) / ps;
-            const int my_page = (part & 1) ? pg_b : pg_a;
+            const int my_page = is_k ? pg_b : pg_a;
             if constexpr (KVT == KV_NVFP4) {
               const int sw = is_k ? C::SFW_K : C::SFW_V;
               const int si = nsf % C::NSF;
@@ -783,8 +783,8 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
               }
             }
           }
-          pg_a = pg_c;
-          pg_b = pg_d;
+          pg_a = pg_b;
+          pg_b = pg_c;
         }
       }
       // end marker
@@ -990,9 +990,9 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     // follow one another without the softmax, except where the first pass rescaled O
     // before tile j: then the MMAs so far are committed to o_ready, and the PV waits until
     // the softmax warps have applied the same factor (resc_done).
-    auto issue_pv_reuse = [&](int j, int last, int tag) {
+    auto issue_pv_reuse = [&](int j, int last, uint64_t rmask) {
       if (j == 0) point(C::NB_OFREE, o_free, (n_pass - 1) & 1, SITE_PRE_O_DONE);
-      if (rtag[j] == tag) {
+      if ((rmask >> j) & 1) {
         if (leader) commit_both(o_ready);
         point(C::NB_OFREE, resc_done, n_rs & 1, SITE_PRE_P_FULL);
         ++n_rs;
@@ -1007,9 +1007,10 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
           tc_fence_after();
           if (leader) {
             const uint32_t bsm = ring + slot * C::CHUNK, psm = q_s + s * C::CHUNK;
+            // P: K-major without swizzle, key group g8 (8 keys) of every row at g8 x 2048
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tbase + C::TM_O + c * 128, desc_kmajor_sw128(psm + (kk >> 2) * C::HALF + (kk & 3) * 32),
+              mma_ss(tbase + C::TM_O + c * 128, desc_kmajor_plain(psm + kk * 2 * 2048, 2048, 128),
                      desc_mnmajor_sw128(bsm + kk * 2048, C::HALF), ID_PV, (j > 0) || kk > 0);
             commit_both(&kv_empty[slot]);
           }
@@ -1031,19 +1032,26 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       point(C::NB_Q, q_full, it_local & 1, SITE_PRE_Q);
       // the S of the second step of a pair is computed while the softmax of the first
       // runs, and the PVs of the pair while the softmax of the second finishes
-      for (int k = 0; k < steps; k += 2) {
-        const bool two = k + 1 < steps;
-        issue_qk();
-        if (two) issue_qk();
-        if (leader && k + (two ? 1 : 0) == steps - 1) {  // the item's last QK
-          commit_both(q_empty);
-          if (reuse) commit_both(qreg_free);
+      for (int k = -1; k < steps; ++k) {
+        if (k + 1 < steps) {
+          issue_qk();
+          if (leader && k + 1 == steps - 1) {  // the item's last QK
+            commit_both(q_empty);
+            if (reuse) commit_both(qreg_free);
+          }
         }
-        issue_pv(k % f.nt == 0, (k + 1) % f.nt == 0);
-        if (two) issue_pv((k + 1) % f.nt == 0, (k + 2) % f.nt == 0);
+        if (k >= 0) issue_pv(k % f.nt == 0, (k + 1) % f.nt == 0);
       }
       if (reuse) {
-        for (int j = 0; j < f.nt; ++j) issue_pv_reuse(j, f.nt - 1, it_local + 1);
+        // the tiles the first pass tagged, read once per item into a mask (a shared-memory
+        // read in the issuing warp waits behind the MMAs' operand reads); every first-pass
+        // tag of the item is visible here, after the gate's p_full waits of the whole pass
+        static_assert(C::MAX_RT <= 64, "rescale tags");
+        const int tag = it_local + 1;
+        const uint64_t rmask = (uint64_t)__ballot_sync(0xffffffffu, lane < C::MAX_RT && rtag[lane] == tag) |
+                               ((uint64_t)__ballot_sync(0xffffffffu, lane + 32 < C::MAX_RT && rtag[lane + 32] == tag)
+                                << 32);
+        for (int j = 0; j < f.nt; ++j) issue_pv_reuse(j, f.nt - 1, rmask);
         if (leader) commit_both(q_empty);  // the P slots (Q region) are free
       }
     }
@@ -1271,19 +1279,15 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
             __syncwarp();
             if (lane == 0) arrive_lead(&p_full[sstep & 1]);
             if (reuse) {
-              // after the PV may start: this thread's keys of P tile jt in the shared-memory
-              // image the second pass's MMAs read (128B-swizzled blocks of 64 keys), and the
-              // rescale factor applied before it
-              // 32-byte stores: logical pieces 2k and 2k+1 of a row land in one aligned pair of
-              // physical 16-byte slots, swapped when the row's swizzle phase is odd
-              uint8_t* prow = pscr + (size_t)jt * C::CHUNK + (col0 / 64) * C::HALF + row * 128;
-              const bool odd = row & 1;
+              // after the PV may start: this thread's keys of P tile jt and the rescale
+              // factor applied before it.  The tile is the second pass's MMA operand image
+              // without swizzle, [16 groups of 8 keys][128 rows][16 B] (8 x 16-byte core
+              // matrices, rows 16 bytes apart), so each store instruction of a warp writes
+              // one key group of 32 consecutive rows: 512 contiguous bytes.
+              uint8_t* prow = pscr + (size_t)jt * C::CHUNK + row * 16;
 #pragma unroll
-              for (int k = 0; k < NCOL / 16; ++k) {
-                const uint32_t* a = pk + 8 * k + (odd ? 4 : 0);
-                const uint32_t* b = pk + 8 * k + (odd ? 0 : 4);
-                st_global_v8_hint(prow + (k >> 2) * C::HALF + (((k & 3) ^ ((row & 7) >> 1)) << 5), a, b, pol_keep);
-              }
+              for (int k = 0; k < NCOL / 8; ++k)
+                st_global_v4_hint(prow + (size_t)(col0 / 8 + k) * (128 * 16), pk + 4 * k, pol_keep);
               mscr[jt * 128 + row] = resc ? alpha : 1.f;
             }
           }

@@ -6,10 +6,13 @@
 //   bits 16-29  leading-dimension byte offset >> 4
 //   bits 32-45  stride-dimension byte offset >> 4
 //   bits 46-47  descriptor version (1)
-//   bits 61-63  layout (2 = 128-byte swizzle)
+//   bits 61-63  layout (0 = no swizzle, 2 = 128-byte swizzle)
 // K-major 128B-swizzled operand: rows of 128 bytes (64 bf16 along K), 8-row atoms of 1024
 // bytes; stride-dimension offset = 1024 (next 8 rows); the leading offset is unused.  A
 // k-step of 16 elements inside the atom advances the start address by 32 bytes.
+// K-major operand without swizzle: 8 x 16-byte core matrices (8 rows, 8 bf16 along K, 128
+// contiguous bytes); leading-dimension offset = the byte distance to the next core matrix
+// along K, stride-dimension offset = to the next 8 rows.
 // MN-major 128B-swizzled operand (V as the B of PV): rows are K (keys), 128 bytes hold 64
 // N-elements; stride-dimension offset = 1024 (next 8 keys), leading offset = the byte
 // distance to the next 64-wide N block.
@@ -26,6 +29,10 @@ namespace pa {
 __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
   return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)64 << 32) | ((uint64_t)1 << 46) |
          ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ uint64_t desc_kmajor_plain(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo_bytes >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46);
 }
 __device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t saddr, uint32_t lbo_bytes) {
   return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFF) << 16) |
@@ -84,6 +91,12 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
+}
+// One 16-byte global store with an L2 cache policy (p 16-byte aligned).
+__device__ __forceinline__ void st_global_v4_hint(void* p, const uint32_t* a, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(a[0]), "r"(a[1]), "r"(a[2]),
+               "r"(a[3]), "l"(pol)
+               : "memory");
 }
 // One 32-byte global store with an L2 cache policy: a[0..3] then b[0..3] (p 32-byte aligned).
 __device__ __forceinline__ void st_global_v8_hint(void* p, const uint32_t* a, const uint32_t* b, uint64_t pol) {
