@@ -62,6 +62,11 @@ struct PrefillCfg {
   static constexpr int Q_BYTES = NQB * HALF;
   static constexpr int SMEM_BUDGET = 232448 - 1024 - 512;
   static constexpr bool QUANT = KVT != KV_BF16;
+  // bf16 KV, one CTA per tile: a V chunk is 64 keys of the tile by the pass's 256 output
+  // columns (four [64 keys][64 dims] 128B-swizzled blocks of 8 KB), so that P.V runs as
+  // N = 256 MMAs (one per 16 keys, four per chunk): on this GPU an N = 128 MMA takes about
+  // 90 cycles and an N = 256 one about 130, against 64 and 128 of arithmetic
+  static constexpr bool VKEYS = !PAIR && !QUANT && DVP == 256;
   // warps 8-11: converters for quantised KV (one key row per thread); for bf16 KV a second
   // softmax warpgroup, so each softmax thread handles half of its row's 128 keys
   static constexpr int THREADS = 384;
@@ -594,6 +599,41 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
           }
         }
         const int pieces = max(0, min(ppt, f.np - (f.jlo + jt) * ppt));
+        if (C::VKEYS && !is_k) {
+          // V by keys: chunk c = tile rows [64 c, 64 c + 64), all of the pass's 256 columns
+          for (int c = 0; c < 2; ++c, ++rc) {
+            const int slot = rc % NSLOT;
+            mbar_wait(&kv_empty[slot], ((rc / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
+            const uint32_t dst = ring + slot * C::CHUNK;
+            const int pc0 = 64 * c / rpp, pc1 = min(pieces, (64 * c + 64) / rpp);
+            const int vrows = min(64, max(0, valid - 64 * c));  // rows that hold tokens
+            const bool fix = vrows < 64;  // V rows past the sequence must be zeroed
+            uint64_t* bar = fix ? aux : &kv_full[slot];
+            if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(4 * max(0, pc1 - pc0) * rpp * 128));
+            for (int pc = pc0; pc < pc1; ++pc) {
+              const int page = __shfl_sync(0xffffffffu, my_page, pc);
+              if (lane == 0)
+                for (int b = 0; b < 4; ++b)
+                  tma_load_3d_hint(dst + b * C::KBLK + (pc - pc0) * rpp * 128, &tm_v, (pass * C::DVP + b * 64) * 2,
+                                   f.kvh * rpp, page, bar, pol_kv);
+            }
+            if (fix) {
+              mbar_wait(aux, aux_phase, p.err, SITE_PRE_DEQ);
+              aux_phase ^= 1;
+              uint8_t* sp = smem + C::OFF_RING + slot * C::CHUNK;
+              const int nz = (64 - vrows) * 8;  // 16-byte pieces per block
+              for (int i = lane; i < 4 * nz; i += 32) {
+                const int b = i / nz, k = i - b * nz;
+                *reinterpret_cast<uint4*>(sp + b * C::KBLK + (vrows + (k >> 3)) * 128 + (k & 7) * 16) =
+                    make_uint4(0, 0, 0, 0);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&kv_full[slot]);
+            }
+          }
+          return;
+        }
         const int nch = is_k ? C::NQC : C::NVS_P;
         for (int c = 0; c < nch; ++c, ++rc) {
           const int slot = rc % NSLOT;
@@ -887,6 +927,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     // quantised KV: P and V in f16.  Pairs: one N = 256 MMA per 16 keys covers the pass's
     // output columns (128 from each CTA's V chunk)
     constexpr uint32_t ID_PV = idesc_f16<!C::QUANT>(128 * C::CL, 128 * C::CL, true);
+    constexpr uint32_t ID_PV2 = idesc_f16<true>(128, 256, true);  // V by keys
     // MMA issue and commits: the pair forms (cta_group::2) in a CTA pair.  commit_both
     // signals the barrier in both CTAs, commit_here only in this (the first) CTA.
     auto mma_ss = [&](uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
@@ -915,10 +956,11 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     // n_spv & 1) and passes finished.  QK of step j + 2 reuses the buffer of step j, where
     // PV of step j reads P: it waits for that PV to complete (an MMA that reads its A
     // operand from TMEM is not ordered against a later MMA writing the same columns).
-    // Steps are issued in pairs, QK QK PV PV, so that another MMA group is always queued
-    // behind the PV being waited for and the pipe never drains.  One mbarrier per buffer:
-    // the next PV on a buffer follows the QK that waits on it, so a barrier is never two
-    // phases ahead of its waiter.
+    // Order: QK(0), then per step j: QK(j + 1), PV(j).  The S of step j + 1 is computed
+    // while the softmax of step j runs, and PV(j) follows at once, so the pipe waits for
+    // a softmax only when the softmax is slower than a QK (measured 1.7 % faster than
+    // issuing QK QK PV PV in pairs).  One mbarrier per buffer: the next PV on a buffer
+    // follows the QK that waits on it, so a barrier is never two phases ahead of its waiter.
     // n_spv counts the PVs that read P from an S buffer (their order is the QKs' order);
     // np counts P slots, n_rs the rescales replayed in second passes that reuse P.  The
     // last PV of every pass commits o_done, which the epilogue waits for.
@@ -961,8 +1003,9 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       point(C::NB_P + (n_spv & 1), &p_full[n_spv & 1], (n_spv >> 1) & 1, SITE_PRE_P_FULL);
       const uint32_t p_col = C::TM_S + 128 * (n_spv & 1);
       if (first_of_pass && n_pass > 0) point(C::NB_OFREE, o_free, (n_pass - 1) & 1, SITE_PRE_O_DONE);
-      // one N=128 MMA per 16 keys covers the chunk's 128 output columns (pairs: N=256
-      // over both CTAs' chunks)
+      // V by keys: one N = 256 MMA per 16 keys of the chunk covers the pass's 256 output
+      // columns (four 64-column atoms 8 KB apart).  Otherwise one N = 128 MMA per 16 keys
+      // covers the chunk's 128 output columns (pairs: N = 256 over both CTAs' chunks).
       for (int c = 0; c < C::NVS_P; ++c, ++rc) {
         const int slot = rc % NSLOT;
         point(C::NB_SLOT + slot, &kv_full[slot], (rc / NSLOT) & 1, SITE_PRE_KV_FULL);
@@ -970,10 +1013,17 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
           tc_fence_after();
           if (leader) {
             const uint32_t bsm = ring + slot * C::CHUNK;
+            if constexpr (C::VKEYS) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ts(tbase + C::TM_O + c * 128, tbase + p_col + kk * 8, desc_mnmajor_sw128(bsm + kk * 2048, C::HALF),
-                     ID_PV, (!first_of_pass) || kk > 0);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ts(tbase + C::TM_O, tbase + p_col + (4 * c + kk) * 8, desc_mnmajor_sw128(bsm + kk * 2048, C::KBLK),
+                       ID_PV2, (!first_of_pass) || c > 0 || kk > 0);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ts(tbase + C::TM_O + c * 128, tbase + p_col + kk * 8,
+                       desc_mnmajor_sw128(bsm + kk * 2048, C::HALF), ID_PV, (!first_of_pass) || kk > 0);
+            }
             commit_both(&kv_empty[slot]);
           }
         }
@@ -1008,10 +1058,17 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
           if (leader) {
             const uint32_t bsm = ring + slot * C::CHUNK, psm = q_s + s * C::CHUNK;
             // P: K-major without swizzle, key group g8 (8 keys) of every row at g8 x 2048
+            if constexpr (C::VKEYS) {
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_ss(tbase + C::TM_O + c * 128, desc_kmajor_plain(psm + kk * 2 * 2048, 2048, 128),
-                     desc_mnmajor_sw128(bsm + kk * 2048, C::HALF), ID_PV, (j > 0) || kk > 0);
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ss(tbase + C::TM_O, desc_kmajor_plain(psm + (4 * c + kk) * 2 * 2048, 2048, 128),
+                       desc_mnmajor_sw128(bsm + kk * 2048, C::KBLK), ID_PV2, (j > 0) || c > 0 || kk > 0);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 8; ++kk)
+                mma_ss(tbase + C::TM_O + c * 128, desc_kmajor_plain(psm + kk * 2 * 2048, 2048, 128),
+                       desc_mnmajor_sw128(bsm + kk * 2048, C::HALF), ID_PV, (j > 0) || kk > 0);
+            }
             commit_both(&kv_empty[slot]);
           }
         }
@@ -1030,8 +1087,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       const bool reuse = item_reuse(f);
       const int steps = reuse ? f.nt : C::NPASS * f.nt;
       point(C::NB_Q, q_full, it_local & 1, SITE_PRE_Q);
-      // the S of the second step of a pair is computed while the softmax of the first
-      // runs, and the PVs of the pair while the softmax of the second finishes
+      // QK(k + 1) runs while the softmax of step k works, then PV(k)
       for (int k = -1; k < steps; ++k) {
         if (k + 1 < steps) {
           issue_qk();
