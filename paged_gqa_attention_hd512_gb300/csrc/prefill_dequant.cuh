@@ -63,6 +63,7 @@ __device__ __forceinline__ void prefill_dequant_body(const DequantParams& d, int
   const size_t elems_out = (size_t)units * 16;                                 // values per copy page
   // bytes per caller page: 16 values per unit of 2, 1 or 1/2 bytes
   const size_t in_page = (size_t)units_in * (KVT == KV_BF16 ? 32 : (KVT == KV_FP8 ? 16 : 8));
+  const uint64_t pol_keep = l2_policy_evict_last();
   for (uint64_t g0 = (uint64_t)blk * blockDim.x + threadIdx.x; g0 < total; g0 += U * stride) {
     uint4 a8[U], b8[U];
     uint2 a4[U];
@@ -122,9 +123,9 @@ __device__ __forceinline__ void prefill_dequant_body(const DequantParams& d, int
 #pragma unroll
         for (int j = 0; j < 8; ++j) w[j] = f16x2_to_bf16x2(hmul2_u32(w[j], sf2));
       }
-      uint4* dst = reinterpret_cast<uint4*>(d.shadow + page[k] * elems_out + dst_elem[k]);
-      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      // one 32-byte store per unit (the copy's pages and units are 32-byte aligned), kept in
+      // L2 for the prefill kernel that reads the copy next
+      st_global_v8_hint(d.shadow + page[k] * elems_out + dst_elem[k], w, w + 4, pol_keep);
     }
   }
 }

@@ -295,10 +295,23 @@ __device__ __forceinline__ void prefill_plan_body(const PrefillParams& p) {
     }
     return;
   }
-  for (int t = tid; t < n_tiles; t += blockDim.x) {
-    int b, q0, cost;
-    tile_of(t, b, q0, cost);
-    atomicAdd(&hist[min(kPlanBuckets - 1, cost)], 1);
+  // bucket counts aggregated per warp: the lanes of a warp with the same cost add once
+  // (tiles of equal cost are common: neighbouring tiles of a sequence differ by one KV
+  // tile at most), so a warp makes one shared-memory atomic per distinct cost
+  auto bucket_add = [&](int key, bool valid) -> int {
+    const int lane = tid & 31;
+    const unsigned peers = __match_any_sync(0xffffffffu, valid ? key : -1 - lane);
+    const int first = __ffs(peers) - 1;
+    int base = 0;
+    if (valid && lane == first) base = atomicAdd(&hist[key], __popc(peers));
+    base = __shfl_sync(0xffffffffu, base, first);
+    return base + __popc(peers & ((1u << lane) - 1u));
+  };
+  for (int t0 = 0; t0 < n_tiles; t0 += blockDim.x) {  // blockDim.x is a multiple of 32
+    const int t = t0 + tid;
+    int b = 0, q0 = 0, cost = 0;
+    if (t < n_tiles) tile_of(t, b, q0, cost);
+    bucket_add(min(kPlanBuckets - 1, cost), t < n_tiles);
   }
   __syncthreads();
   // exclusive prefix in descending cost order: bucket c starts after all buckets > c
@@ -332,10 +345,12 @@ __device__ __forceinline__ void prefill_plan_body(const PrefillParams& p) {
     }
   }
   __syncthreads();
-  for (int t = tid; t < n_tiles; t += blockDim.x) {
-    int b, q0, cost;
-    tile_of(t, b, q0, cost);
-    const int slot = atomicAdd(&hist[min(kPlanBuckets - 1, cost)], 1);
+  for (int t0 = 0; t0 < n_tiles; t0 += blockDim.x) {
+    const int t = t0 + tid;
+    int b = 0, q0 = 0, cost = 0;
+    if (t < n_tiles) tile_of(t, b, q0, cost);
+    const int slot = bucket_add(min(kPlanBuckets - 1, cost), t < n_tiles);
+    if (t >= n_tiles) continue;
     for (int k = 0; k < p.Hkv; ++k) {
       if (slot * p.Hkv + k >= p.max_items) break;  // cannot happen within the host bound
       PrefillItem it;
