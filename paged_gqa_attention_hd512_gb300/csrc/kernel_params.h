@@ -87,7 +87,7 @@ struct PrefillParams {
   uint16_t* out;  // bf16 [total_q, Hq, d_vo]
   float* lse;
   int* err;
-  int* hdr;  // [0] number of items
+  int* hdr;  // [0] number of items, [1] number of merges, [2] 1: items are per-tile records
   PrefillItem* items;
   int* tile_off;  // [batch + 1] first tile of each sequence
   // head_dim_vo 512: P tiles of the first pass ([128 rows][128 keys] bf16, in the MMA's

@@ -292,6 +292,7 @@ __device__ __forceinline__ void prefill_plan_body(const PrefillParams& p) {
       }
       p.hdr[0] = n_items;
       p.hdr[1] = n_merge;
+      p.hdr[2] = 0;  // full item records
     }
     return;
   }
@@ -350,23 +351,15 @@ __device__ __forceinline__ void prefill_plan_body(const PrefillParams& p) {
     int b = 0, q0 = 0, cost = 0;
     if (t < n_tiles) tile_of(t, b, q0, cost);
     const int slot = bucket_add(min(kPlanBuckets - 1, cost), t < n_tiles);
-    if (t >= n_tiles) continue;
-    for (int k = 0; k < p.Hkv; ++k) {
-      if (slot * p.Hkv + k >= p.max_items) break;  // cannot happen within the host bound
-      PrefillItem it;
-      it.b = b;
-      it.q_begin = q0;
-      it.kvh = k;
-      it.cost = cost;
-      it.kv_t0 = 0;
-      it.kv_t1 = 0;
-      it.slot = -1;
-      p.items[slot * p.Hkv + k] = it;
-    }
+    // one 16-byte record per tile (sequence, first new token, cost); item it is the
+    // tile's record it / Hkv with kv head it % Hkv
+    if (t < n_tiles && (slot + 1) * p.Hkv <= p.max_items)  // always within the host bound
+      reinterpret_cast<int4*>(p.items)[slot] = make_int4(b, q0, cost, 0);
   }
   if (tid == 0) {
     p.hdr[0] = min(n_tiles * p.Hkv, p.max_items);
     p.hdr[1] = 0;
+    p.hdr[2] = 1;  // tile records
   }
 }
 
@@ -380,8 +373,22 @@ struct PrefillItemInfo {
 
 // `rank`: which tile of a CTA pair's item this CTA computes (0 without pairs).  Both CTAs
 // of a pair walk the KV range of the whole item; the second tile may be empty (n_pos 0).
-__device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams& p, int it, int rank) {
-  const PrefillItem item = p.items[it];
+// tile_list: the plan holds one 16-byte record per tile (sequence, first new token, cost),
+// item it being record it / Hkv with kv head it % Hkv; otherwise full item records.
+__device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams& p, int it, int rank,
+                                                             bool tile_list) {
+  PrefillItem item;
+  if (tile_list) {
+    const int4 r = reinterpret_cast<const int4*>(p.items)[it / p.Hkv];
+    item.b = r.x;
+    item.q_begin = r.y;
+    item.kvh = it % p.Hkv;
+    item.cost = r.z;
+    item.kv_t0 = item.kv_t1 = 0;
+    item.slot = -1;
+  } else {
+    item = p.items[it];
+  }
   PrefillItemInfo f;
   f.b = item.b;
   f.kvh = item.kvh;
@@ -534,6 +541,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
   const uint32_t tbase = *tmem_slot;
   grid_dep_wait();  // the planner (and the page conversion) of this call are complete
   const int n_items = min(p.hdr[0], p.max_items);
+  const bool tile_list = p.hdr[2] != 0;
   const int ps = p.page_size, g = p.group;
   // head_dim_vo 512 (bf16 KV): the second pass reads P of the first from global scratch
   // instead of recomputing S, for items whose KV range fits the scratch
@@ -554,7 +562,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     for (int r = 0;; ++r) {
       const int it = prefill_item_at<C::PAIR>(r);
       if (it >= n_items) break;
-      const PrefillItemInfo f = prefill_item_info(p, it, rank);
+      const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
       const bool reuse = item_reuse(f);
       mbar_wait<C::PAIR>(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
       if (lane == 0) {
@@ -732,7 +740,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     for (int r = 0;; ++r) {
       const int it = prefill_item_at<C::PAIR>(r);
       if (it >= n_items) break;
-      const PrefillItemInfo f = prefill_item_info(p, it, rank);
+      const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
       if (!item_reuse(f)) continue;
       mbar_wait<C::PAIR>(qreg_free, n_reuse & 1, p.err, SITE_PRE_Q);
       mbar_wait(ps_done, n_reuse & 1, p.err, SITE_PRE_P_FULL);
@@ -777,7 +785,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       for (int r = 0;; ++r, ++it_local) {
         const int it = prefill_item_at<C::PAIR>(r);
         if (it >= n_items) break;
-        const PrefillItemInfo f = prefill_item_info(p, it, rank);
+        const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
         mbar_wait(q_empty, (it_local & 1) ^ 1, p.err, SITE_PRE_Q);
         if (lane == 0) {
           mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQB * 128 * g * p.rows_per_tile));
@@ -1098,7 +1106,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     for (int r = 0;; ++r, ++it_local) {
       const int it = prefill_item_at<C::PAIR>(r);
       if (it >= n_items) break;
-      const PrefillItemInfo f = prefill_item_info(p, it, rank);
+      const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
       const bool reuse = item_reuse(f);
       const int steps = reuse ? f.nt : C::NPASS * f.nt;
       point(C::NB_Q, q_full, it_local & 1, SITE_PRE_Q);
@@ -1191,7 +1199,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     for (int r = 0;; ++r, ++it_local) {
       const int it = prefill_item_at<C::PAIR>(r);
       if (it >= n_items) break;
-      const PrefillItemInfo f = prefill_item_info(p, it, rank);
+      const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
       const bool reuse = item_reuse(f);
       const int tag = it_local + 1;
       const int p_local = row / g, h_local = row % g;
