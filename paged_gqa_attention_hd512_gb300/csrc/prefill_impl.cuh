@@ -100,13 +100,16 @@ struct PrefillCfg {
   // head_dim_vo 512 with P reuse: the second pass reads the first pass's P tiles into
   // NPS slots of the Q region (Q is not needed by then)
   static constexpr int NPS = NPASS == 2 ? Q_BYTES / CHUNK : 0;
-  // barriers: q_full, q_empty, s_full[2], p_full[2], pv_done[2], o_free, aux, sfree[2],
+  // barriers: (unused), q_empty, s_full[2], p_full[2], pv_done[2], o_free, aux, sfree[2],
   // ps_done, o_done, o_ready, resc_done, tags_done, qreg_free, kv_full[], kv_empty[], stg_full[], stg_empty[],
   // sf_full[], sf_empty[], pslot_full[], pslot_empty[].  Every waiter of a barrier is at
   // most one phase behind or ahead of it (a parity wait cannot tell more apart): hence one
   // s_full / p_full / pv_done / sfree per S buffer.
   static constexpr int NB_FIXED = 18;
-  static constexpr int NBAR = NB_FIXED + 2 * NSLOT + 2 * NSTG + 2 * NSF + 2 * NPS;
+  // q_part[NKC]: the Q columns of K chunk c have landed (the first QK of an item starts on
+  // the first part of Q instead of waiting for the whole 128 KB tile)
+  static constexpr int NBAR = NB_FIXED + 2 * NSLOT + 2 * NSTG + 2 * NSF + 2 * NPS + NKC;
+  static constexpr int QB_PER = NQB / NKC;  // 64-column Q blocks per K chunk
   static constexpr int BYTES = OFF_BAR + NBAR * 8 + 16;
   static constexpr int ALLOC = BYTES + 1024;
   // TMEM columns: two S buffers of 128 keys (step j uses buffer j & 1; its P, 128 keys of
@@ -461,7 +464,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
   const uint32_t q_s = smem_u32(smem);
   const uint32_t ring = q_s + C::OFF_RING;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* q_full = bars + 0;
+  // bars + 0: unused (the Q tile completes on q_part[] below)
   uint64_t* q_empty = bars + 1;
   uint64_t* s_full = bars + 2;  // [2]: S of step j complete in buffer j & 1
   uint64_t* p_full = bars + 4;  // [2]: P of step j written over buffer j & 1
@@ -483,6 +486,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
   uint64_t* sf_empty = sf_full + C::NSF;
   uint64_t* pslot_full = sf_empty + C::NSF;
   uint64_t* pslot_empty = pslot_full + C::NPS;
+  uint64_t* q_part = pslot_empty + C::NPS;  // [NKC]
   int2* stg_desc = reinterpret_cast<int2*>(smem + C::OFF_DESC);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::NBAR);
 
@@ -493,7 +497,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
   const uint32_t rank = C::PAIR ? cluster_ctarank() : 0;
   auto lead = [&](uint64_t* b) -> uint32_t { return C::PAIR ? mapa_shared(smem_u32(b), 0) : smem_u32(b); };
   if (threadIdx.x == 0) {
-    mbar_init(q_full, C::CL);
+    for (int c = 0; c < C::NKC; ++c) mbar_init(&q_part[c], C::CL);
     mbar_init(q_empty, 1);
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
@@ -565,18 +569,20 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
       const bool reuse = item_reuse(f);
       mbar_wait<C::PAIR>(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
-      if (lane == 0) {
-        const uint32_t qbytes = (uint32_t)(C::NQB * 128 * g * p.rows_per_tile);
+      // Q part c (the columns of K chunk c), into its own barrier
+      auto load_q_part = [&](int c) {
+        if (lane != 0) return;
+        const uint32_t qbytes = (uint32_t)(C::QB_PER * 128 * g * p.rows_per_tile);
         if constexpr (C::PAIR) {
-          mbar_arrive_expect_tx_cluster(lead(q_full), qbytes);
-          for (int c = 0; c < C::NQB; ++c)
-            tma_load_3d_pair(q_s + c * C::HALF, &tm_q, c * 128, f.kvh * g, f.q_row0, lead(q_full), pol_q);
+          mbar_arrive_expect_tx_cluster(lead(&q_part[c]), qbytes);
+          for (int b = c * C::QB_PER; b < (c + 1) * C::QB_PER; ++b)
+            tma_load_3d_pair(q_s + b * C::HALF, &tm_q, b * 128, f.kvh * g, f.q_row0, lead(&q_part[c]), pol_q);
         } else {
-          mbar_arrive_expect_tx(q_full, qbytes);
-          for (int c = 0; c < C::NQB; ++c)
-            tma_load_3d_hint(q_s + c * C::HALF, &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
+          mbar_arrive_expect_tx(&q_part[c], qbytes);
+          for (int b = c * C::QB_PER; b < (c + 1) * C::QB_PER; ++b)
+            tma_load_3d_hint(q_s + b * C::HALF, &tm_q, b * 128, f.kvh * g, f.q_row0, &q_part[c], pol_q);
         }
-      }
+      };
       // steps that compute S: both passes, or only the first when the second reuses P
       const int steps = reuse ? f.nt : C::NPASS * f.nt;
       // a KV tile is ppt pages of rpp rows each (rpp = page_size, or 8 for the padded copy
@@ -590,8 +596,8 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
         const int pieces = max(0, min(ppt, f.np - pg0));
         return (lane < pieces) ? __ldg(p.kv_indices + f.ip0 + pg0 + lane) : 0;
       };
-      // the K or V chunks of step st into the ring
-      auto emit = [&](bool is_k, int st, int my_page) {
+      // the K or V chunks of step st into the ring (K: chunks [c_lo, c_hi), one CTA per tile)
+      auto emit = [&](bool is_k, int st, int my_page, int c_lo = 0, int c_hi = C::NQC) {
         const int pass = st / f.nt, jt = st % f.nt;
         // tile rows before the first that holds no token of the sequence
         const int rem = max(0, f.kv_len - (f.jlo + jt) * p.tile_tok);
@@ -657,8 +663,8 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
           }
           return;
         }
-        const int nch = is_k ? C::NQC : C::NVS_P;
-        for (int c = 0; c < nch; ++c, ++rc) {
+        const int c_end = is_k ? c_hi : C::NVS_P;
+        for (int c = is_k ? c_lo : 0; c < c_end; ++c, ++rc) {
           const int slot = rc % NSLOT;
           mbar_wait<C::PAIR>(&kv_empty[slot], ((rc / NSLOT) & 1) ^ 1, p.err, SITE_PRE_KV_EMPTY);
           const uint32_t dst = ring + slot * C::CHUNK;
@@ -707,9 +713,19 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
           }
         }
       };
-      // chunks in the MMA thread's order: K of step 0, then per step k: K of k + 1, V of k
+      // chunks in the MMA thread's order: K of step 0 (one CTA per tile: each chunk after its
+      // Q part, so the port brings the first Q part and K chunk before the rest of Q), then
+      // per step k: K of k + 1, V of k
       int pg_a = step_pages(0), pg_b = step_pages(1);
-      emit(true, 0, pg_a);
+      if constexpr (C::PAIR) {
+        for (int c = 0; c < C::NKC; ++c) load_q_part(c);
+        emit(true, 0, pg_a);
+      } else {
+        for (int c = 0; c < C::NKC; ++c) {
+          load_q_part(c);
+          emit(true, 0, pg_a, c, c + 1);
+        }
+      }
       for (int k = 0; k < steps; ++k) {
         const int pg_c = step_pages(k + 2);
         if (k + 1 < steps) emit(true, k + 1, pg_b);
@@ -787,11 +803,12 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
         if (it >= n_items) break;
         const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
         mbar_wait(q_empty, (it_local & 1) ^ 1, p.err, SITE_PRE_Q);
-        if (lane == 0) {
-          mbar_arrive_expect_tx(q_full, (uint32_t)(C::NQB * 128 * g * p.rows_per_tile));
-          for (int c = 0; c < C::NQB; ++c)
-            tma_load_3d_hint(q_s + c * C::HALF, &tm_q, c * 128, f.kvh * g, f.q_row0, q_full, pol_q);
-        }
+        if (lane == 0)
+          for (int c = 0; c < C::NKC; ++c) {
+            mbar_arrive_expect_tx(&q_part[c], (uint32_t)(C::QB_PER * 128 * g * p.rows_per_tile));
+            for (int b = c * C::QB_PER; b < (c + 1) * C::QB_PER; ++b)
+              tma_load_3d_hint(q_s + b * C::HALF, &tm_q, b * 128, f.kvh * g, f.q_row0, &q_part[c], pol_q);
+          }
         const int steps = C::NPASS * f.nt;
         const int page_tok_cap = f.np * ps;
         auto step_pages = [&](int st) -> int {
@@ -989,10 +1006,12 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     // last PV of every pass commits o_done, which the epilogue waits for.
     uint32_t rc = 0, n_qk = 0, n_spv = 0, n_pass = 0, np = 0, n_rs = 0;
     int it_local = 0;
-    auto issue_qk = [&]() {
+    // q_wait: the item's first QK, which waits for each Q part before its K chunk
+    auto issue_qk = [&](bool q_wait) {
       const uint32_t s_col = C::TM_S + 128 * (n_qk & 1);
       if (n_qk >= 2) point(C::NB_SFREE + (n_qk & 1), &sfree[n_qk & 1], ((n_qk - 2) >> 1) & 1, SITE_PRE_O_DONE);
       for (int c = 0; c < C::NKC; ++c, ++rc) {
+        if (q_wait) point(C::NB_Q, &q_part[c], it_local & 1, SITE_PRE_Q);
         const int slot = rc % NSLOT;
         point(C::NB_SLOT + slot, &kv_full[slot], (rc / NSLOT) & 1, SITE_PRE_KV_FULL);
         if (warp == 1) {
@@ -1109,11 +1128,10 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
       const bool reuse = item_reuse(f);
       const int steps = reuse ? f.nt : C::NPASS * f.nt;
-      point(C::NB_Q, q_full, it_local & 1, SITE_PRE_Q);
       // QK(k + 1) runs while the softmax of step k works, then PV(k)
       for (int k = -1; k < steps; ++k) {
         if (k + 1 < steps) {
-          issue_qk();
+          issue_qk(k < 0);
           if (leader && k + 1 == steps - 1) {  // the item's last QK
             commit_both(q_empty);
             if (reuse) commit_both(qreg_free);
