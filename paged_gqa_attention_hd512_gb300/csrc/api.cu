@@ -172,6 +172,13 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 int x2_of(int kvt) { return kvt == KV_BF16 ? 4 : (kvt == KV_FP8 ? 2 : 1); }
 
+// Decode chunks of at least about 4 MiB of K and V per kv head (NVFP4: with its scales).
+int decode_min_chunk_pages(int kvt, int dqk, int dvo, int page_size) {
+  const long row = (long)(dqk + dvo) * x2_of(kvt) / 2 + (kvt == KV_NVFP4 ? (dqk + dvo) / 16 : 0);
+  const long page = row * page_size;
+  return (int)std::max(1l, ((4l << 20) + page - 1) / page);
+}
+
 // Checks shared by both phases.  Returns PA_OK or an error status.
 int check_common(const void* q, const void* kv_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
                  const int32_t* kv_last_page_len, int batch, int num_pages, int Hq, int Hkv, int dqk, int dvo,
@@ -505,6 +512,7 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
   p.max_chunks = max_chunks;
   p.target_chunks = target;
   p.forced_chunk_pages = forced;
+  p.min_chunk_pages = decode_min_chunk_pages(kv_dtype, head_dim_qk, head_dim_vo, page_size);
   p.box_rows = box_rows;
   p.box_shift = __builtin_ctz((unsigned)box_rows);
   p.swz = swz ? 7 : 0;
@@ -869,6 +877,7 @@ extern "C" int paged_attn_decode_noalloc(const void* q, const void* kv_cache, co
   p.max_chunks = max_chunks;
   p.target_chunks = (int)target;
   p.forced_chunk_pages = forced;
+  p.min_chunk_pages = decode_min_chunk_pages(kv_dtype, head_dim_qk, head_dim_vo, page_size);
   p.box_rows = box_rows;
   p.box_shift = __builtin_ctz((unsigned)box_rows);
   p.swz = swz ? 7 : 0;

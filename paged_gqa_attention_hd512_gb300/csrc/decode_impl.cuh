@@ -66,9 +66,10 @@ struct DecodeSmem {
 
 // ----------------------------------------------------------------------------- plan
 // Cut the visible page range of every sequence into page-aligned chunks.  With W the
-// total visible pages, chunks hold C = max(forced, ceil(W / target_chunks)) pages, so
-// the number of chunks never exceeds target_chunks + batch (the workspace bound); each
-// sequence's range is then split evenly into ceil(pages / C) chunks.
+// total visible pages, chunks hold C >= ceil(W / target_chunks) pages (raised towards
+// min_chunk_pages, or set by the chunk-size test hook), so the number of chunks never
+// exceeds target_chunks + batch (the workspace bound); each sequence's range is then
+// split evenly into ceil(pages / C) chunks.
 #ifdef PA_DECODE_AUX
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
   __shared__ int s_red[32];
@@ -97,7 +98,15 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
   __syncthreads();
   const int total = s_red[0];
   int cp = (total + p.target_chunks - 1) / max(1, p.target_chunks);
-  cp = max(cp, max(1, p.forced_chunk_pages));
+  if (p.forced_chunk_pages > 0) {
+    cp = max(cp, p.forced_chunk_pages);
+  } else {
+    // a split costs a partial row written and merged: chunks of at least min_chunk_pages
+    // (about 4 MiB of K and V per kv head), as long as a quarter of the target number of
+    // chunks remains for the balance of the persistent CTAs
+    const int cap = (int)max(1ll, 4ll * total / max(1, p.target_chunks));
+    cp = max(cp, min(p.min_chunk_pages, cap));
+  }
   __syncthreads();
   if (tid == 0) s_carry = 0;
   __syncthreads();

@@ -50,6 +50,7 @@ struct DecodeParams {
   float2* ws_ml;      // [max_chunks][Hq] {running max (log2 units), running sum}
   int batch, Hq, Hkv, group, page_size, window_left;
   int max_chunks, target_chunks, forced_chunk_pages;
+  int min_chunk_pages;  // pages of about 4 MiB of K and V of one kv head
   int box_rows;   // rows per TMA box: min(page_size, tile tokens), a power of two
   int box_shift;  // log2(box_rows)
   int swz;        // 7 when the K/V smem tiles are 128B-swizzled, 0 when not
