@@ -529,7 +529,7 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
   else e = launch_decode_nvfp4(head_dim_qk, head_dim_vo, hp, L, &name);
   prof_mark(L.stream, false);
   if (e != cudaSuccess) return PA_ERR_CUDA;
-  if (launch_decode_merge(head_dim_vo, p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_decode_merge(head_dim_vo, p, L.grid, L.stream) != cudaSuccess) return PA_ERR_CUDA;
   static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};
   std::snprintf(g_variant, sizeof g_variant, "%s_%s", name, kv_names[kv_dtype]);
   return PA_OK;
@@ -892,7 +892,7 @@ extern "C" int paged_attn_decode_noalloc(const void* q, const void* kv_cache, co
   else e = launch_decode_nvfp4(head_dim_qk, head_dim_vo, hp, L, &name);
   prof_mark(L.stream, false);
   if (e != cudaSuccess) return PA_ERR_CUDA;
-  if (launch_decode_merge(head_dim_vo, p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_decode_merge(head_dim_vo, p, L.grid, L.stream) != cudaSuccess) return PA_ERR_CUDA;
   static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};
   std::snprintf(g_variant, sizeof g_variant, "%s_%s_noalloc", name, kv_names[kv_dtype]);
   return PA_OK;

@@ -1,5 +1,6 @@
 // decode_aux.cu -- the decode work planner, the split-K merge and shape queries.
 #define PA_DECODE_AUX 1
+#include <algorithm>
 #include "decode_inst.cuh"
 
 namespace pa {
@@ -9,9 +10,10 @@ cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode_merge(int dvo, const DecodeParams& p, cudaStream_t s) {
+cudaError_t launch_decode_merge(int dvo, const DecodeParams& p, int sms, cudaStream_t s) {
   const long warps = (long)p.batch * p.Hq * (dvo / 128);
-  const int blocks = (int)((warps * 32 + 255) / 256);
+  // one warp per unit up to two 256-thread blocks per SM; the warps stride over the rest
+  const int blocks = (int)std::min<long>((warps * 32 + 255) / 256, 2l * sms);
   if (blocks == 0) return cudaSuccess;
   // a programmatic dependent of the decode kernel
   if (dvo == 512) return launch_pdl(decode_merge_kernel<512>, dim3(blocks), dim3(256), 0, s, 1, p);

@@ -166,17 +166,10 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
 
 // ----------------------------------------------------------------------------- merge
 // out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  lse = ln2 * (M + log2 L).
-// One warp per (sequence, query head, 128 output columns): lane s of the warp reads the
-// (m, l) of partial s (32 at a time) and forms its weight once; every lane then owns 4
-// columns and issues the loads of 8 partials before it sums them, so the warp waits on
-// L2 once per 8 partials rather than once per partial.
+// One (row, 128-column quarter) unit of the merge, by one warp.
 template <int DVO>
-__global__ void __launch_bounds__(256) decode_merge_kernel(DecodeParams p) {
-  constexpr int NQ = DVO / 128;  // column quarters (warps) per row
-  grid_dep_wait();  // the decode kernel's partials are complete
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (gw >= p.batch * p.Hq * NQ) return;
+__device__ __forceinline__ void decode_merge_unit(const DecodeParams& p, int gw, int lane) {
+  constexpr int NQ = DVO / 128;
   const int row = gw / NQ, qc = gw % NQ;
   const int b = row / p.Hq, hq = row % p.Hq;
   const int2 si = p.seq_info[b];
@@ -227,6 +220,22 @@ __global__ void __launch_bounds__(256) decode_merge_kernel(DecodeParams p) {
   const float inv = L > 0.f ? 1.f / L : 0.f;
   *orow = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
   if (p.lse && qc == 0 && lane == 0) p.lse[row] = (L > 0.f) ? (M + log2f(L)) * 0.69314718055994531f : -INFINITY;
+}
+
+// One warp per (sequence, query head, 128 output columns) unit, the units strided over a
+// grid of at most two blocks per SM (most rows were written by the decode kernel itself,
+// and a block per few units would cost more to schedule than to run): lane s of the warp
+// reads the (m, l) of partial s (32 at a time) and forms its weight once; every lane then
+// owns 4 columns and issues the loads of 8 partials before it sums them, so the warp
+// waits on L2 once per 8 partials rather than once per partial.
+template <int DVO>
+__global__ void __launch_bounds__(256) decode_merge_kernel(DecodeParams p) {
+  constexpr int NQ = DVO / 128;  // column quarters (warps) per row
+  grid_dep_wait();  // the decode kernel's partials are complete
+  const int lane = threadIdx.x & 31;
+  const int units = p.batch * p.Hq * NQ;
+  for (int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; gw < units; gw += (gridDim.x * blockDim.x) >> 5)
+    decode_merge_unit<DVO>(p, gw, lane);
 }
 
 }  // namespace pa

@@ -58,7 +58,7 @@ cudaError_t launch_decode_bf16(int dqk, int dvo, int hp, const DecodeLaunch& L, 
 cudaError_t launch_decode_fp8(int dqk, int dvo, int hp, const DecodeLaunch& L, const char** variant);
 cudaError_t launch_decode_nvfp4(int dqk, int dvo, int hp, const DecodeLaunch& L, const char** variant);
 cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t s);
-cudaError_t launch_decode_merge(int dvo, const DecodeParams& p, cudaStream_t s);
+cudaError_t launch_decode_merge(int dvo, const DecodeParams& p, int sms, cudaStream_t s);
 // Shared memory (bytes) the decode kernel of this shape needs.
 int decode_smem_bytes(int kvt, int dqk, int dvo, int hp);
 // Tokens per decode tile of this shape.
