@@ -67,12 +67,13 @@ def bench_case(name, device="cuda"):
 
 
 def prefill_launches(variant: str) -> int:
-    """Kernels one prefill call launches: planner and prefill, plus the FP8 / NVFP4 page
-    conversion and the split-KV merge when the variant names them."""
-    return 2 + ("_dequant" in variant) + ("_splitkv" in variant)
+    """Kernels one prefill call launches: the preparation (planner, with the FP8 / NVFP4
+    page conversion or the small-page padding in the same launch) and the prefill kernel,
+    plus the split-KV merge when the variant names it."""
+    return 2 + ("_splitkv" in variant)
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DECODE_SOURCES = ("decode_impl.cuh", "common.cuh", "decode_inst.cuh", "kernel_params.h")
-PREFILL_SOURCES = ("prefill_impl.cuh", "common.cuh", "kernel_params.h")
+PREFILL_SOURCES = ("prefill_impl.cuh", "common.cuh", "tc_helpers.cuh", "kernel_params.h")
 
 
 # ------------------------------------------------------------------------- work counts
@@ -352,7 +353,7 @@ def bench_decode(name, steps, warmup, barrier, gpu_index, pk, with_e2e=True, wit
     res = {"workload": name, "config": {"workload": DESCRIBE.get(name, name), "name": name},
            "ms_per_step": ms / steps, "value": nbytes / (ms / steps * 1e-3) / 1e9,
            "unit": "GB/s", "bytes_per_step": nbytes, "steps": steps, "clocks": clocks, "variant": variant,
-           "gpu_launches": 2 * steps}
+           "gpu_launches": 3 * steps}  # planner, decode kernel, merge
     kern_ms = k_ms / max(1, n_k)
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
     digest = sources_digest(DECODE_SOURCES)
