@@ -1006,9 +1006,13 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     // last PV of every pass commits o_done, which the epilogue waits for.
     uint32_t rc = 0, n_qk = 0, n_spv = 0, n_pass = 0, np = 0, n_rs = 0;
     int it_local = 0;
+    // TMEM halves of this item: S buffers at tm_s, O of the first pass at tm_o; a second
+    // pass that reuses P accumulates at tm_s (the S buffers are free by then), so it need
+    // not wait for the first pass's O to drain; after such an item the halves swap
+    uint32_t flip = 0, tm_s = C::TM_S, tm_o = C::TM_O;
     // q_wait: the item's first QK, which waits for each Q part before its K chunk
     auto issue_qk = [&](bool q_wait) {
-      const uint32_t s_col = C::TM_S + 128 * (n_qk & 1);
+      const uint32_t s_col = tm_s + 128 * (n_qk & 1);
       if (n_qk >= 2) point(C::NB_SFREE + (n_qk & 1), &sfree[n_qk & 1], ((n_qk - 2) >> 1) & 1, SITE_PRE_O_DONE);
       for (int c = 0; c < C::NKC; ++c, ++rc) {
         if (q_wait) point(C::NB_Q, &q_part[c], it_local & 1, SITE_PRE_Q);
@@ -1043,7 +1047,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     };
     auto issue_pv = [&](bool first_of_pass, bool last_of_pass) {
       point(C::NB_P + (n_spv & 1), &p_full[n_spv & 1], (n_spv >> 1) & 1, SITE_PRE_P_FULL);
-      const uint32_t p_col = C::TM_S + 128 * (n_spv & 1);
+      const uint32_t p_col = tm_s + 128 * (n_spv & 1);
       if (first_of_pass && n_pass > 0) point(C::NB_OFREE, o_free, (n_pass - 1) & 1, SITE_PRE_O_DONE);
       // V by keys: one N = 256 MMA per 16 keys of the chunk covers the pass's 256 output
       // columns (four 64-column atoms 8 KB apart).  Otherwise one N = 128 MMA per 16 keys
@@ -1058,12 +1062,12 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
             if constexpr (C::VKEYS) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tbase + C::TM_O, tbase + p_col + (4 * c + kk) * 8, desc_mnmajor_sw128(bsm + kk * 2048, C::KBLK),
+                mma_ts(tbase + tm_o, tbase + p_col + (4 * c + kk) * 8, desc_mnmajor_sw128(bsm + kk * 2048, C::KBLK),
                        ID_PV2, (!first_of_pass) || c > 0 || kk > 0);
             } else {
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                mma_ts(tbase + C::TM_O + c * 128, tbase + p_col + kk * 8,
+                mma_ts(tbase + tm_o + c * 128, tbase + p_col + kk * 8,
                        desc_mnmajor_sw128(bsm + kk * 2048, C::HALF), ID_PV, (!first_of_pass) || kk > 0);
             }
             commit_both(&kv_empty[slot]);
@@ -1082,8 +1086,11 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     // follow one another without the softmax, except where the first pass rescaled O
     // before tile j: then the MMAs so far are committed to o_ready, and the PV waits until
     // the softmax warps have applied the same factor (resc_done).
-    auto issue_pv_reuse = [&](int j, int last, uint64_t rmask) {
-      if (j == 0) point(C::NB_OFREE, o_free, (n_pass - 1) & 1, SITE_PRE_O_DONE);
+    // p1: index of the item's first pass (its o_done / o_free phases)
+    auto issue_pv_reuse = [&](int j, int last, uint64_t rmask, uint32_t p1) {
+      // the first pass's MMAs are complete (its last PVs read P from the columns this pass
+      // accumulates in); its O may still be draining from the other half
+      if (j == 0) point(C::NB_OFREE, o_done, p1 & 1, SITE_PRE_O_DONE);
       if ((rmask >> j) & 1) {
         if (leader) commit_both(o_ready);
         point(C::NB_OFREE, resc_done, n_rs & 1, SITE_PRE_P_FULL);
@@ -1103,21 +1110,24 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
             if constexpr (C::VKEYS) {
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_ss(tbase + C::TM_O, desc_kmajor_plain(psm + (4 * c + kk) * 2 * 2048, 2048, 128),
+                mma_ss(tbase + tm_s, desc_kmajor_plain(psm + (4 * c + kk) * 2 * 2048, 2048, 128),
                        desc_mnmajor_sw128(bsm + kk * 2048, C::KBLK), ID_PV2, (j > 0) || c > 0 || kk > 0);
             } else {
 #pragma unroll
               for (int kk = 0; kk < 8; ++kk)
-                mma_ss(tbase + C::TM_O + c * 128, desc_kmajor_plain(psm + kk * 2 * 2048, 2048, 128),
+                mma_ss(tbase + tm_s + c * 128, desc_kmajor_plain(psm + kk * 2 * 2048, 2048, 128),
                        desc_mnmajor_sw128(bsm + kk * 2048, C::HALF), ID_PV, (j > 0) || kk > 0);
             }
             commit_both(&kv_empty[slot]);
           }
         }
       }
-      if (leader) {
-        commit_both(&pslot_empty[s]);
-        if (j == last) commit_both(o_done);
+      if (leader) commit_both(&pslot_empty[s]);
+      if (j == last) {
+        // the first pass's O has drained before the next item writes S over it (waited here,
+        // before this pass's o_done exists, so o_free is never two phases ahead)
+        point(C::NB_OFREE, o_free, p1 & 1, SITE_PRE_O_DONE);
+        if (leader) commit_both(o_done);
       }
       ++np;
       if (j == 0) ++n_pass;
@@ -1148,8 +1158,12 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
         const uint64_t rmask = (uint64_t)__ballot_sync(0xffffffffu, lane < C::MAX_RT && rtag[lane] == tag) |
                                ((uint64_t)__ballot_sync(0xffffffffu, lane + 32 < C::MAX_RT && rtag[lane + 32] == tag)
                                 << 32);
-        for (int j = 0; j < f.nt; ++j) issue_pv_reuse(j, f.nt - 1, rmask);
+        const uint32_t p1 = n_pass - 1;
+        for (int j = 0; j < f.nt; ++j) issue_pv_reuse(j, f.nt - 1, rmask, p1);
         if (leader) commit_both(q_empty);  // the P slots (Q region) are free
+        flip ^= 1;
+        tm_s = flip ? C::TM_O : C::TM_S;
+        tm_o = flip ? C::TM_S : C::TM_O;
       }
     }
   } else if (warp >= 4) {
@@ -1188,15 +1202,18 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     const bool pos_scale = scale_log2 > 0.f;
     const float eff_scale = pos_scale ? scale_log2 : 1.f;
     const float v_scale = p.v_scale ? __ldg(p.v_scale) : 1.f;
-    auto rescale_o = [&](float a) {
+    // TMEM halves as the MMA warp uses them: S at tm_s, the first pass's O at tm_o, a
+    // second pass that reuses P at tm_s; swapped after every such item
+    uint32_t flip = 0, tm_s = C::TM_S, tm_o = C::TM_O;
+    auto rescale_o = [&](float a, uint32_t o_col) {
 #pragma unroll 1
       for (int c = 0; c < OCOL / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld32(lane_base + C::TM_O + ocol0 + 32 * c, ov);
+        tmem_ld32(lane_base + o_col + ocol0 + 32 * c, ov);
         tc_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * a);
-        tmem_st32(lane_base + C::TM_O + ocol0 + 32 * c, ov);
+        tmem_st32(lane_base + o_col + ocol0 + 32 * c, ov);
       }
       tc_wait_st();
     };
@@ -1245,7 +1262,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
             ++n_rs;
             __syncwarp();
             tc_fence_after();
-            if (__any_sync(0xffffffffu, a != 1.f)) rescale_o(a);
+            if (__any_sync(0xffffffffu, a != 1.f)) rescale_o(a, tm_s);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) arrive_lead(resc_done);
@@ -1254,7 +1271,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
           m_used = -INFINITY;
           l = 0.f;
           for (int jt = 0; jt < f.nt; ++jt, ++sstep) {
-            const uint32_t s_col = C::TM_S + 128 * (sstep & 1);
+            const uint32_t s_col = tm_s + 128 * (sstep & 1);
             mbar_wait<C::PAIR>(&s_full[sstep & 1], (sstep >> 1) & 1, p.err, SITE_PRE_S_FULL);
             __syncwarp();  // the tcgen05 loads below are warp-collective
             tc_fence_after();
@@ -1361,7 +1378,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
               mbar_wait<C::PAIR>(&pv_done[(sstep - 1) & 1], ((sstep - 1) >> 1) & 1, p.err, SITE_PRE_O_DONE);
               __syncwarp();
               tc_fence_after();
-              rescale_o(resc ? alpha : 1.f);
+              rescale_o(resc ? alpha : 1.f, tm_o);
               if (reuse && lane == 0) {  // the second pass replays this rescale (pairs: in both CTAs)
                 rtag[jt] = tag;
                 if constexpr (C::PAIR) st_shared_cluster_u32(mapa_shared(smem_u32(&rtag[jt]), rank ^ 1), (uint32_t)tag);
@@ -1412,6 +1429,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
         __syncwarp();
         tc_fence_after();
         const float inv = lt > 0.f ? v_scale / lt : 0.f;
+        const uint32_t o_col = (reuse && pass == 1) ? tm_s : tm_o;  // this pass's O
         uint16_t* orow = p.out + ((size_t)(f.q_row0 + p_local) * p.Hq + hq) * DVO + pass * C::DVP + ocol0;
         const float row_lse = lt > 0.f ? (m_used + log2f(lt)) * 0.69314718055994531f : -INFINITY;
         if (f.slot >= 0) {
@@ -1420,7 +1438,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
 #pragma unroll 1
           for (int c = 0; c < OCOL / 32; ++c) {
             uint32_t ov[32];
-            tmem_ld32(lane_base + C::TM_O + ocol0 + 32 * c, ov);
+            tmem_ld32(lane_base + o_col + ocol0 + 32 * c, ov);
             tc_wait_ld();
             if (row_ok) {
               float4* dst = reinterpret_cast<float4*>(prow + 32 * c);
@@ -1435,7 +1453,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
 #pragma unroll 1
           for (int c = 0; c < OCOL / 32; ++c) {
             uint32_t ov[32];
-            tmem_ld32(lane_base + C::TM_O + ocol0 + 32 * c, ov);
+            tmem_ld32(lane_base + o_col + ocol0 + 32 * c, ov);
             tc_wait_ld();
             uint32_t pkd[16];
 #pragma unroll
@@ -1454,6 +1472,11 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) arrive_lead(o_free);
+      }
+      if (reuse) {
+        flip ^= 1;
+        tm_s = flip ? C::TM_O : C::TM_S;
+        tm_o = flip ? C::TM_S : C::TM_O;
       }
     }
   }
