@@ -513,6 +513,7 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
   p.target_chunks = target;
   p.forced_chunk_pages = forced;
   p.min_chunk_pages = decode_min_chunk_pages(kv_dtype, head_dim_qk, head_dim_vo, page_size);
+  p.grid = grid;
   p.box_rows = box_rows;
   p.box_shift = __builtin_ctz((unsigned)box_rows);
   p.swz = swz ? 7 : 0;
@@ -878,6 +879,7 @@ extern "C" int paged_attn_decode_noalloc(const void* q, const void* kv_cache, co
   p.target_chunks = (int)target;
   p.forced_chunk_pages = forced;
   p.min_chunk_pages = decode_min_chunk_pages(kv_dtype, head_dim_qk, head_dim_vo, page_size);
+  p.grid = grid;
   p.box_rows = box_rows;
   p.box_shift = __builtin_ctz((unsigned)box_rows);
   p.swz = swz ? 7 : 0;

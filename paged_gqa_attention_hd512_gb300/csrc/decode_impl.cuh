@@ -72,13 +72,14 @@ struct DecodeSmem {
 // split evenly into ceil(pages / C) chunks.
 #ifdef PA_DECODE_AUX
 __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
-  __shared__ int s_red[32];
+  __shared__ int s_red[32], s_max[32], s_min[32];
   __shared__ int s_carry;
   grid_dep_launch();  // the decode kernel may start its set-up (it waits for this grid)
   const int tid = threadIdx.x;
   const int ps = p.page_size;
-  // pass 1: total visible pages
-  int mine = 0;
+  // pass 1: total visible pages, and their largest and smallest count over the sequences
+  // that have any
+  int mine = 0, pmax = 0, pmin = INT_MAX;
   for (int b = tid; b < p.batch; b += blockDim.x) {
     int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
     if (np <= 0) continue;
@@ -86,26 +87,93 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
     int first = 0;
     if (p.window_left >= 0) first = max(0, kv_len - 1 - p.window_left) / ps;
     mine += np - first;
+    pmax = max(pmax, np - first);
+    pmin = min(pmin, np - first);
   }
-  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
-  if ((tid & 31) == 0) s_red[tid >> 5] = mine;
+  for (int o = 16; o > 0; o >>= 1) {
+    mine += __shfl_xor_sync(0xffffffffu, mine, o);
+    pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, o));
+    pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, o));
+  }
+  if ((tid & 31) == 0) {
+    s_red[tid >> 5] = mine;
+    s_max[tid >> 5] = pmax;
+    s_min[tid >> 5] = pmin;
+  }
   __syncthreads();
   if (tid < 32) {
-    int v = (tid < (int)(blockDim.x >> 5)) ? s_red[tid] : 0;
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (tid == 0) s_red[0] = v;
+    const bool in = tid < (int)(blockDim.x >> 5);
+    int v = in ? s_red[tid] : 0, vmax = in ? s_max[tid] : 0, vmin = in ? s_min[tid] : INT_MAX;
+    for (int o = 16; o > 0; o >>= 1) {
+      v += __shfl_xor_sync(0xffffffffu, v, o);
+      vmax = max(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+      vmin = min(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
+    }
+    if (tid == 0) {
+      s_red[0] = v;
+      s_max[0] = vmax;
+      s_min[0] = vmin;
+    }
   }
   __syncthreads();
   const int total = s_red[0];
+  const bool uniform = s_max[0] > 0 && s_max[0] == s_min[0];  // every sequence the same pages
   int cp = (total + p.target_chunks - 1) / max(1, p.target_chunks);
   if (p.forced_chunk_pages > 0) {
     cp = max(cp, p.forced_chunk_pages);
   } else {
-    // a split costs a partial row written and merged: chunks of at least min_chunk_pages
+    // a split costs a partial row written and merged: chunks of up to min_chunk_pages
     // (about 4 MiB of K and V per kv head), as long as a quarter of the target number of
-    // chunks remains for the balance of the persistent CTAs
+    // chunks (about four items per CTA) remains for the balance of the persistent CTAs ...
     const int cap = (int)max(1ll, 4ll * total / max(1, p.target_chunks));
-    cp = max(cp, min(p.min_chunk_pages, cap));
+    const int cp_big = max(cp, min(p.min_chunk_pages, cap));
+    const long long grid = max(1, p.grid);
+    if (cp_big > cp && uniform) {
+      // equal sequences give equal items, and the kernel's time is the rounds of items over
+      // the CTAs times the item size: the fewest chunks per sequence, between those of
+      // cp_big and those of cp, with the least of that product
+      const int P = s_max[0];
+      const int n_lo = (P + cp_big - 1) / cp_big, n_hi = (P + cp - 1) / cp;
+      const long long seq_items = (long long)(total / P) * p.Hkv;  // items per chunk of every sequence
+      long long best = LLONG_MAX;
+      int best_n = n_hi;
+      for (int n = n_lo; n <= n_hi; ++n) {
+        const long long t = (seq_items * n + grid - 1) / grid * ((P + n - 1) / n);
+        if (t < best) {
+          best = t;
+          best_n = n;
+        }
+      }
+      cp = (P + best_n - 1) / best_n;
+    } else if (cp_big > cp) {
+      // ... then the smallest chunks that keep the same number of rounds of items over
+      // the CTAs, so the last round is as full as the others
+      int n = 0;
+      for (int b = tid; b < p.batch; b += blockDim.x) {
+        const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
+        if (np <= 0) continue;
+        const int kv_len = (np - 1) * ps + p.kv_last_page_len[b];
+        const int first = p.window_left >= 0 ? max(0, kv_len - 1 - p.window_left) / ps : 0;
+        n += (np - first + cp_big - 1) / cp_big;
+      }
+      for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+      __syncthreads();
+      if ((tid & 31) == 0) s_red[tid >> 5] = n;
+      __syncthreads();
+      if (tid < 32) {
+        int v = (tid < (int)(blockDim.x >> 5)) ? s_red[tid] : 0;
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (tid == 0) s_red[0] = v;
+      }
+      __syncthreads();
+      // (aiming below the full last round by one item per sequence and kv head, since each
+      // sequence's chunk count rounds up)
+      const long long items = (long long)s_red[0] * p.Hkv;
+      const long long rounds = (items + grid - 1) / grid;
+      const long long room = max(1ll, rounds * grid - (long long)p.batch * p.Hkv);
+      const int cp_fill = (int)min((long long)cp_big, (cp_big * items + room - 1) / room);
+      cp = max(cp, cp_fill);
+    }
   }
   __syncthreads();
   if (tid == 0) s_carry = 0;

@@ -51,6 +51,7 @@ struct DecodeParams {
   int batch, Hq, Hkv, group, page_size, window_left;
   int max_chunks, target_chunks, forced_chunk_pages;
   int min_chunk_pages;  // pages of about 4 MiB of K and V of one kv head
+  int grid;             // CTAs of the decode kernel
   int box_rows;   // rows per TMA box: min(page_size, tile tokens), a power of two
   int box_shift;  // log2(box_rows)
   int swz;        // 7 when the K/V smem tiles are 128B-swizzled, 0 when not
