@@ -111,3 +111,57 @@ def test_appended_nvfp4_cache_feeds_the_prefill():
     ref_out, ref_lse = oracle.full(filled)
     n = q.shape[0] * hq
     compare(out.reshape(n, -1), lse.reshape(n), ref_out.reshape(n, -1), ref_lse.reshape(n), "append -> prefill")
+
+
+def _near(m, k):
+    """The fp32 value k units in the last place away from m (m > 0, same binade)."""
+    ulp = 2.0 ** (np.floor(np.log2(m)) - 23)
+    return float(np.float32(m + k * ulp))
+
+
+@pytest.mark.parametrize("k_off", [-3, -2, -1, 0, 1, 2, 3])
+def test_append_fp8_quotients_at_rounding_midpoints(k_off):
+    """x / scale within a few fp32 units of an e4m3 rounding midpoint (and on it): the
+    codes follow the correctly rounded quotient, as in the oracle, wherever the kernel
+    forms it."""
+    ensure_built()
+    rng = np.random.default_rng(5 + k_off)
+    # midpoints between neighbouring e4m3 values: 1 and 1.125, 2.5 and 2.75, 13 and 14,
+    # 416 and 448, and in the smallest normal binade 2^-6 (1 + 1/16)
+    for j, m in enumerate([1.0625, 2.625, 13.5, 432.0, 2.0 ** -6 * 1.0625]):
+        x = float(torch.tensor(rng.standard_normal() * 4.0 + 0.5).to(torch.bfloat16))
+        if x == 0.0:
+            x = 1.5
+        scale = float(np.float32(abs(x) / _near(m, k_off)))
+        case = ac.make(kv_lens=[3], n_new=[1], Hkv=1, d_qk=256, d_vo=256, page_size=8, kv_dtype=ac.FP8,
+                       seed=40 + j, k_scale=scale, v_scale=scale)
+        case.k_new[0, 0, 0] = x
+        case.v_new[0, 0, 5] = -x
+        cache, _, code = _run_gpu(case)
+        ref_cache, _, skipped = _oracle(case)
+        assert code == 0 and skipped == 0
+        _assert_bytes_equal(cache, ref_cache, f"midpoint {m} offset {k_off}")
+
+
+@pytest.mark.parametrize("k_off", [-3, -2, -1, 0, 1, 2, 3])
+def test_append_nvfp4_quotients_at_rounding_midpoints(k_off):
+    """Within an NVFP4 block, x / d within a few fp32 units of an e2m1 rounding midpoint
+    (and on it), with the block scale 1.0 and a global scale chosen for it: codes as in the
+    oracle."""
+    ensure_built()
+    for j, mid in enumerate([1.25, 1.75, 2.5, 3.5, 5.0]):
+        target = _near(mid, k_off)
+        g = float(np.float32(1.0 / target))            # d = 1.0 * g, so 1.0 / d is near the target
+        amax = float(torch.tensor(5.88 * g).to(torch.bfloat16))  # (amax / 6) / g rounds to e4m3 1.0
+        case = ac.make(kv_lens=[3], n_new=[1], Hkv=1, d_qk=256, d_vo=256, page_size=8, kv_dtype=ac.NVFP4,
+                       seed=60 + j, k_scale=g, v_scale=g)
+        for t in (case.k_new, case.v_new):
+            t[0, 0, 0:16] = 0.0
+            t[0, 0, 0] = amax
+            t[0, 0, 1] = 1.0
+            t[0, 0, 2] = -1.0
+        cache, sf, code = _run_gpu(case)
+        ref_cache, ref_sf, skipped = _oracle(case)
+        assert code == 0 and skipped == 0
+        _assert_bytes_equal(cache, ref_cache, f"midpoint {mid} offset {k_off}")
+        _assert_bytes_equal(sf, ref_sf, f"scales, midpoint {mid} offset {k_off}")
