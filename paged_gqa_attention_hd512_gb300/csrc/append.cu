@@ -18,8 +18,8 @@
 // Every operation is a correctly rounded fp32 operation in this order, so the codes are
 // a function of the inputs alone.
 //
-// One CTA per new token; each thread converts 16-element units (32 bytes of bf16), so a
-// warp reads 1 KB of consecutive input.
+// One warp per new token, eight per CTA; each lane converts 16-element units (32 bytes of
+// bf16), so a warp reads 1 KB of consecutive input.
 #include "launch.h"
 #include "common.cuh"
 
@@ -56,28 +56,33 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 
+constexpr int kAppendWarps = 8;  // new tokens per CTA, one per warp
+
 template <int KVT>
-__global__ void __launch_bounds__(256) append_kv_kernel(const AppendParams p) {
-  __shared__ int s_b;
-  const int i = blockIdx.x;  // new token
-  if (threadIdx.x == 0) {
-    int lo = 0, hi = p.batch - 1;  // last b with append_indptr[b] <= i
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (p.append_indptr[mid] <= i) lo = mid; else hi = mid - 1;
-    }
-    s_b = lo;
+__global__ void __launch_bounds__(32 * kAppendWarps) append_kv_kernel(const AppendParams p) {
+  const int lane = threadIdx.x & 31;
+  const int i = blockIdx.x * kAppendWarps + (threadIdx.x >> 5);  // this warp's new token
+  if (i >= p.total_new) return;
+  // the last sequence b with append_indptr[b] <= i, 32 candidates per round: a chain of
+  // dependent loads is what a token's work waits on, so it is kept to a few rounds
+  int lo = 0, hi = p.batch;  // append_indptr[lo] <= i, and i < append_indptr[hi] unless hi == batch
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) / 32;
+    const int c = lo + step * lane;
+    const bool le = lane > 0 && c < hi && __ldg(p.append_indptr + c) <= i;
+    const unsigned m = __ballot_sync(0xffffffffu, le);
+    if (m) lo += step * (31 - __clz(m));
+    hi = min(hi, lo + step);
   }
-  __syncthreads();
-  const int b = s_b;
-  const int n_new = p.append_indptr[b + 1] - p.append_indptr[b];
-  const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
-  const int kv_len = np > 0 ? (np - 1) * p.page_size + p.kv_last_page_len[b] : 0;
-  const int t = kv_len - n_new + (i - p.append_indptr[b]);  // position in the sequence
+  const int b = lo;
+  const int a0 = __ldg(p.append_indptr + b), n_new = __ldg(p.append_indptr + b + 1) - a0;
+  const int ip0 = __ldg(p.kv_indptr + b), np = __ldg(p.kv_indptr + b + 1) - ip0;
+  const int kv_len = np > 0 ? (np - 1) * p.page_size + __ldg(p.kv_last_page_len + b) : 0;
+  const int t = kv_len - n_new + (i - a0);  // position in the sequence
   int page = -1;
-  if (t >= 0 && t < kv_len) page = p.kv_indices[p.kv_indptr[b] + t / p.page_size];
+  if (t >= 0 && t < kv_len) page = __ldg(p.kv_indices + ip0 + t / p.page_size);
   if (page < 0 || page >= p.num_pages) {
-    if (threadIdx.x == 0) record_error(p.err, SITE_APPEND_POS);
+    if (lane == 0) record_error(p.err, SITE_APPEND_POS);
     return;
   }
   const int slot = t % p.page_size;
@@ -93,7 +98,7 @@ __global__ void __launch_bounds__(256) append_kv_kernel(const AppendParams p) {
     ks = __ldg(p.k_scale);
     vs = __ldg(p.v_scale);
   }
-  for (int u = threadIdx.x; u < units; u += blockDim.x) {
+  for (int u = lane; u < units; u += 32) {
     const int h = u / (ku + vu), w = u % (ku + vu);
     const bool is_k = w < ku;
     const int blk = is_k ? w : w - ku;
@@ -143,11 +148,10 @@ __global__ void __launch_bounds__(256) append_kv_kernel(const AppendParams p) {
 
 cudaError_t launch_append_kv(int kvt, const AppendParams& p, cudaStream_t s) {
   if (p.total_new == 0) return cudaSuccess;
-  const int units = p.Hkv * (p.d_qk + p.d_vo) / 16;
-  const int threads = units >= 256 ? 256 : ((units + 31) / 32) * 32;
-  if (kvt == KV_BF16) append_kv_kernel<KV_BF16><<<p.total_new, threads, 0, s>>>(p);
-  else if (kvt == KV_FP8) append_kv_kernel<KV_FP8><<<p.total_new, threads, 0, s>>>(p);
-  else if (kvt == KV_NVFP4) append_kv_kernel<KV_NVFP4><<<p.total_new, threads, 0, s>>>(p);
+  const int grid = (p.total_new + kAppendWarps - 1) / kAppendWarps, threads = 32 * kAppendWarps;
+  if (kvt == KV_BF16) append_kv_kernel<KV_BF16><<<grid, threads, 0, s>>>(p);
+  else if (kvt == KV_FP8) append_kv_kernel<KV_FP8><<<grid, threads, 0, s>>>(p);
+  else if (kvt == KV_NVFP4) append_kv_kernel<KV_NVFP4><<<grid, threads, 0, s>>>(p);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }
