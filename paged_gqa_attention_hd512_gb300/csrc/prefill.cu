@@ -50,7 +50,11 @@ cudaError_t launch_prefill_prep(int kvt, int dqk, int dvo, int copy, const Prefi
 template <int KVT, int DQK, int DVO, bool PAIR>
 static cudaError_t run_prefill(const PrefillLaunch& L) {
   using C = PrefillCfg<DQK, DVO, KVT, PAIR>;
-  auto kern = prefill_kernel<KVT, DQK, DVO, PAIR>;
+  // the bf16 kernel on one CTA per tile without a custom mask or padded pages: the
+  // instantiation without that code
+  const bool plain = KVT == KV_BF16 && !PAIR && L.p.mask == nullptr && L.p.box_rows == L.p.page_size;
+  auto kern = plain ? prefill_kernel<KVT, DQK, DVO, PAIR, !(KVT == KV_BF16 && !PAIR)>
+                    : prefill_kernel<KVT, DQK, DVO, PAIR, true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC);
   if (e != cudaSuccess) return e;
   // a programmatic dependent of the preparation kernel (pairs: clusters of two CTAs, one

@@ -451,7 +451,9 @@ __device__ __forceinline__ int prefill_item_at(int r) {
 }
 
 // tm_p (CTA pairs only): the P scratch as rows of 128 bytes, boxes of one 32 KB P tile
-template <int KVT, int DQK, int DVO, bool PAIR>
+// GEN: custom masks and small padded pages may occur (false: neither, their code is not
+// compiled in, which the plain causal / windowed calls run)
+template <int KVT, int DQK, int DVO, bool PAIR, bool GEN = true>
 __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_sfk,
@@ -1244,7 +1246,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       const int klo = p.window_left >= 0 ? pos - p.window_left : 0;
       const int hq = f.kvh * g + h_local;
       // custom mask: bit index of (this row, key 0)
-      const int64_t mbase = (p.mask != nullptr && row_ok)
+      const int64_t mbase = (GEN && p.mask != nullptr && row_ok)
                                 ? p.mask_indptr[f.b] * 8 + (int64_t)(f.q_begin + p_local) * f.kv_len
                                 : 0;
       float m_used = -INFINITY, l = 0.f;
@@ -1294,7 +1296,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
             // pages of fewer than 8 tokens, read from their copy padded to 8 rows: column i
             // of this thread is token tok0 + (i / 8) * page_size + i % 8 when i % 8 <
             // page_size and padding otherwise (at most 8 * 4 tokens per thread)
-            const bool padded = p.box_rows != ps;
+            const bool padded = GEN && p.box_rows != ps;
             const int tok0 = padded ? (f.jlo + jt) * p.tile_tok + (col0 >> 3) * ps : 0;
             // the row maximum over the visible keys of this thread's columns, masked scores
             // set to -inf; a tile every row of the warp sees in full skips the mask
@@ -1323,7 +1325,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
                 sr[i] = __float_as_uint(x);
                 mx4[i & 3] = fmaxf(mx4[i & 3], x);
               }
-            } else if (p.mask == nullptr) {
+            } else if (!GEN || p.mask == nullptr) {
               if (__all_sync(0xffffffffu, (lo <= 0) & (hi >= NCOL - 1))) plain_max();
               else mask_and_max(nullptr, false);
             } else {
