@@ -648,6 +648,7 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   p.kv_cache = static_cast<const uint8_t*>(kv_cache);
   p.sf = kv_scales ? kv_scales->sf : nullptr;
   p.out = static_cast<uint16_t*>(out);
+  p.out_v8 = aligned(out, 32) ? 1 : 0;
   p.lse = lse;
   p.err = reinterpret_cast<int*>(ws + kErrOffset);
   p.hdr = reinterpret_cast<int*>(ws + o_hdr);

@@ -122,6 +122,7 @@ struct PrefillParams {
   // tile_tok = 128 / box_rows * page_size tokens
   int box_rows;
   int tile_tok;
+  int out_v8;  // out is 32-byte aligned: the epilogue writes whole 32-byte sectors
   int swz;
   float sm_scale;
 };

@@ -374,12 +374,10 @@ struct PrefillItemInfo {
   int slot;  // split KV: partial slot of this item, -1 when it writes the output
 };
 
-// `rank`: which tile of a CTA pair's item this CTA computes (0 without pairs).  Both CTAs
-// of a pair walk the KV range of the whole item; the second tile may be empty (n_pos 0).
-// tile_list: the plan holds one 16-byte record per tile (sequence, first new token, cost),
-// item it being record it / Hkv with kv head it % Hkv; otherwise full item records.
-__device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams& p, int it, int rank,
-                                                             bool tile_list) {
+// The plan record of item it: one 16-byte record per tile (sequence, first new token,
+// cost), item it being record it / Hkv with kv head it % Hkv, when tile_list; otherwise
+// full item records.
+__device__ __forceinline__ PrefillItem prefill_item_record(const PrefillParams& p, int it, bool tile_list) {
   PrefillItem item;
   if (tile_list) {
     const int4 r = reinterpret_cast<const int4*>(p.items)[it / p.Hkv];
@@ -392,16 +390,41 @@ __device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams
   } else {
     item = p.items[it];
   }
+  return item;
+}
+
+// An item's record with the entries of its sequence's index arrays.
+struct PrefillItemRaw {
+  PrefillItem item;
+  int qo0, qo1, kv0, kv1, last;
+};
+
+__device__ __forceinline__ PrefillItemRaw prefill_item_raw(const PrefillParams& p, const PrefillItem& item) {
+  PrefillItemRaw w;
+  w.item = item;
+  w.qo0 = p.qo_indptr[item.b];
+  w.qo1 = p.qo_indptr[item.b + 1];
+  w.kv0 = p.kv_indptr[item.b];
+  w.kv1 = p.kv_indptr[item.b + 1];
+  w.last = p.kv_last_page_len[item.b];
+  return w;
+}
+
+// `rank`: which tile of a CTA pair's item this CTA computes (0 without pairs).  Both CTAs
+// of a pair walk the KV range of the whole item; the second tile may be empty (n_pos 0).
+__device__ __forceinline__ PrefillItemInfo prefill_item_finish(const PrefillParams& p, const PrefillItemRaw& w,
+                                                               int rank) {
+  const PrefillItem& item = w.item;
   PrefillItemInfo f;
   f.b = item.b;
   f.kvh = item.kvh;
   f.q_begin = item.q_begin + rank * p.rows_per_tile;
-  f.qo_len = p.qo_indptr[f.b + 1] - p.qo_indptr[f.b];
-  f.ip0 = p.kv_indptr[f.b];
-  f.np = p.kv_indptr[f.b + 1] - f.ip0;
-  f.kv_len = f.np > 0 ? (f.np - 1) * p.page_size + p.kv_last_page_len[f.b] : 0;
+  f.qo_len = w.qo1 - w.qo0;
+  f.ip0 = w.kv0;
+  f.np = w.kv1 - w.kv0;
+  f.kv_len = f.np > 0 ? (f.np - 1) * p.page_size + w.last : 0;
   f.n_pos = max(0, min(p.rows_per_tile, f.qo_len - f.q_begin));
-  f.q_row0 = p.qo_indptr[f.b] + f.q_begin;
+  f.q_row0 = w.qo0 + f.q_begin;
   f.pos0 = f.kv_len - f.qo_len + f.q_begin;
   const int ipos0 = f.kv_len - f.qo_len + item.q_begin;
   const int inpos = min(p.rows_per_tile * (p.pair ? 2 : 1), f.qo_len - item.q_begin);
@@ -418,6 +441,11 @@ __device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams
     f.nt = max(1, t1 - t0);
   }
   return f;
+}
+
+__device__ __forceinline__ PrefillItemInfo prefill_item_info(const PrefillParams& p, int it, int rank,
+                                                             bool tile_list) {
+  return prefill_item_finish(p, prefill_item_raw(p, prefill_item_record(p, it, tile_list)), rank);
 }
 
 // Bits [s, s + n) of a little-endian bit array (bit k of the result = bit s + k; n <= 0
@@ -449,6 +477,34 @@ __device__ __forceinline__ int prefill_item_at(int r) {
   const int off = (r & 1) ? n - 1 - u : u;
   return r * n + off;
 }
+
+// The items of this CTA (or CTA pair) in order.  The loads behind an item's info form a
+// chain (plan record, then its sequence's index arrays), which a role that fetched them at
+// the item boundary would wait out there, twice: so the record of item r + 2 and the index
+// entries of item r + 1 are fetched while item r runs, and only the arithmetic is left for
+// the boundary.
+template <bool PAIR>
+struct PrefillItemWalk {
+  int r = 0;
+  PrefillItemRaw next;  // item r + 1
+  PrefillItem rec;      // the record of item r + 2
+  __device__ __forceinline__ void start(const PrefillParams& p, int n_items, bool tile_list) {
+    const int i0 = prefill_item_at<PAIR>(0), i1 = prefill_item_at<PAIR>(1);
+    if (i0 < n_items) next = prefill_item_raw(p, prefill_item_record(p, i0, tile_list));
+    if (i1 < n_items) rec = prefill_item_record(p, i1, tile_list);
+  }
+  // false when the CTA has no item left; else the current item's info in f
+  __device__ __forceinline__ bool advance(const PrefillParams& p, int n_items, bool tile_list, int rank,
+                                          PrefillItemInfo& f) {
+    if (prefill_item_at<PAIR>(r) >= n_items) return false;
+    f = prefill_item_finish(p, next, rank);
+    if (prefill_item_at<PAIR>(r + 1) < n_items) next = prefill_item_raw(p, rec);
+    const int i2 = prefill_item_at<PAIR>(r + 2);
+    if (i2 < n_items) rec = prefill_item_record(p, i2, tile_list);
+    ++r;
+    return true;
+  }
+};
 
 // tm_p (CTA pairs only): the P scratch as rows of 128 bytes, boxes of one 32 KB P tile
 // GEN: custom masks and small padded pages may occur (false: neither, their code is not
@@ -565,12 +621,12 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     }
     uint32_t rc = 0, aux_phase = 0, qe = 0;
     const uint64_t pol_kv = l2_policy_evict_last(), pol_q = l2_policy_evict_first();
-    for (int r = 0;; ++r) {
-      const int it = prefill_item_at<C::PAIR>(r);
-      if (it >= n_items) break;
-      const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
+    PrefillItemWalk<C::PAIR> walk;
+    walk.start(p, n_items, tile_list);
+    for (;;) {
+      PrefillItemInfo f;
+      if (!walk.advance(p, n_items, tile_list, rank, f)) break;
       const bool reuse = item_reuse(f);
-      mbar_wait<C::PAIR>(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
       // Q part c (the columns of K chunk c), into its own barrier
       auto load_q_part = [&](int c) {
         if (lane != 0) return;
@@ -718,7 +774,10 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       // chunks in the MMA thread's order: K of step 0 (one CTA per tile: each chunk after its
       // Q part, so the port brings the first Q part and K chunk before the rest of Q), then
       // per step k: K of k + 1, V of k
+      // (the first pages are fetched before the wait for the Q region, so their loads run
+      // during it)
       int pg_a = step_pages(0), pg_b = step_pages(1);
+      mbar_wait<C::PAIR>(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
       if constexpr (C::PAIR) {
         for (int c = 0; c < C::NKC; ++c) load_q_part(c);
         emit(true, 0, pg_a);
@@ -755,10 +814,11 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     const uint8_t* pscr = p.p_scratch + (size_t)blockIdx.x * p.reuse_tiles * C::CHUNK;
     const uint64_t pol_p = l2_policy_evict_first();
     uint32_t np = 0, n_reuse = 0;
-    for (int r = 0;; ++r) {
-      const int it = prefill_item_at<C::PAIR>(r);
-      if (it >= n_items) break;
-      const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
+    PrefillItemWalk<C::PAIR> walk;
+    walk.start(p, n_items, tile_list);
+    for (;;) {
+      PrefillItemInfo f;
+      if (!walk.advance(p, n_items, tile_list, rank, f)) break;
       if (!item_reuse(f)) continue;
       mbar_wait<C::PAIR>(qreg_free, n_reuse & 1, p.err, SITE_PRE_Q);
       mbar_wait(ps_done, n_reuse & 1, p.err, SITE_PRE_P_FULL);
@@ -800,10 +860,11 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       const uint32_t stg = q_s + C::OFF_STG, sfb = q_s + C::OFF_SF;
       uint32_t n = 0, nsf = 0;
       int it_local = 0;
-      for (int r = 0;; ++r, ++it_local) {
-        const int it = prefill_item_at<C::PAIR>(r);
-        if (it >= n_items) break;
-        const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
+      PrefillItemWalk<C::PAIR> walk;
+      walk.start(p, n_items, tile_list);
+      for (;; ++it_local) {
+        PrefillItemInfo f;
+        if (!walk.advance(p, n_items, tile_list, rank, f)) break;
         mbar_wait(q_empty, (it_local & 1) ^ 1, p.err, SITE_PRE_Q);
         if (lane == 0)
           for (int c = 0; c < C::NKC; ++c) {
@@ -1134,10 +1195,11 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       ++np;
       if (j == 0) ++n_pass;
     };
-    for (int r = 0;; ++r, ++it_local) {
-      const int it = prefill_item_at<C::PAIR>(r);
-      if (it >= n_items) break;
-      const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
+    PrefillItemWalk<C::PAIR> walk;
+    walk.start(p, n_items, tile_list);
+    for (;; ++it_local) {
+      PrefillItemInfo f;
+      if (!walk.advance(p, n_items, tile_list, rank, f)) break;
       const bool reuse = item_reuse(f);
       const int steps = reuse ? f.nt : C::NPASS * f.nt;
       // QK(k + 1) runs while the softmax of step k works, then PV(k)
@@ -1233,6 +1295,8 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     // the first pass's P tiles are read back by the second pass of the same item: keep
     // them in L2 ahead of streaming data; the second pass reads them with evict-first
     const uint64_t pol_keep = l2_policy_evict_last();
+    // (the softmax warps fetch an item's info at its start: they wait for its first S
+    // anyway, and holding the next item's loads would cost them registers)
     for (int r = 0;; ++r, ++it_local) {
       const int it = prefill_item_at<C::PAIR>(r);
       if (it >= n_items) break;
@@ -1443,11 +1507,11 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
             tmem_ld32(lane_base + o_col + ocol0 + 32 * c, ov);
             tc_wait_ld();
             if (row_ok) {
-              float4* dst = reinterpret_cast<float4*>(prow + 32 * c);
+              // 32-byte stores: each writes a whole sector of the thread's row
 #pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(__uint_as_float(ov[4 * i]) * inv, __uint_as_float(ov[4 * i + 1]) * inv,
-                                     __uint_as_float(ov[4 * i + 2]) * inv, __uint_as_float(ov[4 * i + 3]) * inv);
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * inv);
+#pragma unroll
+              for (int i = 0; i < 4; ++i) st_global_v8(prow + 32 * c + 8 * i, ov + 8 * i, ov + 8 * i + 4);
             }
           }
           if (pass == C::NPASS - 1 && row_ok && wg == 0) p.part_lse[(size_t)f.slot * 128 + row] = row_lse;
@@ -1462,10 +1526,18 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
             for (int i = 0; i < 16; ++i)
               pkd[i] = pack_bf16x2(__uint_as_float(ov[2 * i]) * inv, __uint_as_float(ov[2 * i + 1]) * inv);
             if (row_ok) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+              // 32-byte stores where out allows them: a warp's instruction then writes 32
+              // whole sectors (the rows of a warp are 2 * DVO bytes apart, so 16-byte stores
+              // leave every sector half written and take twice the instructions)
+              if (p.out_v8) {
+                st_global_stream_v8(orow + 32 * c, pkd);
+                st_global_stream_v8(orow + 32 * c + 16, pkd + 8);
+              } else {
+                uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                st_global_stream_v4(dst + i, make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]));
+                for (int i = 0; i < 4; ++i)
+                  st_global_stream_v4(dst + i, make_uint4(pkd[4 * i], pkd[4 * i + 1], pkd[4 * i + 2], pkd[4 * i + 3]));
+              }
             }
           }
           if (pass == C::NPASS - 1 && row_ok && p.lse && wg == 0)

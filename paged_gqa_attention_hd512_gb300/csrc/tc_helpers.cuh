@@ -119,6 +119,12 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* a, const u
                "r"(a[3]), "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3])
                : "memory");
 }
+// 32-byte streaming store (evict-first): a whole sector per thread
+__device__ __forceinline__ void st_global_stream_v8(void* p, const uint32_t* a) {
+  asm volatile("st.global.cs.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a[0]), "r"(a[1]), "r"(a[2]),
+               "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7])
+               : "memory");
+}
 __device__ __forceinline__ void st_global_stream_v4(void* p, uint4 v) {
   asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");

@@ -103,6 +103,26 @@ def test_prefill_pairs_on_the_dequantised_copy(cta_mode, _dequant_limit):
     assert _variant() == f"prefill_512x256{cta_mode}_nvfp4_dequant"
 
 
+@pytest.mark.parametrize("dvo", [512, 256])
+def test_prefill_output_only_16_byte_aligned(dvo):
+    """out 16 but not 32 bytes aligned: the epilogue keeps to 16-byte stores (32-byte
+    stores need 32-byte addresses) and the rows land where they belong."""
+    import torch
+    ensure_built()
+    case = synth.make_case("prefill", batch=2, Hq=8, Hkv=2, d_qk=512, d_vo=dvo, page_size=16,
+                           kv_lens=[300, 70], qo_lens=[300, 70], seed=611)
+    n = case.total_q * case.Hq * dvo
+    buf = torch.zeros(n + 32, dtype=torch.bfloat16, device="cuda")
+    off = next(k for k in range(16) if (buf.data_ptr() + 2 * k) % 32 == 16)
+    out = buf[off:off + n].view(case.total_q, case.Hq, dvo)
+    pa.paged_attn_set_prefill_split_kv(0)  # the kernel writes out itself
+    try:
+        check_full(case, f"out at 16 mod 32, d_vo {dvo}", out=out)
+    finally:
+        pa.paged_attn_set_prefill_split_kv(-1)
+    assert not buf[:off].any() and not buf[off + n:].any(), "writes outside out"
+
+
 SMALL_PAGE_CASES = [
     # (dtype, dqk, dvo, Hq, Hkv, page_size, kv_lens, qo_lens, causal, window)
     (BF16, 512, 512, 8, 2, 1, [130, 33], [130, 33], 1, -1),
