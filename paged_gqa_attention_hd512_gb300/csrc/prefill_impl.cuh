@@ -771,22 +771,18 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
           }
         }
       };
-      // chunks in the MMA thread's order: K of step 0 (one CTA per tile: each chunk after its
-      // Q part, so the port brings the first Q part and K chunk before the rest of Q), then
-      // per step k: K of k + 1, V of k
+      // chunks in the MMA thread's order: K of step 0, then per step k: K of k + 1, V of k.
+      // One CTA per tile: warp 3 loads the Q tiles, so that the next item's Q is requested
+      // as soon as the Q region is free, not after this warp has queued the V chunks of the
+      // item's last steps (which wait for ring slots).  CTA pairs: Q here, before K.
       // (the first pages are fetched before the wait for the Q region, so their loads run
       // during it)
       int pg_a = step_pages(0), pg_b = step_pages(1);
-      mbar_wait<C::PAIR>(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
       if constexpr (C::PAIR) {
+        mbar_wait<C::PAIR>(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
         for (int c = 0; c < C::NKC; ++c) load_q_part(c);
-        emit(true, 0, pg_a);
-      } else {
-        for (int c = 0; c < C::NKC; ++c) {
-          load_q_part(c);
-          emit(true, 0, pg_a, c, c + 1);
-        }
       }
+      emit(true, 0, pg_a);
       for (int k = 0; k < steps; ++k) {
         const int pg_c = step_pages(k + 2);
         if (k + 1 < steps) emit(true, k + 1, pg_b);
@@ -796,7 +792,7 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
       }
       if (reuse) {
         // second pass: V of the upper output half (the P tiles come from warp 3)
-        mbar_wait<C::PAIR>(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
+        if constexpr (C::PAIR) mbar_wait<C::PAIR>(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
         int pg = step_pages(f.nt);
         for (int j = 0; j < f.nt; ++j) {
           const int pg_n = step_pages(f.nt + j + 1);
@@ -805,21 +801,39 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
         }
       }
     }
-  } else if (warp == 3 && C::NPASS == 2 && !C::QUANT) {
-    // ------------------------------------------- P tiles of second passes (lane 0 of warp 3)
-    // The first pass's P tiles of an item (usually back from HBM) go into the P slots of the
-    // Q region once the item's last QK is done and the softmax has written them; up to NPS
-    // tiles ahead of the PVs, independently of the V chunks in the ring.
+  } else if (warp == 3 && !C::QUANT && (C::NPASS == 2 || !C::PAIR)) {
+    // ------------------------------- Q tiles (one CTA per tile) and P tiles of second passes
+    // Q: each item's tile, in parts of the K chunks' dims on their own barriers, as soon as
+    // the previous item has released the Q region (its last QK, or its second pass).
+    // P: the first pass's P tiles of an item (usually back from HBM) go into the P slots of
+    // the Q region once the item's last QK is done and the softmax has written them; up to
+    // NPS tiles ahead of the PVs, independently of the V chunks in the ring.
     constexpr int NPS = C::NPS > 0 ? C::NPS : 1;
     const uint8_t* pscr = p.p_scratch + (size_t)blockIdx.x * p.reuse_tiles * C::CHUNK;
-    const uint64_t pol_p = l2_policy_evict_first();
-    uint32_t np = 0, n_reuse = 0;
+    const uint64_t pol_p = l2_policy_evict_first(), pol_q = l2_policy_evict_first();
+    uint32_t np = 0, n_reuse = 0, qe = 0;
     PrefillItemWalk<C::PAIR> walk;
     walk.start(p, n_items, tile_list);
     for (;;) {
       PrefillItemInfo f;
       if (!walk.advance(p, n_items, tile_list, rank, f)) break;
-      if (!item_reuse(f)) continue;
+      const bool reuse = item_reuse(f);
+      if constexpr (!C::PAIR) {
+        mbar_wait(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
+        if (lane == 0) {
+          const uint32_t qbytes = (uint32_t)(C::QB_PER * 128 * g * p.rows_per_tile);
+          for (int c = 0; c < C::NKC; ++c) {
+            mbar_arrive_expect_tx(&q_part[c], qbytes);
+            for (int b = c * C::QB_PER; b < (c + 1) * C::QB_PER; ++b)
+              tma_load_3d_hint(q_s + b * C::HALF, &tm_q, b * 128, f.kvh * g, f.q_row0, &q_part[c], pol_q);
+          }
+        }
+        __syncwarp();
+        // an item that reuses P releases the Q region twice: after its last QK (the P slots
+        // may fill) and after its second pass (the next Q may load)
+        if (reuse) mbar_wait(q_empty, (qe++ & 1) ^ 1, p.err, SITE_PRE_Q);
+      }
+      if (!reuse) continue;
       mbar_wait<C::PAIR>(qreg_free, n_reuse & 1, p.err, SITE_PRE_Q);
       mbar_wait(ps_done, n_reuse & 1, p.err, SITE_PRE_P_FULL);
       ++n_reuse;
@@ -1295,12 +1309,17 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
     // the first pass's P tiles are read back by the second pass of the same item: keep
     // them in L2 ahead of streaming data; the second pass reads them with evict-first
     const uint64_t pol_keep = l2_policy_evict_last();
-    // (the softmax warps fetch an item's info at its start: they wait for its first S
-    // anyway, and holding the next item's loads would cost them registers)
+    // bf16 KV: the next item's info is fetched in the last epilogue of the current one,
+    // while it waits for the last PV (holding it through the softmax loop would cost
+    // registers).  Quantised KV (one softmax warpgroup, more registers a thread): at the
+    // item's start.
+    int it_next = prefill_item_at<C::PAIR>(0);
+    PrefillItemInfo f_next;
+    if (!C::QUANT && it_next < n_items) f_next = prefill_item_info(p, it_next, rank, tile_list);
     for (int r = 0;; ++r, ++it_local) {
-      const int it = prefill_item_at<C::PAIR>(r);
-      if (it >= n_items) break;
-      const PrefillItemInfo f = prefill_item_info(p, it, rank, tile_list);
+      if (it_next >= n_items) break;
+      if constexpr (C::QUANT) f_next = prefill_item_info(p, it_next, rank, tile_list);
+      const PrefillItemInfo f = f_next;
       const bool reuse = item_reuse(f);
       const int tag = it_local + 1;
       const int p_local = row / g, h_local = row % g;
@@ -1490,6 +1509,10 @@ __global__ void __launch_bounds__(PrefillCfg<DQK, DVO, KVT, PAIR>::THREADS, 1)
         // ---- epilogue of this pass: O / l -> bf16
         static_assert(C::NPASS == 1 || C::QUANT || C::SMW == 2, "P reuse orders the rescale tags through the warpgroups' barrier");
         const float lt = combine(l, false);
+        if (pass == C::NPASS - 1) {
+          it_next = prefill_item_at<C::PAIR>(r + 1);
+          if (!C::QUANT && it_next < n_items) f_next = prefill_item_info(p, it_next, rank, tile_list);
+        }
         mbar_wait<C::PAIR>(o_done, n_epi & 1, p.err, SITE_PRE_O_DONE);
         ++n_epi;
         __syncwarp();
