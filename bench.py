@@ -345,8 +345,13 @@ def bench_decode(name, steps, warmup, barrier, gpu_index, pk, with_e2e=True, wit
         raise RuntimeError("device error word set after the first decode call")
     nbytes = decode_bytes(c)
     with ClockSampler(gpu_index) as clk:
-        pa.paged_attn_profile_begin(steps)
+        # the steps as a user makes them; then the same steps again with the library's
+        # events around the decode kernel for its own duration (an event between the
+        # planner and the kernel keeps the kernel from starting under the planner's tail,
+        # so those steps are not the ones the value reports)
         ms = time_region(step, steps, warmup, barrier)
+        pa.paged_attn_profile_begin(steps)
+        time_region(step, steps, 0, barrier)
         n_k, k_ms = pa.paged_attn_profile_end()
     clocks = clk.summary()
     variant = pa.paged_attn_last_variant()
@@ -475,16 +480,25 @@ def _bench_prefill(pa, name, steps, warmup, gpu_index, pk, with_cpu, with_e2e):
         for _ in range(warmup):
             step()
         torch.cuda.synchronize()
+
+        def timed_steps():
+            tot = 0.0
+            for _ in range(steps):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                step()
+                e1.record(s)
+                e1.synchronize()
+                tot += e0.elapsed_time(e1)
+            return tot
+
+        # the calls as a user makes them, then again with the library's events around the
+        # prefill kernel for its own duration (an event between the preparation kernel and
+        # the prefill kernel keeps the latter from starting under the former's tail)
+        tot = timed_steps()
         pa.paged_attn_profile_begin(steps)
-        tot = 0.0
-        for _ in range(steps):
-            flush.fill_(1)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(s)
-            step()
-            e1.record(s)
-            e1.synchronize()
-            tot += e0.elapsed_time(e1)
+        timed_steps()
         n_k, k_ms = pa.paged_attn_profile_end()
     ms = tot / steps
     kern_ms = k_ms / max(1, n_k)
