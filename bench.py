@@ -605,6 +605,8 @@ def main():
     ap.add_argument("--workload", default=MAIN, help="decode workload of the main line")
     ap.add_argument("--prefill-only", action="store_true", help="time only the prefill workload (profiling)")
     ap.add_argument("--prefill-workload", default=PREFILL, help="prefill workload of --prefill-only")
+    ap.add_argument("--append-only", choices=sorted(APPEND_WORKLOADS), default=None,
+                    help="time only this append workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -637,6 +639,11 @@ def main():
         res = bench_prefill(args.prefill_workload, psteps, args.warmup, local, pk)
         if rank == 0:
             print(json.dumps({"prefill": res}), flush=True)
+        return 0
+    if args.append_only:
+        res = bench_append(args.append_only, max(3, args.steps // 10), args.warmup, local, pk)
+        if rank == 0:
+            print(json.dumps({"append": res}), flush=True)
         return 0
     main_res = bench_decode(args.workload, args.steps, args.warmup, barrier, local, pk,
                             with_e2e=not args.no_e2e, with_cpu=(rank == 0 and not args.no_cpu))

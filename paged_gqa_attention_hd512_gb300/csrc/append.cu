@@ -43,13 +43,10 @@ __device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float a, float b) {
       : "f"(b), "f"(a));
   return r;
 }
-// one code with the sign of v (also for results that round to zero), magnitude RNE and
+// one e4m3 code with the sign of v (also for a magnitude that rounds to zero), RNE and
 // saturating
 __device__ __forceinline__ uint32_t e4m3_code(float v) {
   return (f32x2_to_e4m3x2(fabsf(v), 0.f) & 0x7Fu) | ((__float_as_uint(v) >> 24) & 0x80u);
-}
-__device__ __forceinline__ uint32_t e2m1_code(float v) {
-  return (f32x2_to_e2m1x2(fabsf(v), 0.f) & 0x7u) | ((__float_as_uint(v) >> 28) & 0x8u);
 }
 __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
   const uint32_t h2 = e4m3x2_to_f16x2(code & 0xFFu);
@@ -121,9 +118,12 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kv_kernel(const Appe
       }
       const float scale = is_k ? ks : vs;
       if constexpr (KVT == KV_FP8) {
+        // two codes per conversion (the conversion keeps the operand's sign, also on a
+        // magnitude that rounds to zero)
         uint32_t o[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-        for (int k = 0; k < 16; ++k) o[k >> 2] |= e4m3_code(__fdiv_rn(x[k], scale)) << (8 * (k & 3));
+        for (int k = 0; k < 8; ++k)
+          o[k >> 1] |= f32x2_to_e4m3x2(__fdiv_rn(x[2 * k], scale), __fdiv_rn(x[2 * k + 1], scale)) << (16 * (k & 1));
         *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
       } else {
         float amax = 0.f;
@@ -134,7 +134,8 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kv_kernel(const Appe
         uint32_t o[2] = {0u, 0u};
         if (d != 0.f) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) o[k >> 3] |= e2m1_code(__fdiv_rn(x[k], d)) << (4 * (k & 7));
+          for (int k = 0; k < 8; ++k)
+            o[k >> 2] |= f32x2_to_e2m1x2(__fdiv_rn(x[2 * k], d), __fdiv_rn(x[2 * k + 1], d)) << (8 * (k & 3));
         }
         *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
         uint8_t* sfp = p.sf + (size_t)page * sf_page + (is_k ? row * ku : rows * ku + row * vu) + blk;

@@ -165,3 +165,26 @@ def test_append_nvfp4_quotients_at_rounding_midpoints(k_off):
         assert code == 0 and skipped == 0
         _assert_bytes_equal(cache, ref_cache, f"midpoint {mid} offset {k_off}")
         _assert_bytes_equal(sf, ref_sf, f"scales, midpoint {mid} offset {k_off}")
+
+
+@pytest.mark.parametrize("dt", [ac.FP8, ac.NVFP4])
+def test_append_codes_that_round_to_zero_keep_their_sign(dt):
+    """Values far below the smallest nonzero code (with the scale, or the block's largest
+    value, fixed by one element): the codes are zero with the operand's sign, as the
+    oracle writes them (e4m3 0x80, e2m1 0x8 for the negative ones)."""
+    ensure_built()
+    case = ac.make(kv_lens=[3], n_new=[1], Hkv=1, d_qk=256, d_vo=256, page_size=8, kv_dtype=dt,
+                   seed=71, k_scale=1.0, v_scale=1.0)
+    tiny = [2.0 ** -14, -(2.0 ** -14), 2.0 ** -20, -(2.0 ** -20), -(2.0 ** -12), 2.0 ** -12, -0.0, 0.0]
+    for t in (case.k_new, case.v_new):
+        t[0, 0, :] = 0.0
+        t[0, 0, 0] = 4.0  # the block maximum (NVFP4) and one ordinary code
+        for k, v in enumerate(tiny):
+            t[0, 0, 1 + k] = v
+            t[0, 0, 17 + k] = v  # a block of tiny values only (NVFP4: its scale rounds to 0)
+    cache, sf, code = _run_gpu(case)
+    ref_cache, ref_sf, skipped = _oracle(case)
+    assert code == 0 and skipped == 0
+    _assert_bytes_equal(cache, ref_cache, "codes that round to zero")
+    if dt == ac.NVFP4:
+        _assert_bytes_equal(sf, ref_sf, "scale pool")
