@@ -53,6 +53,26 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
   return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 
+// a / b rounded to nearest even, from y = RN(1/b): the estimate a*y (within two units in
+// the last place of a/b) corrected twice by exact FMA residuals.  Markstein's theorem (P.
+// Markstein, "Computation of elementary functions on the IBM RISC System/6000 processor",
+// IBM J. Res. Develop. 34, 1990): with y the correctly rounded reciprocal of b and q within
+// one unit in the last place of a/b, RN(q + (a - b q) y) is the correctly rounded a/b; the
+// first correction brings the estimate within that unit.  It holds while a, b, y and the
+// quotient stay in the normal range and finite; callers take the IEEE division otherwise.
+// Below the normal range the result keeps the sign and stays below it, which is all a
+// code of e4m3 or e2m1 (whose smallest step is far above it) depends on there.
+// The corrections turn a zero quotient into +0 (the residual of -0 is +0), so the result
+// takes the sign of the first estimate, which is the sign of a/b (also when it rounds to
+// zero).
+__device__ __forceinline__ float quot_recip(float a, float b, float y) {
+  const float q0 = __fmul_rn(a, y);
+  const float q1 = __fmaf_rn(__fmaf_rn(-q0, b, a), y, q0);
+  return copysignf(__fmaf_rn(__fmaf_rn(-q1, b, a), y, q1), q0);
+}
+// |b| in the range where b, 1/b and quotients of bounded magnitude stay normal
+__device__ __forceinline__ bool recip_ok(float b) { return fabsf(b) >= 0x1p-100f && fabsf(b) <= 0x1p100f; }
+
 constexpr int kAppendWarps = 8;  // new tokens per CTA, one per warp
 
 template <int KVT>
@@ -95,6 +115,11 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kv_kernel(const Appe
     ks = __ldg(p.k_scale);
     vs = __ldg(p.v_scale);
   }
+  // FP8: the reciprocal of each per-tensor scale, and the largest |x| below which x / scale
+  // stays under 2^100 (0: always the IEEE division)
+  const float yk = __frcp_rn(ks), yv = __frcp_rn(vs);
+  const float lim_k = recip_ok(ks) ? fminf(0x1p100f * fabsf(ks), 0x1p100f) : 0.f;
+  const float lim_v = recip_ok(vs) ? fminf(0x1p100f * fabsf(vs), 0x1p100f) : 0.f;
   for (int u = lane; u < units; u += 32) {
     const int h = u / (ku + vu), w = u % (ku + vu);
     const bool is_k = w < ku;
@@ -119,11 +144,24 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kv_kernel(const Appe
       const float scale = is_k ? ks : vs;
       if constexpr (KVT == KV_FP8) {
         // two codes per conversion (the conversion keeps the operand's sign, also on a
-        // magnitude that rounds to zero)
-        uint32_t o[4] = {0u, 0u, 0u, 0u};
+        // magnitude that rounds to zero).  The unit's largest magnitude (bf16 bits, NaN
+        // above infinity) decides between the reciprocal form and the IEEE division.
+        uint32_t mb = 0u;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          o[k >> 1] |= f32x2_to_e4m3x2(__fdiv_rn(x[2 * k], scale), __fdiv_rn(x[2 * k + 1], scale)) << (16 * (k & 1));
+        for (int k = 0; k < 8; ++k) mb = __vmaxu2(mb, wv[k] & 0x7FFF7FFFu);
+        const float amax = bf16_to_f32(max(mb & 0xFFFFu, mb >> 16));
+        uint32_t o[4] = {0u, 0u, 0u, 0u};
+        if (amax < (is_k ? lim_k : lim_v)) {
+          const float y = is_k ? yk : yv;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            o[k >> 1] |= f32x2_to_e4m3x2(quot_recip(x[2 * k], scale, y), quot_recip(x[2 * k + 1], scale, y))
+                         << (16 * (k & 1));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            o[k >> 1] |= f32x2_to_e4m3x2(__fdiv_rn(x[2 * k], scale), __fdiv_rn(x[2 * k + 1], scale)) << (16 * (k & 1));
+        }
         *reinterpret_cast<uint4*>(dst) = make_uint4(o[0], o[1], o[2], o[3]);
       } else {
         float amax = 0.f;
@@ -133,9 +171,18 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kv_kernel(const Appe
         const float d = __fmul_rn(e4m3_to_f32(sf_code), scale);
         uint32_t o[2] = {0u, 0u};
         if (d != 0.f) {
+          // |x / d| <= amax / d, about 6 unless the block scale saturated at the e4m3
+          // maximum: the reciprocal form while d is in range and amax / d <= 2^100
+          if (recip_ok(d) && amax <= fminf(0x1p100f, 0x1p100f * fabsf(d))) {
+            const float y = __frcp_rn(d);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            o[k >> 2] |= f32x2_to_e2m1x2(__fdiv_rn(x[2 * k], d), __fdiv_rn(x[2 * k + 1], d)) << (8 * (k & 3));
+            for (int k = 0; k < 8; ++k)
+              o[k >> 2] |= f32x2_to_e2m1x2(quot_recip(x[2 * k], d, y), quot_recip(x[2 * k + 1], d, y)) << (8 * (k & 3));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              o[k >> 2] |= f32x2_to_e2m1x2(__fdiv_rn(x[2 * k], d), __fdiv_rn(x[2 * k + 1], d)) << (8 * (k & 3));
+          }
         }
         *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
         uint8_t* sfp = p.sf + (size_t)page * sf_page + (is_k ? row * ku : rows * ku + row * vu) + blk;
