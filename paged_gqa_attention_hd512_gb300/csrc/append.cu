@@ -120,14 +120,28 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kv_kernel(const Appe
   const float yk = __frcp_rn(ks), yv = __frcp_rn(vs);
   const float lim_k = recip_ok(ks) ? fminf(0x1p100f * fabsf(ks), 0x1p100f) : 0.f;
   const float lim_v = recip_ok(vs) ? fminf(0x1p100f * fabsf(vs), 0x1p100f) : 0.f;
+  // the 32 input bytes of unit u
+  auto src_of = [&](int u) -> const uint4* {
+    const int h = u / (ku + vu), w = u % (ku + vu);
+    return reinterpret_cast<const uint4*>(w < ku ? p.k_new + ((size_t)i * p.Hkv + h) * p.d_qk + w * 16
+                                                 : p.v_new + ((size_t)i * p.Hkv + h) * p.d_vo + (w - ku) * 16);
+  };
+  // each lane's next unit is loaded before the current one is converted, so two units'
+  // loads of each warp are in flight (the kernel waits on memory latency otherwise)
+  uint4 a_n = make_uint4(0, 0, 0, 0), c_n = a_n;
+  if (lane < units) {
+    a_n = __ldg(src_of(lane));
+    c_n = __ldg(src_of(lane) + 1);
+  }
   for (int u = lane; u < units; u += 32) {
     const int h = u / (ku + vu), w = u % (ku + vu);
     const bool is_k = w < ku;
     const int blk = is_k ? w : w - ku;
-    const uint16_t* src = is_k ? p.k_new + ((size_t)i * p.Hkv + h) * p.d_qk + blk * 16
-                               : p.v_new + ((size_t)i * p.Hkv + h) * p.d_vo + blk * 16;
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
-    const uint4 c = __ldg(reinterpret_cast<const uint4*>(src) + 1);
+    const uint4 a = a_n, c = c_n;
+    if (u + 32 < units) {
+      a_n = __ldg(src_of(u + 32));
+      c_n = __ldg(src_of(u + 32) + 1);
+    }
     const size_t row = (size_t)h * p.page_size + slot;
     uint8_t* dst = page_base + (is_k ? row * k_row : rows * k_row + row * v_row) + (size_t)blk * 16 * X2 / 2;
     if constexpr (KVT == KV_BF16) {
