@@ -74,6 +74,7 @@ def prefill_launches(variant: str) -> int:
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 DECODE_SOURCES = ("decode_impl.cuh", "common.cuh", "decode_inst.cuh", "kernel_params.h")
 PREFILL_SOURCES = ("prefill_impl.cuh", "common.cuh", "tc_helpers.cuh", "kernel_params.h")
+APPEND_SOURCES = ("append.cu", "common.cuh", "kernel_params.h")
 
 
 # ------------------------------------------------------------------------- work counts
@@ -579,12 +580,15 @@ def bench_append(name, steps, warmup, gpu_index, pk):
         n_k, k_ms = pa.paged_attn_profile_end()
     kern_ms = k_ms / max(1, n_k)
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    digest = sources_digest(APPEND_SOURCES)
     res = {"workload": name, "ms_per_step": ms / steps, "value": nbytes / (ms / steps * 1e-3) / 1e9, "unit": "GB/s",
            "bytes_per_step": nbytes, "variant": pa.paged_attn_last_variant(), "clocks": clk.summary(),
            "l2": f"{nbytes / 1e6:.0f} MB per step, larger than L2", "gpu_launches": steps,
            "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk[0]["hbm_gbs"], "unit": "GB/s",
-                        "frac": achieved / pk[0]["hbm_gbs"], "traffic": None, "kernel": "append_kv_kernel",
-                        "kernel_ms": kern_ms, "launches_timed": n_k, "peak_source": f"{pk[1]} hbm_gbs"}}
+                        "frac": achieved / pk[0]["hbm_gbs"],
+                        "traffic": traffic_record("append_kv_kernel", name, digest), "kernel": "append_kv_kernel",
+                        "kernel_ms": kern_ms, "launches_timed": n_k, "peak_source": f"{pk[1]} hbm_gbs",
+                        "source_digest": digest}}
     del k_new, v_new, cache, sf
     torch.cuda.empty_cache()
     return res
