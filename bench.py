@@ -356,10 +356,12 @@ def bench_decode(name, steps, warmup, barrier, gpu_index, pk, with_e2e=True, wit
         n_k, k_ms = pa.paged_attn_profile_end()
     clocks = clk.summary()
     variant = pa.paged_attn_last_variant()
+    # planner, decode kernel and merge; the decode kernel alone on the single-launch path
+    launches = (1 if variant.endswith("_direct") else 3) * steps
     res = {"workload": name, "config": {"workload": DESCRIBE.get(name, name), "name": name},
            "ms_per_step": ms / steps, "value": nbytes / (ms / steps * 1e-3) / 1e9,
            "unit": "GB/s", "bytes_per_step": nbytes, "steps": steps, "clocks": clocks, "variant": variant,
-           "gpu_launches": 3 * steps}  # planner, decode kernel, merge
+           "gpu_launches": launches}
     kern_ms = k_ms / max(1, n_k)
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
     digest = sources_digest(DECODE_SOURCES)

@@ -250,6 +250,16 @@ int paged_attn_debug_set_error_word(int target, int code);
  * The device still widens chunks when the workspace bound requires it.  Process-wide. */
 int paged_attn_set_decode_chunk_pages(int pages);
 
+/* Single-launch decode.  A decode call whose (sequence, kv head) items number at most the
+ * device's SMs and whose page pool holds at most 256 KiB of K and V per kv head runs as one
+ * kernel: each item covers its sequence's whole visible range and writes its rows
+ * directly, without the planner and merge launches (the split-K scheme of "[None][feat]
+ * Run Gemma4 head_dim 512 attention on Triton", Approach, pays off only where there is
+ * KV to split).  mode -1 = that rule (the default), 0 = never, 1 = whenever the items fit
+ * one round (a test hook).  A forced chunk size (paged_attn_set_decode_chunk_pages) turns
+ * it off.  Process-wide.  Returns PA_OK or PA_ERR_INVALID_ARG. */
+int paged_attn_set_decode_direct(int mode);
+
 /* Largest bf16 copy (bytes) of FP8 / NVFP4 pages that paged_attn_prefill may build in its
  * workspace; 0 = always convert inside the prefill kernel, negative = the default (4 GiB).
  * Process-wide.  Returns PA_OK. */

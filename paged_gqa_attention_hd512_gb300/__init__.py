@@ -29,7 +29,7 @@ PA_NOALLOC_SCRATCH_BYTES = 32 << 20
 # every symbol include/paged_attn.h declares
 EXPORTED = ("paged_attn_decode", "paged_attn_prefill", "paged_attn_status_string",
             "paged_attn_release_workspace", "paged_attn_check_device_error",
-            "paged_attn_set_decode_chunk_pages", "paged_attn_last_variant",
+            "paged_attn_set_decode_chunk_pages", "paged_attn_set_decode_direct", "paged_attn_last_variant",
             "paged_attn_profile_begin", "paged_attn_profile_end", "paged_attn_decode_noalloc",
             "paged_attn_set_prefill_dequant_limit", "paged_attn_set_prefill_cta_pairs",
             "paged_attn_append_kv", "paged_attn_prefill_custom_mask", "paged_attn_set_prefill_split_kv",
@@ -80,6 +80,8 @@ def load(path: Optional[str] = None):
     lib.paged_attn_debug_set_error_word.argtypes = [i32, i32]
     lib.paged_attn_set_decode_chunk_pages.restype = i32
     lib.paged_attn_set_decode_chunk_pages.argtypes = [i32]
+    lib.paged_attn_set_decode_direct.restype = i32
+    lib.paged_attn_set_decode_direct.argtypes = [i32]
     lib.paged_attn_set_prefill_dequant_limit.restype = i32
     lib.paged_attn_set_prefill_dequant_limit.argtypes = [ctypes.c_longlong]
     lib.paged_attn_set_prefill_cta_pairs.restype = i32
@@ -267,6 +269,14 @@ def paged_attn_set_decode_chunk_pages(pages: int) -> None:
     st = load().paged_attn_set_decode_chunk_pages(pages)
     if st != PA_OK:
         raise PagedAttnError(st, "paged_attn_set_decode_chunk_pages")
+
+
+def paged_attn_set_decode_direct(mode: int) -> None:
+    """Single-launch decode: -1 where the library's rule applies (default), 0 never, 1
+    whenever every (sequence, kv head) item fits one round of CTAs."""
+    st = load().paged_attn_set_decode_direct(mode)
+    if st != PA_OK:
+        raise PagedAttnError(st, "paged_attn_set_decode_direct")
 
 
 def paged_attn_set_prefill_dequant_limit(nbytes: int) -> None:

@@ -1,7 +1,7 @@
 """Compile the CUDA library (libpaged_attn.so) in-tree for sm_103a.
 
 Every translation unit under csrc/ is compiled in parallel with nvcc, then linked into
-_build/libpaged_attn.so (CUDA runtime linked statically; the driver's tensor-map encoder
+_build/libpaged_attn.so (CUDA runtime linked statically; the CUDA driver API's tensor-map encoder
 is resolved at run time through the runtime's entry-point query, so no -lcuda).
 """
 

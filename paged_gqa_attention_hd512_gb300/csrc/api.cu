@@ -45,6 +45,7 @@ void prof_mark(cudaStream_t s, bool begin) {
   }
 }
 int g_forced_chunk_pages = 0;
+int g_decode_direct = -1;  // -1: single-launch decode where it applies, 0: never, 1: whenever every item fits one round
 std::mutex g_ws_mutex;
 
 constexpr int kMaxDevices = 64;
@@ -177,6 +178,18 @@ int decode_min_chunk_pages(int kvt, int dqk, int dvo, int page_size) {
   const long row = (long)(dqk + dvo) * x2_of(kvt) / 2 + (kvt == KV_NVFP4 ? (dqk + dvo) / 16 : 0);
   const long page = row * page_size;
   return (int)std::max(1l, ((4l << 20) + page - 1) / page);
+}
+
+// A decode call small enough for one launch: every (sequence, kv head) item gets its own
+// CTA in a single round, and even a single sequence holding the whole pool would cost its
+// CTA little (about 6 us) against the planner and merge launches it saves (at most
+// 256 KiB of K and V per kv head in the pool).
+bool decode_direct(int kvt, int dqk, int dvo, int page_size, long long num_pages, int batch, int hkv, int sms) {
+  if (g_decode_direct == 0 || g_forced_chunk_pages > 0) return false;
+  if ((long long)batch * hkv > sms) return false;
+  if (g_decode_direct == 1) return true;
+  const double per_elem = kvt == PA_KV_BF16 ? 2.0 : (kvt == PA_KV_FP8_E4M3 ? 1.0 : 0.5 + 1.0 / 16.0);
+  return (double)num_pages * page_size * (dqk + dvo) * per_elem <= 256.0 * 1024.0;
 }
 
 // Checks shared by both phases.  Returns PA_OK or an error status.
@@ -364,6 +377,12 @@ int paged_attn_set_prefill_split_kv(int mode) {
   return PA_OK;
 }
 
+int paged_attn_set_decode_direct(int mode) {
+  if (mode < -1 || mode > 1) return PA_ERR_INVALID_ARG;
+  g_decode_direct = mode;
+  return PA_OK;
+}
+
 int paged_attn_set_decode_chunk_pages(int pages) {
   if (pages < 0) return PA_ERR_INVALID_ARG;
   g_forced_chunk_pages = pages;
@@ -475,7 +494,8 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
                         num_kv_heads, head_dim_qk, head_dim_vo, page_size, kv_dtype, box_rows, swz))
     return PA_ERR_CUDA;
 
-  const int grid = sms;
+  const bool direct = decode_direct(kv_dtype, head_dim_qk, head_dim_vo, page_size, num_pages, batch, num_kv_heads, sms);
+  const int grid = direct ? std::min(sms, batch * num_kv_heads) : sms;
   const int forced = g_forced_chunk_pages;
   const int target = forced > 0 ? 2048 : (16 * grid + num_kv_heads - 1) / num_kv_heads;
   const int max_chunks = target + batch;
@@ -517,11 +537,12 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
   p.box_rows = box_rows;
   p.box_shift = __builtin_ctz((unsigned)box_rows);
   p.swz = swz ? 7 : 0;
+  p.direct = direct ? 1 : 0;
   p.sm_scale = sm_scale;
   L.grid = grid;
   L.stream = static_cast<cudaStream_t>(stream);
 
-  if (launch_decode_plan(p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (!direct && launch_decode_plan(p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
   const char* name = "?";
   cudaError_t e;
   prof_mark(L.stream, true);
@@ -530,9 +551,9 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
   else e = launch_decode_nvfp4(head_dim_qk, head_dim_vo, hp, L, &name);
   prof_mark(L.stream, false);
   if (e != cudaSuccess) return PA_ERR_CUDA;
-  if (launch_decode_merge(head_dim_vo, p, L.grid, L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (!direct && launch_decode_merge(head_dim_vo, p, L.grid, L.stream) != cudaSuccess) return PA_ERR_CUDA;
   static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};
-  std::snprintf(g_variant, sizeof g_variant, "%s_%s", name, kv_names[kv_dtype]);
+  std::snprintf(g_variant, sizeof g_variant, "%s_%s%s", name, kv_names[kv_dtype], direct ? "_direct" : "");
   return PA_OK;
 }
 
@@ -826,7 +847,8 @@ extern "C" int paged_attn_decode_noalloc(const void* q, const void* kv_cache, co
   if (fixed >= cap) return PA_ERR_SCRATCH;
   const long fit = (long)((cap - fixed) / per_chunk) - batch;
   const int forced = g_forced_chunk_pages;
-  const int grid = sms;
+  const bool direct = decode_direct(kv_dtype, head_dim_qk, head_dim_vo, page_size, num_pages, batch, num_kv_heads, sms);
+  const int grid = direct ? std::min(sms, batch * num_kv_heads) : sms;
   const long usual = forced > 0 ? 2048 : (16 * grid + num_kv_heads - 1) / num_kv_heads;
   const long target = fit < usual ? fit : usual;
   if (target < 1) return PA_ERR_SCRATCH;
@@ -884,9 +906,10 @@ extern "C" int paged_attn_decode_noalloc(const void* q, const void* kv_cache, co
   p.box_rows = box_rows;
   p.box_shift = __builtin_ctz((unsigned)box_rows);
   p.swz = swz ? 7 : 0;
+  p.direct = direct ? 1 : 0;
   p.sm_scale = sm_scale;
 
-  if (launch_decode_plan(p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (!direct && launch_decode_plan(p, L.stream) != cudaSuccess) return PA_ERR_CUDA;
   const char* name = "?";
   cudaError_t e;
   prof_mark(L.stream, true);
@@ -895,8 +918,8 @@ extern "C" int paged_attn_decode_noalloc(const void* q, const void* kv_cache, co
   else e = launch_decode_nvfp4(head_dim_qk, head_dim_vo, hp, L, &name);
   prof_mark(L.stream, false);
   if (e != cudaSuccess) return PA_ERR_CUDA;
-  if (launch_decode_merge(head_dim_vo, p, L.grid, L.stream) != cudaSuccess) return PA_ERR_CUDA;
+  if (!direct && launch_decode_merge(head_dim_vo, p, L.grid, L.stream) != cudaSuccess) return PA_ERR_CUDA;
   static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};
-  std::snprintf(g_variant, sizeof g_variant, "%s_%s_noalloc", name, kv_names[kv_dtype]);
+  std::snprintf(g_variant, sizeof g_variant, "%s_%s%s_noalloc", name, kv_names[kv_dtype], direct ? "_direct" : "");
   return PA_OK;
 }

@@ -232,6 +232,24 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(DecodeParams p) {
 }
 #endif  // PA_DECODE_AUX
 
+// The chunk of decode item it: from the planner's list, or (direct calls) the whole
+// visible page range of sequence it / Hkv, as the planner would give it in one chunk.
+__device__ __forceinline__ DecodeChunk decode_item_chunk(const DecodeParams& p, int it) {
+  if (!p.direct) return p.chunks[it / p.Hkv];
+  DecodeChunk c;
+  c.b = it / p.Hkv;
+  c.split = 0;
+  const int np = p.kv_indptr[c.b + 1] - p.kv_indptr[c.b];
+  int first = 0;
+  if (np > 0 && p.window_left >= 0) {
+    const int kv_len = (np - 1) * p.page_size + p.kv_last_page_len[c.b];
+    first = max(0, kv_len - 1 - p.window_left) / p.page_size;
+  }
+  c.page_begin = first;
+  c.page_end = max(np, 0);
+  return c;
+}
+
 // ----------------------------------------------------------------------------- merge
 // out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s,  lse = ln2 * (M + log2 L).
 // One (row, 128-column quarter) unit of the merge, by one warp.
@@ -393,7 +411,7 @@ __global__ void __launch_bounds__(288, 1)
   }
   __syncthreads();
   grid_dep_wait();  // the planner of this call is complete
-  const int n_items = p.hdr[0] * p.Hkv;
+  const int n_items = p.direct ? p.batch * p.Hkv : p.hdr[0] * p.Hkv;
   const int ps = p.page_size;
 
   if (warp == 8) {
@@ -408,7 +426,7 @@ __global__ void __launch_bounds__(288, 1)
     const int br = p.box_rows;
     uint32_t g = 0;
     for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-      const DecodeChunk ch = p.chunks[it / p.Hkv];
+      const DecodeChunk ch = decode_item_chunk(p, it);
       const int kvh = it % p.Hkv;
       const int ip0 = p.kv_indptr[ch.b];
       const int np = p.kv_indptr[ch.b + 1] - ip0;
@@ -457,7 +475,7 @@ __global__ void __launch_bounds__(288, 1)
   uint32_t g = 0;
 
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const DecodeChunk ch = p.chunks[it / p.Hkv];
+    const DecodeChunk ch = decode_item_chunk(p, it);
     const int kvh = it % p.Hkv;
     const int b = ch.b;
     const int ip0 = p.kv_indptr[b];
@@ -776,8 +794,10 @@ __global__ void __launch_bounds__(288, 1)
     }
 
     // ---- epilogue: the final row (single chunk) or a partial (O, m, l)
-    const int2 si = p.seq_info[b];
+    // (a direct item without a visible key wrote no (m, l): its row is 0, its lse -inf)
+    const int2 si = p.direct ? make_int2(0, 1) : p.seq_info[b];
     const bool direct = (si.y == 1);
+    const bool keys = n_tiles > 0;
     const size_t prow = (size_t)(si.x + ch.split);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -786,7 +806,7 @@ __global__ void __launch_bounds__(288, 1)
         const int h = nt * 8 + 2 * tig + c;
         if (h >= gsz) continue;
         const int hq = kvh * gsz + h;
-        const float2 ml = ml_s[h];
+        const float2 ml = keys ? ml_s[h] : make_float2(-INFINITY, 0.f);
         if (direct) {
           const float inv = ml.y > 0.f ? vscale / ml.y : 0.f;
           uint16_t* orow = p.out + ((size_t)b * p.Hq + hq) * DVO;
@@ -809,7 +829,7 @@ __global__ void __launch_bounds__(288, 1)
         const int h = cw + 8 * j;
         if (h >= gsz) continue;
         const int hq = kvh * gsz + h;
-        const float2 ml = ml_s[h];
+        const float2 ml = keys ? ml_s[h] : make_float2(-INFINITY, 0.f);
         if (direct) {
           if (p.lse)
             p.lse[(size_t)b * p.Hq + hq] = ml.y > 0.f ? (ml.x + log2f(ml.y)) * 0.69314718055994531f : -INFINITY;

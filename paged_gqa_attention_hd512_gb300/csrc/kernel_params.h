@@ -55,6 +55,9 @@ struct DecodeParams {
   int box_rows;   // rows per TMA box: min(page_size, tile tokens), a power of two
   int box_shift;  // log2(box_rows)
   int swz;        // 7 when the K/V smem tiles are 128B-swizzled, 0 when not
+  // 1: one item per (sequence, kv head) over its whole visible range, written directly
+  // (no planner, no split, no merge: problems whose every item fits one CTA's round)
+  int direct;
   float sm_scale;
 };
 

@@ -137,6 +137,10 @@ def test_mode_setters_reject_other_values(lib):
     assert lib.paged_attn_set_prefill_split_kv(1) == pa.PA_ERR_INVALID_ARG
     assert lib.paged_attn_set_prefill_cta_pairs(-1) == pa.PA_OK
     assert lib.paged_attn_set_prefill_split_kv(-1) == pa.PA_OK
+    for bad in (2, -2):
+        assert lib.paged_attn_set_decode_direct(bad) == pa.PA_ERR_INVALID_ARG
+    for ok in (0, 1, -1):
+        assert lib.paged_attn_set_decode_direct(ok) == pa.PA_OK
 
 
 def _decode_noalloc(lib, **over):

@@ -22,13 +22,19 @@ BF16, FP8, NVFP4 = synth.KV_BF16, synth.KV_FP8, synth.KV_NVFP4
 def _reset_split():
     ensure_built()
     pa.paged_attn_set_decode_chunk_pages(0)
+    pa.paged_attn_set_decode_direct(-1)
     yield
     pa.paged_attn_set_decode_chunk_pages(0)
+    pa.paged_attn_set_decode_direct(-1)
 
 
 def test_tiny_mqa_decode_workload():
+    """Two short sequences of one kv head: the single-launch path (no planner, no merge)."""
     c = synth.workload("tiny_mqa_decode")
     check_full(c, "tiny mqa decode")
+    assert pa.paged_attn_last_variant() == "decode_512x512_hp8_bf16_direct"
+    pa.paged_attn_set_decode_direct(0)
+    check_full(c, "tiny mqa decode, planned")
     assert pa.paged_attn_last_variant() == "decode_512x512_hp8_bf16"
 
 
@@ -67,12 +73,17 @@ def _id(c):
     return f"{names[c[0]]}-{c[1]}x{c[2]}-{c[3]}q{c[4]}kv-ps{c[5]}-kv{'_'.join(map(str, c[6]))}-w{c[7]}"
 
 
+@pytest.mark.parametrize("mode", ["planned", "direct"])
 @pytest.mark.parametrize("c", CASES, ids=[_id(c) for c in CASES])
-def test_decode_parity(c):
+def test_decode_parity(c, mode):
+    """Every case through the planner (split-K where it splits, and the merge) and through
+    the single-launch path (one item per sequence and kv head)."""
     dt, dqk, dvo, hq, hkv, ps, lens, win = c
+    pa.paged_attn_set_decode_direct(1 if mode == "direct" else 0)
     case = synth.make_case("decode", batch=len(lens), Hq=hq, Hkv=hkv, d_qk=dqk, d_vo=dvo, page_size=ps,
                            kv_lens=lens, kv_dtype=dt, window_left=win, seed=300 + len(CASES))
-    check_full(case, _id(c))
+    check_full(case, _id(c) + " " + mode)
+    assert pa.paged_attn_last_variant().endswith("_direct") == (mode == "direct")
 
 
 @pytest.mark.parametrize("chunk_pages", [1, 2, 7])
@@ -99,7 +110,9 @@ def test_decode_split_equals_unsplit_nvfp4():
     assert float((l1 - l2).abs().max()) <= 1e-4
 
 
-def test_decode_empty_sequence_and_window_zero():
+@pytest.mark.parametrize("direct", [0, 1])
+def test_decode_empty_sequence_and_window_zero(direct):
+    pa.paged_attn_set_decode_direct(direct)
     case = synth.make_case("decode", batch=3, Hq=6, Hkv=2, d_qk=512, d_vo=512, page_size=16,
                            kv_lens=[0, 40, 0], seed=43)
     check_full(case, "empty sequences")
