@@ -235,67 +235,119 @@ __device__ __forceinline__ void prefill_plan_body(const PrefillParams& p) {
     }
     cost = prefill_tile_cost(p, kv_len, qo_len, q0);
   };
-  // split KV: fewer tiles x kv heads than split_target (short queries over long KV).  The
-  // tile list is short, so one thread lays the items out tile by tile: every (tile, kv
-  // head) whose range exceeds `chunk` KV tiles becomes ceil(range / chunk) items over
-  // consecutive chunks, each with its own partial slot, plus one merge entry; chunk is
-  // chosen so that about 2 x split_target items exist.
-  if (p.split_target > 0 && n_tiles * p.Hkv < p.split_target) {
+  // split KV: fewer tiles x kv heads than split_target (short queries over long KV): every
+  // (tile, kv head) whose range exceeds `chunk` KV tiles becomes ceil(range / chunk) items
+  // over consecutive chunks, each with its own partial slot, plus one merge entry; chunk
+  // is chosen so that about 2 x split_target items exist.  A thread per tile finds its
+  // range and part count, one thread turns the counts into offsets (the tiles number
+  // fewer than split_target), and every thread then writes items and merges in parallel.
+  if (p.split_target > 0 && n_tiles * p.Hkv < p.split_target && n_tiles <= 256) {
+    // per-tile records in the (here unused) histogram
+    int* t_b = hist;
+    int* t_q0 = hist + 256;
+    int* t_jlo = hist + 512;
+    int* t_nt = hist + 768;
+    int* t_parts = hist + 1024;
+    int* t_ioff = hist + 1280;  // first item
+    int* t_soff = hist + 1536;  // first partial slot
+    int* t_moff = hist + 1792;  // first merge entry
+    int cost = 0;
+    if (tid < n_tiles) {
+      int b, q0;
+      tile_of(tid, b, q0, cost);
+      int qo_len, kv_len;
+      if (cached) {
+        qo_len = c_qo[b];
+        kv_len = c_kv[b];
+      } else {
+        qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
+        const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
+        kv_len = np > 0 ? (np - 1) * p.page_size + p.kv_last_page_len[b] : 0;
+      }
+      int jlo, nt;
+      prefill_tile_range(p, kv_len, qo_len, q0, jlo, nt);
+      t_b[tid] = b;
+      t_q0[tid] = q0;
+      t_jlo[tid] = jlo;
+      t_nt[tid] = nt;
+    }
+    // the total cost of the tiles
+    for (int o = 16; o > 0; o >>= 1) cost += __shfl_xor_sync(0xffffffffu, cost, o);
+    __syncthreads();  // (s_red was last read before the tile offsets' scan finished)
+    if ((tid & 31) == 0) s_red[tid >> 5] = cost;
+    __syncthreads();
+    long long total = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += s_red[w];
+    const int chunk = max(4, (int)((total * p.Hkv + 2ll * p.split_target - 1) / (2ll * p.split_target)));
+    if (tid < n_tiles) t_parts[tid] = max(1, (t_nt[tid] + chunk - 1) / chunk);
+    __syncthreads();
     if (tid == 0) {
-      long long total = 0;
+      int ni = 0, ns = 0, nm = 0;
       for (int t = 0; t < n_tiles; ++t) {
-        int b, q0, cost;
-        tile_of(t, b, q0, cost);
-        total += cost;
-      }
-      const int chunk = max(4, (int)((total * p.Hkv + 2ll * p.split_target - 1) / (2ll * p.split_target)));
-      int n_items = 0, n_slots = 0, n_merge = 0;
-      for (int t = 0; t < n_tiles; ++t) {
-        int b, q0, cost;
-        tile_of(t, b, q0, cost);
-        int qo_len, kv_len;
-        if (cached) {
-          qo_len = c_qo[b];
-          kv_len = c_kv[b];
-        } else {
-          qo_len = p.qo_indptr[b + 1] - p.qo_indptr[b];
-          const int np = p.kv_indptr[b + 1] - p.kv_indptr[b];
-          kv_len = np > 0 ? (np - 1) * p.page_size + p.kv_last_page_len[b] : 0;
-        }
-        int jlo, nt;
-        prefill_tile_range(p, kv_len, qo_len, q0, jlo, nt);
-        int parts = max(1, (nt + chunk - 1) / chunk);
-        // stay inside the host's bounds (cannot trigger with chunk as chosen above)
-        if (n_items + parts * p.Hkv > p.max_items || n_slots + parts * p.Hkv > p.max_slots) parts = 1;
-        const int step = (nt + parts - 1) / parts;
-        for (int k = 0; k < p.Hkv; ++k) {
-          if (n_items + parts > p.max_items) break;
-          if (parts > 1) {
-            PrefillMerge m;
-            m.b = b;
-            m.q_begin = q0;
-            m.kvh = k;
-            m.slot0 = n_slots;
-            m.parts = parts;
-            p.merges[n_merge++] = m;
-          }
-          for (int s2 = 0; s2 < parts; ++s2) {
-            PrefillItem it;
-            it.b = b;
-            it.q_begin = q0;
-            it.kvh = k;
-            it.kv_t0 = jlo + s2 * step;
-            it.kv_t1 = min(jlo + nt, jlo + (s2 + 1) * step);
-            it.cost = it.kv_t1 - it.kv_t0;
-            it.slot = parts > 1 ? n_slots + s2 : -1;
-            p.items[n_items++] = it;
-          }
-          if (parts > 1) n_slots += parts;
+        const int parts = t_parts[t];
+        t_ioff[t] = ni;
+        t_soff[t] = ns;
+        t_moff[t] = nm;
+        ni += parts * p.Hkv;
+        if (parts > 1) {
+          ns += parts * p.Hkv;
+          nm += p.Hkv;
         }
       }
-      p.hdr[0] = n_items;
-      p.hdr[1] = n_merge;
+      // stay inside the host's bounds (cannot trigger with chunk as chosen above): no split
+      if (ni > p.max_items || ns > p.max_slots) {
+        for (int t = 0; t < n_tiles; ++t) {
+          t_parts[t] = 1;
+          t_ioff[t] = t * p.Hkv;
+          t_soff[t] = t_moff[t] = 0;
+        }
+        ni = n_tiles * p.Hkv;
+        nm = 0;
+      }
+      s_carry = ni;
+      s_red[0] = nm;
+      p.hdr[0] = ni;
+      p.hdr[1] = nm;
       p.hdr[2] = 0;  // full item records
+    }
+    __syncthreads();
+    const int n_items = s_carry, n_merge = s_red[0];
+    // the last tile whose first entry (in off[]) is at or before i
+    auto tile_at = [&](const int* off, int i) {
+      int lo = 0, hi = n_tiles - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off[mid] <= i) lo = mid; else hi = mid - 1;
+      }
+      return lo;
+    };
+    for (int i = tid; i < n_items; i += blockDim.x) {
+      const int t = tile_at(t_ioff, i);
+      const int parts = t_parts[t], local = i - t_ioff[t];
+      const int k = local / parts, s2 = local % parts;
+      const int jlo = t_jlo[t], nt = t_nt[t], step = (nt + parts - 1) / parts;
+      PrefillItem it;
+      it.b = t_b[t];
+      it.q_begin = t_q0[t];
+      it.kvh = k;
+      it.kv_t0 = jlo + s2 * step;
+      it.kv_t1 = min(jlo + nt, jlo + (s2 + 1) * step);
+      it.cost = it.kv_t1 - it.kv_t0;
+      it.slot = parts > 1 ? t_soff[t] + k * parts + s2 : -1;
+      p.items[i] = it;
+    }
+    for (int i = tid; i < n_merge; i += blockDim.x) {
+      // split tiles only own merge entries, and a split tile's entries precede every later
+      // tile's offset, so the last tile at or before i is the split tile that owns i
+      const int t = tile_at(t_moff, i);
+      const int k = i - t_moff[t];
+      PrefillMerge m;
+      m.b = t_b[t];
+      m.q_begin = t_q0[t];
+      m.kvh = k;
+      m.slot0 = t_soff[t] + k * t_parts[t];
+      m.parts = t_parts[t];
+      p.merges[i] = m;
     }
     return;
   }

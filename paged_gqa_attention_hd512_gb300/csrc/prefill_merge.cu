@@ -6,9 +6,11 @@
 // Test Coverage: split-K): weights exp(lse_s - lse) with lse = ln sum_s exp(lse_s); a row
 // that no chunk saw gives 0 and lse -inf.
 //
-// Grid: (merge entries, 16 blocks of 8 rows); a warp per row, its lanes over 4-column
-// groups; every part's values are loaded before any is summed, so the loads of a row are
-// in flight together.
+// Grid: (merge entries, 16 blocks of 8 rows); a warp per row.  Lane s takes the lse of
+// part s (32 parts at a time): the row's max and sum are warp reductions, and each lane
+// forms its part's weight once.  The lanes then own 4-column groups and load four parts'
+// values before summing them with the weights broadcast from their lanes, so the warp
+// waits on memory once per four parts.
 #include "launch.h"
 #include "common.cuh"
 
@@ -19,6 +21,7 @@ namespace {
 template <int DVO>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams p) {
   constexpr int G4 = DVO / 128;  // float4 groups per lane
+  constexpr int B = 4;           // parts loaded together
   grid_dep_wait();  // the prefill kernel's partial slots are complete
   const int n = p.hdr[1];
   const int g = p.group;
@@ -30,29 +33,44 @@ __global__ void __launch_bounds__(256) prefill_merge_kernel(const PrefillParams 
     const int n_pos = min(p.rows_per_tile, qo_len - m.q_begin);
     if (r >= n_pos * g) continue;
     const int q_row0 = p.qo_indptr[m.b] + m.q_begin;
+    const float* plse = p.part_lse + (size_t)m.slot0 * 128 + r;  // part s at plse[s * 128]
     float M = -INFINITY;
-    for (int s = 0; s < m.parts; ++s) M = fmaxf(M, p.part_lse[(size_t)(m.slot0 + s) * 128 + r]);
+    for (int s = lane; s < m.parts; s += 32) M = fmaxf(M, plse[(size_t)s * 128]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     float L = 0.f;
     if (M != -INFINITY)
-      for (int s = 0; s < m.parts; ++s) L += expf(p.part_lse[(size_t)(m.slot0 + s) * 128 + r] - M);
+      for (int s = lane; s < m.parts; s += 32) L += expf(plse[(size_t)s * 128] - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
     const float lse = M == -INFINITY ? -INFINITY : M + logf(L);
     float4 acc[G4];
 #pragma unroll
     for (int k = 0; k < G4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
-#pragma unroll 2
-      for (int s = 0; s < m.parts; ++s) {
-        const size_t base = (size_t)(m.slot0 + s) * 128 + r;
-        const float w = expf(p.part_lse[base] - lse);
-        float4 v[G4];
+      const float4* src = reinterpret_cast<const float4*>(p.part_o + ((size_t)m.slot0 * 128 + r) * DVO) + lane;
+      const size_t step = (size_t)128 * DVO / 4;  // float4s between consecutive parts
+      for (int s0 = 0; s0 < m.parts; s0 += 32) {
+        const float w = s0 + lane < m.parts ? expf(plse[(size_t)(s0 + lane) * 128] - lse) : 0.f;
+        const int cnt = min(32, m.parts - s0);
+        for (int k0 = 0; k0 < cnt; k0 += B) {
+          float4 v[B][G4];
 #pragma unroll
-        for (int k = 0; k < G4; ++k) v[k] = __ldg(reinterpret_cast<const float4*>(p.part_o + base * DVO) + lane + 32 * k);
+          for (int b = 0; b < B; ++b)
 #pragma unroll
-        for (int k = 0; k < G4; ++k) {
-          acc[k].x += w * v[k].x;
-          acc[k].y += w * v[k].y;
-          acc[k].z += w * v[k].z;
-          acc[k].w += w * v[k].w;
+            for (int k = 0; k < G4; ++k)
+              v[b][k] = k0 + b < cnt ? __ldg(src + (size_t)(s0 + k0 + b) * step + 32 * k) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int b = 0; b < B; ++b) {
+            const float wb = __shfl_sync(0xffffffffu, w, (k0 + b) & 31);
+#pragma unroll
+            for (int k = 0; k < G4; ++k) {
+              acc[k].x += wb * v[b][k].x;
+              acc[k].y += wb * v[b][k].y;
+              acc[k].z += wb * v[b][k].z;
+              acc[k].w += wb * v[b][k].w;
+            }
+          }
         }
       }
     }
