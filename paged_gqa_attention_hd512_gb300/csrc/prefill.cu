@@ -37,8 +37,9 @@ cudaError_t launch_prefill_prep(int kvt, int dqk, int dvo, int copy, const Prefi
     prefill_prep_kernel<KV_BF16, 512, 512, false, false><<<1, 1024, 0, s>>>(p, d);
     return cudaGetLastError();
   }
-  // two 1024-thread blocks per SM write the copy, all resident at once
-  const int grid = 1 + 2 * sms;
+  // two 1024-thread blocks per SM, the planner's among them, all resident at once (one
+  // block more would wait for a slot and run as a second wave)
+  const int grid = 2 * sms;
   const bool pad = copy == 2;
   if (kvt == KV_BF16) return pad ? run_prep<KV_BF16, true>(dqk, dvo, grid, p, d, s) : cudaErrorInvalidValue;
   if (kvt == KV_FP8) return pad ? run_prep<KV_FP8, true>(dqk, dvo, grid, p, d, s) : run_prep<KV_FP8, false>(dqk, dvo, grid, p, d, s);
