@@ -12,8 +12,10 @@ cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t s) {
 
 cudaError_t launch_decode_merge(int dvo, const DecodeParams& p, int sms, cudaStream_t s) {
   const long warps = (long)p.batch * p.Hq * (dvo / 128);
-  // one warp per unit up to two 256-thread blocks per SM; the warps stride over the rest
-  const int blocks = (int)std::min<long>((warps * 32 + 255) / 256, 2l * sms);
+  // one warp per unit up to eight 256-thread blocks per SM (every unit of the bf16 GQA
+  // decode at once: 0.3883 -> 0.3873 ms per step against two blocks per SM); the warps
+  // stride over the rest
+  const int blocks = (int)std::min<long>((warps * 32 + 255) / 256, 8l * sms);
   if (blocks == 0) return cudaSuccess;
   // a programmatic dependent of the decode kernel
   if (dvo == 512) return launch_pdl(decode_merge_kernel<512>, dim3(blocks), dim3(256), 0, s, 1, p);
