@@ -158,3 +158,16 @@ def test_decode_heavy_tailed_kv(dt):
     check_full(case, "heavy tails")
     pa.paged_attn_set_decode_chunk_pages(2)
     check_full(case, "heavy tails, split")
+
+
+def test_decode_batch_beyond_one_planner_round():
+    """1100 sequences: the planner's block (at most 1024 threads) walks the batch in two
+    rounds for its page counts and its scan of chunk offsets."""
+    import numpy as np
+    lens = [int(x) for x in np.random.default_rng(48).integers(0, 40, size=1100)]
+    case = synth.make_case("decode", batch=len(lens), Hq=8, Hkv=1, d_qk=256, d_vo=256, page_size=16,
+                           kv_lens=lens, seed=48)
+    check_full(case, "1100 sequences")
+    assert not pa.paged_attn_last_variant().endswith("_direct")
+    pa.paged_attn_set_decode_chunk_pages(1)
+    check_full(case, "1100 sequences, one page per chunk")
