@@ -55,10 +55,16 @@
  *
  * Streams and workspace: work is enqueued on `stream` (a cudaStream_t, NULL = legacy
  * default stream) and the call returns without waiting.  The library owns a grow-only
- * device workspace (work lists, split-K partials, an error word); it grows with
- * cudaMalloc only when a call needs more than it has, so once warmed up a call
- * allocates nothing.  Calls that overlap on the GPU (different streams) share that
- * workspace and must not run concurrently.
+ * device workspace per stream (work lists, split-K partials, the prefill's copy of FP8 /
+ * NVFP4 pages, an error word); it grows with cudaMalloc (and the cudaFree of the smaller
+ * one, which waits for the device) only when a call needs more than it has, so once
+ * warmed up a call allocates nothing.  Calls on different streams use different
+ * workspaces and may overlap on the GPU; calls on one stream are ordered by it.  A call
+ * captured into a CUDA graph allocates nothing: it uses the capturing stream's workspace
+ * if that is large enough, else the legacy default stream's, else it fails with
+ * PA_ERR_CUDA; so make an eager call of the same shape on one of those streams before
+ * capturing.  The graph keeps that workspace's address, and replays share it with the
+ * eager calls on its stream.
  *
  * Errors: every entry point returns 0 (PA_OK) or a negative pa_status, and launches
  * nothing when it rejects its arguments.
@@ -228,19 +234,21 @@ int paged_attn_append_kv(const void* k_new, const void* v_new, const int32_t* ap
 /* Human-readable text of a pa_status value (static storage, never NULL). */
 const char* paged_attn_status_string(int status);
 
-/* Frees the library-owned workspace of the current device (blocking).  Returns PA_OK or
- * PA_ERR_CUDA.  The next call allocates it again. */
+/* Frees the library-owned workspaces of the current device, one per stream that has made
+ * a call (blocking).  Returns PA_OK or PA_ERR_CUDA.  The next call on a stream allocates
+ * that stream's again. */
 int paged_attn_release_workspace(void);
 
 /* Synchronises the current device, then reports and clears the device error words that
- * kernels set when a bounded wait gives up (the workspace's and, once
+ * kernels set when a bounded wait gives up (each stream's workspace's and, once
  * paged_attn_decode_noalloc has run on the device, the one in its fixed array):
- * *code = 0 (none) or the wait site id (the workspace's first when both are set).
+ * *code = 0 (none) or the wait site id (a workspace's first when several are set).
  * Returns PA_OK, PA_ERR_DEVICE when a wait gave up, PA_ERR_CUDA on a CUDA error. */
 int paged_attn_check_device_error(int* code);
 
 /* Test hook: stores `code` in a device error word of the current device (blocking):
- * target 0 = the workspace's (allocating the workspace if there is none), 1 = the one in
+ * target 0 = the legacy default stream's workspace's (allocating that workspace if there
+ * is none), 1 = the one in
  * paged_attn_decode_noalloc's fixed array.  Lets a test check that
  * paged_attn_check_device_error reports and clears each word without making a kernel
  * wait time out.  Returns PA_OK, PA_ERR_INVALID_ARG or PA_ERR_CUDA. */

@@ -14,6 +14,7 @@
 #include <cstring>
 #include <algorithm>
 #include <atomic>
+#include <map>
 #include <mutex>
 #include <vector>
 
@@ -53,7 +54,9 @@ struct Workspace {
   void* base = nullptr;
   size_t bytes = 0;
 };
-Workspace g_ws[kMaxDevices];
+// one grow-only workspace per (device, stream): calls on different streams may overlap on
+// the GPU, calls on one stream are ordered by it
+std::map<cudaStream_t, Workspace> g_ws[kMaxDevices];
 constexpr size_t kErrOffset = 0;      // int error word
 constexpr size_t kFixedBytes = 256;   // error word region
 constexpr int kReuseTiles = 64;       // prefill P reuse: items of up to 64 KV tiles (8192 keys)
@@ -87,16 +90,33 @@ int pair_clusters(int dqk, int dvo) {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Make sure the current device's workspace holds at least `need` bytes; returns its
-// base or nullptr.  Growth frees the old buffer (cudaFree waits for the device).
-void* workspace(size_t need, int* status) {
+// Make sure the workspace of `stream` on the current device holds at least `need` bytes;
+// returns its base or nullptr.  Growth frees the old buffer (cudaFree waits for the
+// device, so no kernel still uses it).
+void* workspace(size_t need, cudaStream_t stream, int* status) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     *status = PA_ERR_CUDA;
     return nullptr;
   }
   std::lock_guard<std::mutex> lock(g_ws_mutex);
-  Workspace& w = g_ws[dev];
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (stream && cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+    *status = PA_ERR_CUDA;
+    return nullptr;
+  }
+  if (cs != cudaStreamCaptureStatusNone) {
+    // a call being captured into a graph may not allocate: the capturing stream's own
+    // workspace if it is large enough, else the legacy default stream's (which an eager
+    // warm-up call on that stream has grown), else an error
+    for (cudaStream_t key : {stream, static_cast<cudaStream_t>(nullptr)}) {
+      const auto it = g_ws[dev].find(key);
+      if (it != g_ws[dev].end() && it->second.bytes >= need) return it->second.base;
+    }
+    *status = PA_ERR_CUDA;
+    return nullptr;
+  }
+  Workspace& w = g_ws[dev][stream];
   if (w.bytes >= need) return w.base;
   if (w.base) cudaFree(w.base);
   w.base = nullptr;
@@ -393,9 +413,9 @@ int paged_attn_release_workspace(void) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_ws_mutex);
-  if (g_ws[dev].base && cudaFree(g_ws[dev].base) != cudaSuccess) return PA_ERR_CUDA;
-  g_ws[dev].base = nullptr;
-  g_ws[dev].bytes = 0;
+  for (auto& kv : g_ws[dev])
+    if (kv.second.base && cudaFree(kv.second.base) != cudaSuccess) return PA_ERR_CUDA;
+  g_ws[dev].clear();
   return PA_OK;
 }
 
@@ -436,14 +456,19 @@ int paged_attn_check_device_error(int* code) {
   if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
-  // the workspace's error word and, once paged_attn_decode_noalloc has run on this
-  // device, the one in its fixed array; both are cleared, the first nonzero is reported
+  // the error word of every stream's workspace and, once paged_attn_decode_noalloc has
+  // run on this device, the one in its fixed array; all are cleared, the first nonzero
+  // is reported
   int v = 0;
   {
     std::lock_guard<std::mutex> lock(g_ws_mutex);
-    if (g_ws[dev].base) v = take_error_word(g_ws[dev].base);
+    for (auto& kv : g_ws[dev]) {
+      if (!kv.second.base) continue;
+      const int w = take_error_word(kv.second.base);
+      if (w < 0) return PA_ERR_CUDA;
+      if (v == 0) v = w;
+    }
   }
-  if (v < 0) return PA_ERR_CUDA;
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
     if (g_noalloc_ptr[dev]) {
@@ -459,7 +484,7 @@ int paged_attn_check_device_error(int* code) {
 int paged_attn_debug_set_error_word(int target, int code) {
   if (target != 0 && target != 1) return PA_ERR_INVALID_ARG;
   int st = PA_OK;
-  void* base = target == 0 ? workspace(kFixedBytes, &st) : noalloc_scratch(&st);
+  void* base = target == 0 ? workspace(kFixedBytes, nullptr, &st) : noalloc_scratch(&st);
   if (!base) return st;
   if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
   if (cudaMemcpy(static_cast<char*>(base) + kErrOffset, &code, sizeof code, cudaMemcpyHostToDevice) != cudaSuccess)
@@ -505,7 +530,7 @@ int paged_attn_decode(const void* q, const void* kv_cache, const int32_t* kv_ind
   const size_t o_seq = off; off = align_up(off + (size_t)batch * sizeof(int2), 256);
   const size_t o_ml = off; off = align_up(off + (size_t)max_chunks * num_qo_heads * sizeof(float2), 256);
   const size_t o_o = off; off = align_up(off + (size_t)max_chunks * num_qo_heads * head_dim_vo * sizeof(float), 256);
-  char* ws = static_cast<char*>(workspace(off, &st));
+  char* ws = static_cast<char*>(workspace(off, static_cast<cudaStream_t>(stream), &st));
   if (!ws) return st;
 
   DecodeParams& p = L.p;
@@ -616,7 +641,7 @@ int prefill_call(const void* q, const int32_t* qo_indptr, int total_q, const voi
   const size_t o_part = off; off = align_up(off + (size_t)max_slots * 128 * head_dim_vo * sizeof(float), 256);
   const size_t o_plse = off; off = align_up(off + (size_t)max_slots * 128 * sizeof(float), 256);
   const size_t o_merge = off; off = align_up(off + (size_t)max_slots * sizeof(PrefillMerge), 256);
-  char* ws = static_cast<char*>(workspace(off, &st));
+  char* ws = static_cast<char*>(workspace(off, static_cast<cudaStream_t>(stream), &st));
   if (!ws) return st;
 
   PrefillLaunch L;
@@ -787,7 +812,7 @@ int paged_attn_append_kv(const void* k_new, const void* v_new, const int32_t* ap
       (uint64_t)num_kv_heads * page_size * (head_dim_qk + head_dim_vo) * x2_of(kv_dtype) / 2;
   if ((uint64_t)num_pages * page_bytes >= (1ull << 46)) return PA_ERR_INVALID_ARG;
   int st = PA_OK;
-  char* ws = static_cast<char*>(workspace(kFixedBytes, &st));
+  char* ws = static_cast<char*>(workspace(kFixedBytes, static_cast<cudaStream_t>(stream), &st));
   if (!ws) return st;
   AppendParams p;
   std::memset(&p, 0, sizeof p);
