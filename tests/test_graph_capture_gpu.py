@@ -47,11 +47,38 @@ def _capture_and_check(case, seed_change):
     assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
 
 
-def test_decode_in_a_cuda_graph():
+@pytest.mark.parametrize("direct", [0, 1])
+def test_decode_in_a_cuda_graph(direct):
+    """The planned path (planner, split-K decode, merge) and the single-launch path."""
     kw = dict(batch=5, Hq=24, Hkv=4, d_qk=512, d_vo=512, page_size=16, kv_lens=[1, 100, 700, 64, 333])
     pa.paged_attn_set_decode_chunk_pages(0)
-    case = synth.make_case("decode", seed=81, **kw).to("cuda")
-    _capture_and_check(case, dict(kw, seed=82))
+    pa.paged_attn_set_decode_direct(direct)
+    try:
+        case = synth.make_case("decode", seed=81, **kw).to("cuda")
+        _capture_and_check(case, dict(kw, seed=82))
+        assert pa.paged_attn_last_variant().endswith("_direct") == bool(direct)
+    finally:
+        pa.paged_attn_set_decode_direct(-1)
+
+
+def test_capture_on_a_fresh_stream_uses_the_default_streams_workspace():
+    """Warm-up on the default stream, capture on a stream that has never called the
+    library: the call allocates nothing during the capture and replays correctly."""
+    ensure_built()
+    kw = dict(batch=3, Hq=8, Hkv=2, d_qk=512, d_vo=512, page_size=16, kv_lens=[90, 33, 300])
+    case = synth.make_case("decode", seed=85, **kw).to("cuda")
+    kwa = pa.case_args(case)
+    out0, lse0 = pa.run_case(case)
+    torch.cuda.synchronize()
+    out, lse = torch.empty_like(out0), torch.empty_like(lse0)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        _call(case, kwa, out, lse)
+    g.replay()
+    torch.cuda.synchronize()
+    assert pa.paged_attn_check_device_error() == 0
+    assert torch.equal(out, out0) and torch.equal(lse, lse0)
 
 
 @pytest.mark.parametrize("dt", [synth.KV_BF16, synth.KV_FP8, synth.KV_NVFP4])
