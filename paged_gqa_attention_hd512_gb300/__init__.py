@@ -104,18 +104,20 @@ def paged_attn_status_string(status: int) -> str:
 
 
 def _ptr(t: Optional[torch.Tensor]):
+    """The device address of a contiguous CUDA tensor (an int; ctypes passes it as a
+    pointer), None for None."""
     if t is None:
         return None
     if not t.is_cuda:
         raise ValueError("tensor arguments must be CUDA tensors")
     if not t.is_contiguous():
         raise ValueError("tensor arguments must be contiguous")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
-def _stream(stream) -> ctypes.c_void_p:
+def _stream(stream):
     s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    return s.cuda_stream
 
 
 def _x2(kv_dtype: int) -> int:
@@ -125,9 +127,9 @@ def _x2(kv_dtype: int) -> int:
 def _scales(kv_dtype, k_scale, v_scale, sf):
     sc = _Scales(None, None, None)
     if kv_dtype != PA_KV_BF16:
-        sc.k_scale = _ptr(k_scale).value if k_scale is not None else None
-        sc.v_scale = _ptr(v_scale).value if v_scale is not None else None
-        sc.sf = _ptr(sf).value if sf is not None else None
+        sc.k_scale = _ptr(k_scale)
+        sc.v_scale = _ptr(v_scale)
+        sc.sf = _ptr(sf)
     return sc
 
 
