@@ -2,6 +2,8 @@
 // translation units that instantiate the kernels.
 #pragma once
 
+#include <atomic>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -27,6 +29,20 @@ struct PrefillLaunch {
 // Launch `kern` on `stream` with programmatic stream serialization: it may begin while
 // the preceding kernel on the stream finishes (the kernel itself waits for that one
 // before it touches global memory, see grid_dep_wait in common.cuh).
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current device, once per
+// device: `done` is the caller's per-kernel record of the devices already set (the
+// attribute is per device, and setting it on every call costs host time on every call).
+template <typename Kern>
+inline cudaError_t set_smem_limit_once(Kern kern, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 template <typename Kern, typename... Args>
 cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t stream, int cluster_x,
                        Args... args) {

@@ -56,7 +56,8 @@ static cudaError_t run_prefill(const PrefillLaunch& L) {
   const bool plain = KVT == KV_BF16 && !PAIR && L.p.mask == nullptr && L.p.box_rows == L.p.page_size;
   auto kern = plain ? prefill_kernel<KVT, DQK, DVO, PAIR, !(KVT == KV_BF16 && !PAIR)>
                     : prefill_kernel<KVT, DQK, DVO, PAIR, true>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::ALLOC);
+  static std::atomic<uint64_t> smem_set[2];
+  cudaError_t e = set_smem_limit_once(kern, C::ALLOC, smem_set[plain ? 1 : 0]);
   if (e != cudaSuccess) return e;
   // a programmatic dependent of the preparation kernel (pairs: clusters of two CTAs, one
   // per SM of a pair)
