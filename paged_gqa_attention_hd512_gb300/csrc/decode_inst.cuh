@@ -12,8 +12,7 @@ template <int KVT, int DQK, int DVO, int HP>
 static cudaError_t run_decode(const DecodeLaunch& L) {
   using Sm = DecodeSmem<KVT, DQK, DVO, HP>;
   auto kern = decode_kernel<KVT, DQK, DVO, HP>;
-  static std::atomic<uint64_t> smem_set{0};
-  cudaError_t e = set_smem_limit_once(kern, Sm::ALLOC, smem_set);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sm::ALLOC);
   if (e != cudaSuccess) return e;
   // a programmatic dependent of the planner
   return launch_pdl(kern, dim3(L.grid), dim3(288), Sm::ALLOC, L.stream, 1, L.tk, L.tv, L.tsfk, L.tsfv, L.p);
