@@ -218,3 +218,14 @@ def test_prefill_heavy_tailed_kv(dt, mode, _dequant_limit):
     case = synth.make_case("prefill", batch=2, Hq=16, Hkv=2, d_qk=512, d_vo=512, page_size=16,
                            kv_lens=[300, 129], qo_lens=[300, 129], kv_dtype=dt, seed=48, outlier_every=16)
     check_full(case, f"heavy tails {mode}")
+
+
+@pytest.mark.parametrize("lens", [([50, 20, 100], [50, 0, 30]), ([0, 40, 0], [0, 40, 0])],
+                         ids=["no-new-tokens", "empty-sequences"])
+def test_prefill_sequences_without_new_tokens(lens, cta_mode):
+    """A sequence with cached tokens but no new ones, and sequences with neither, between
+    ordinary ones: they get no work items and the other rows are unchanged."""
+    kv, qo = lens
+    case = synth.make_case("prefill", batch=3, Hq=8, Hkv=2, d_qk=512, d_vo=512, page_size=16, kv_lens=kv,
+                           qo_lens=qo, seed=93)
+    check_full(case, f"kv {kv} qo {qo}{cta_mode}")
