@@ -229,3 +229,15 @@ def test_prefill_sequences_without_new_tokens(lens, cta_mode):
     case = synth.make_case("prefill", batch=3, Hq=8, Hkv=2, d_qk=512, d_vo=512, page_size=16, kv_lens=kv,
                            qo_lens=qo, seed=93)
     check_full(case, f"kv {kv} qo {qo}{cta_mode}")
+
+
+def test_prefill_batch_beyond_the_planner_cache(cta_mode):
+    """2100 sequences of 0-3 new tokens over 0-22 keys: more sequences than the planner
+    keeps in shared memory (2048), so it reads their lengths from the index arrays."""
+    import numpy as np
+    rng = np.random.default_rng(95)
+    qo = [int(x) for x in rng.integers(0, 4, size=2100)]
+    kv = [q + int(x) for q, x in zip(qo, rng.integers(0, 20, size=2100))]
+    case = synth.make_case("prefill", batch=2100, Hq=8, Hkv=2, d_qk=256, d_vo=256, page_size=16, kv_lens=kv,
+                           qo_lens=qo, seed=95)
+    check_full(case, "2100 sequences" + cta_mode)
