@@ -188,3 +188,22 @@ def test_append_codes_that_round_to_zero_keep_their_sign(dt):
     _assert_bytes_equal(cache, ref_cache, "codes that round to zero")
     if dt == ac.NVFP4:
         _assert_bytes_equal(sf, ref_sf, "scale pool")
+
+
+@pytest.mark.parametrize("dt", [ac.FP8, ac.NVFP4])
+def test_append_many_sequences(dt):
+    """1100 sequences of 0-3 new tokens each: a warp finds its token's sequence in three
+    rounds of its 32-way search over append_indptr."""
+    import numpy as np
+    ensure_built()
+    rng = np.random.default_rng(77 + dt)
+    n_new = [int(x) for x in rng.integers(0, 4, size=1100)]
+    kv_lens = [n + int(x) for n, x in zip(n_new, rng.integers(0, 30, size=1100))]
+    case = ac.make(kv_lens=kv_lens, n_new=n_new, Hkv=2, d_qk=256, d_vo=256, page_size=16, kv_dtype=dt,
+                   seed=1100 + dt, k_scale=0.05, v_scale=0.02)
+    cache, sf, code = _run_gpu(case)
+    ref_cache, ref_sf, skipped = _oracle(case)
+    assert code == 0 and skipped == 0
+    _assert_bytes_equal(cache, ref_cache, "1100 sequences")
+    if dt == ac.NVFP4:
+        _assert_bytes_equal(sf, ref_sf, "1100 sequences, scales")
