@@ -236,9 +236,10 @@ __device__ __forceinline__ void prefill_plan_body(const PrefillParams& p) {
     cost = prefill_tile_cost(p, kv_len, qo_len, q0);
   };
   // split KV: fewer tiles x kv heads than split_target (short queries over long KV): every
-  // (tile, kv head) whose range exceeds `chunk` KV tiles becomes ceil(range / chunk) items
-  // over consecutive chunks, each with its own partial slot, plus one merge entry; chunk
-  // is chosen so that about 2 x split_target items exist.  A thread per tile finds its
+  // (tile, kv head) whose range is long enough becomes several items over consecutive
+  // parts of it, each with its own partial slot, plus one merge entry; the part counts
+  // follow the ranges' lengths so that at most about 2 x split_target items exist.  A
+  // thread per tile finds its
   // range and part count, one thread turns the counts into offsets (the tiles number
   // fewer than split_target), and every thread then writes items and merges in parallel.
   if (p.split_target > 0 && n_tiles * p.Hkv < p.split_target && n_tiles <= 256) {
@@ -278,8 +279,20 @@ __device__ __forceinline__ void prefill_plan_body(const PrefillParams& p) {
     __syncthreads();
     long long total = 0;
     for (int w = 0; w < (int)(blockDim.x >> 5); ++w) total += s_red[w];
-    const int chunk = max(4, (int)((total * p.Hkv + 2ll * p.split_target - 1) / (2ll * p.split_target)));
-    if (tid < n_tiles) t_parts[tid] = max(1, (t_nt[tid] + chunk - 1) / chunk);
+    // parts in proportion to each range, rounded down, so that the items number at most
+    // 2 x split_target (two rounds over the CTAs) and come out of near-equal size; at
+    // least 4 KV tiles a part.  (Chunks of one fixed size rounded each range's part
+    // count up: 4 x 32 new tokens over 16384 keys gave 320 items of 13 tiles, a third
+    // round for 16 CTAs.)
+    if (tid < n_tiles) {
+      const int nt = t_nt[tid];
+      const long long want = (long long)nt * 2 * p.split_target / max(1ll, total * p.Hkv);
+      const int parts = (int)max(1ll, min((long long)(nt + 3) / 4, want));
+      // as many parts as parts of ceil(nt / parts) tiles need: none comes out empty
+      // (25 tiles in 6 parts of 5 would leave the sixth empty)
+      const int step = (nt + parts - 1) / parts;
+      t_parts[tid] = (nt + step - 1) / step;
+    }
     __syncthreads();
     if (tid == 0) {
       int ni = 0, ns = 0, nm = 0;
