@@ -17,6 +17,9 @@ CASES = [
     (synth.KV_BF16, 256, 256, 4, 2, 8, [3000, 100, 5000], [7, 100, 3], 1, 1023),
     (synth.KV_BF16, 512, 512, 24, 4, 64, [9000, 700], [5, 64], 0, -1),
     (synth.KV_BF16, 512, 512, 8, 1, 64, [12000], [30], 1, -1),
+    # one token over 20000 keys: 157 KV tiles cut into 40 parts, more than a warp's lanes
+    # hold at once in the merge
+    (synth.KV_BF16, 512, 512, 8, 1, 64, [20000], [1], 1, -1),
     (synth.KV_FP8, 512, 512, 12, 4, 16, [3000, 1200], [9, 33], 1, -1),
     (synth.KV_NVFP4, 512, 256, 16, 2, 32, [4096, 1500], [24, 8], 1, -1),
 ]
