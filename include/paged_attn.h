@@ -222,7 +222,8 @@ int paged_attn_prefill_custom_mask(const void* q, const int32_t* qo_indptr, int 
  * outside its sequence (n_b > kv_len_b) or whose page id is outside [0, num_pages) is
  * skipped and sets the device error word (paged_attn_check_device_error).
  * Returns PA_OK, or PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED / PA_ERR_ALIGNMENT /
- * PA_ERR_CUDA; nothing is launched on error.
+ * PA_ERR_CUDA; nothing is launched on error.  PA_ERR_UNSUPPORTED also when one page
+ * (num_kv_heads * page_size rows of K and V) takes 2^31 bytes or more.
  */
 int paged_attn_append_kv(const void* k_new, const void* v_new, const int32_t* append_indptr,
                          int total_new, void* kv_cache, const int32_t* kv_indptr,

@@ -811,6 +811,7 @@ int paged_attn_append_kv(const void* k_new, const void* v_new, const int32_t* ap
   const uint64_t page_bytes =
       (uint64_t)num_kv_heads * page_size * (head_dim_qk + head_dim_vo) * x2_of(kv_dtype) / 2;
   if ((uint64_t)num_pages * page_bytes >= (1ull << 46)) return PA_ERR_INVALID_ARG;
+  if (page_bytes >= (1ull << 31)) return PA_ERR_UNSUPPORTED;  // the kernel's in-page offsets are 32-bit
   int st = PA_OK;
   char* ws = static_cast<char*>(workspace(kFixedBytes, static_cast<cudaStream_t>(stream), &st));
   if (!ws) return st;

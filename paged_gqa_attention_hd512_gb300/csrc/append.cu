@@ -103,13 +103,14 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kv_kernel(const Appe
     return;
   }
   const int slot = t % p.page_size;
-  const int ku = p.d_qk / 16, vu = p.d_vo / 16, units = p.Hkv * (ku + vu);
+  const int ku = p.d_qk / 16, vu = p.d_vo / 16, kvu = ku + vu, units = p.Hkv * kvu;
   // element widths in bytes x2: bf16 4, fp8 2, nvfp4 1
   constexpr int X2 = KVT == KV_BF16 ? 4 : (KVT == KV_FP8 ? 2 : 1);
-  const size_t rows = (size_t)p.Hkv * p.page_size;
-  const size_t k_row = (size_t)p.d_qk * X2 / 2, v_row = (size_t)p.d_vo * X2 / 2;
+  // offsets inside one page in 32 bits (the host bounds a page below 2^31 bytes)
+  const uint32_t rows = (uint32_t)p.Hkv * p.page_size;
+  const uint32_t k_row = (uint32_t)p.d_qk * X2 / 2, v_row = (uint32_t)p.d_vo * X2 / 2;
   uint8_t* page_base = p.cache + (size_t)page * rows * (k_row + v_row);
-  const size_t sf_page = rows * (size_t)(ku + vu);
+  uint8_t* sf_base = KVT == KV_NVFP4 ? p.sf + (size_t)page * rows * kvu : nullptr;
   float ks = 1.f, vs = 1.f;
   if (KVT != KV_BF16) {
     ks = __ldg(p.k_scale);
@@ -120,30 +121,41 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kv_kernel(const Appe
   const float yk = __frcp_rn(ks), yv = __frcp_rn(vs);
   const float lim_k = recip_ok(ks) ? fminf(0x1p100f * fabsf(ks), 0x1p100f) : 0.f;
   const float lim_v = recip_ok(vs) ? fminf(0x1p100f * fabsf(vs), 0x1p100f) : 0.f;
-  // the 32 input bytes of unit u
-  auto src_of = [&](int u) -> const uint4* {
-    const int h = u / (ku + vu), w = u % (ku + vu);
-    return reinterpret_cast<const uint4*>(w < ku ? p.k_new + ((size_t)i * p.Hkv + h) * p.d_qk + w * 16
-                                                 : p.v_new + ((size_t)i * p.Hkv + h) * p.d_vo + (w - ku) * 16);
+  // unit u of the token is unit w of kv head h (h = u / kvu, w = u % kvu; a head's K units
+  // first, then its V units); a lane's units are 32 apart, so (h, w) advances by adding 32
+  // to w and carrying whole heads, without a division per unit
+  const uint16_t* k_tok = p.k_new + (size_t)i * p.Hkv * p.d_qk;
+  const uint16_t* v_tok = p.v_new + (size_t)i * p.Hkv * p.d_vo;
+  auto src_of = [&](int h, int w) -> const uint4* {
+    return reinterpret_cast<const uint4*>(w < ku ? k_tok + (h * p.d_qk + w * 16) : v_tok + (h * p.d_vo + (w - ku) * 16));
   };
+  auto carry = [&](int& h, int& w) {
+    while (w >= kvu) {
+      w -= kvu;
+      ++h;
+    }
+  };
+  int h = 0, w = lane;
+  carry(h, w);
   // each lane's next unit is loaded before the current one is converted, so two units'
   // loads of each warp are in flight (the kernel waits on memory latency otherwise)
   uint4 a_n = make_uint4(0, 0, 0, 0), c_n = a_n;
   if (lane < units) {
-    a_n = __ldg(src_of(lane));
-    c_n = __ldg(src_of(lane) + 1);
+    a_n = __ldg(src_of(h, w));
+    c_n = __ldg(src_of(h, w) + 1);
   }
   for (int u = lane; u < units; u += 32) {
-    const int h = u / (ku + vu), w = u % (ku + vu);
     const bool is_k = w < ku;
     const int blk = is_k ? w : w - ku;
+    int hn = h, wn = w + 32;
+    carry(hn, wn);
     const uint4 a = a_n, c = c_n;
     if (u + 32 < units) {
-      a_n = __ldg(src_of(u + 32));
-      c_n = __ldg(src_of(u + 32) + 1);
+      a_n = __ldg(src_of(hn, wn));
+      c_n = __ldg(src_of(hn, wn) + 1);
     }
-    const size_t row = (size_t)h * p.page_size + slot;
-    uint8_t* dst = page_base + (is_k ? row * k_row : rows * k_row + row * v_row) + (size_t)blk * 16 * X2 / 2;
+    const uint32_t row = (uint32_t)h * p.page_size + slot;
+    uint8_t* dst = page_base + (is_k ? row * k_row : rows * k_row + row * v_row) + (uint32_t)blk * 16 * X2 / 2;
     if constexpr (KVT == KV_BF16) {
       reinterpret_cast<uint4*>(dst)[0] = a;
       reinterpret_cast<uint4*>(dst)[1] = c;
@@ -199,10 +211,11 @@ __global__ void __launch_bounds__(32 * kAppendWarps) append_kv_kernel(const Appe
           }
         }
         *reinterpret_cast<uint2*>(dst) = make_uint2(o[0], o[1]);
-        uint8_t* sfp = p.sf + (size_t)page * sf_page + (is_k ? row * ku : rows * ku + row * vu) + blk;
-        *sfp = (uint8_t)sf_code;
+        sf_base[(is_k ? row * ku : rows * ku + row * vu) + blk] = (uint8_t)sf_code;
       }
     }
+    h = hn;
+    w = wn;
   }
 }
 

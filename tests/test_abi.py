@@ -130,6 +130,8 @@ def test_append_rejects_bad_arguments(lib):
     assert _append(lib, dt=1, ks=FAKE + 2, vs=FAKE) == pa.PA_ERR_ALIGNMENT
     assert _append(lib, k=FAKE + 8) == pa.PA_ERR_ALIGNMENT
     assert _append(lib, cache=FAKE + 8) == pa.PA_ERR_ALIGNMENT
+    # one page of 2^14 kv heads x 64 rows x 2048 bytes of bf16 K and V: 2^31 bytes
+    assert _append(lib, hkv=1 << 14, ps=64, dqk=512, dvo=512) == pa.PA_ERR_UNSUPPORTED
 
 
 def test_mode_setters_reject_other_values(lib):
