@@ -836,7 +836,9 @@ int paged_attn_append_kv(const void* k_new, const void* v_new, const int32_t* ap
   p.d_vo = head_dim_vo;
   p.page_size = page_size;
   prof_mark(static_cast<cudaStream_t>(stream), true);
-  const cudaError_t e = launch_append_kv(kv_dtype, p, static_cast<cudaStream_t>(stream));
+  int smem_optin = 0;
+  const int sms = device_sms(&smem_optin);
+  const cudaError_t e = launch_append_kv(kv_dtype, p, sms, static_cast<cudaStream_t>(stream));
   prof_mark(static_cast<cudaStream_t>(stream), false);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   static const char* kv_names[3] = {"bf16", "fp8", "nvfp4"};

@@ -92,6 +92,6 @@ int prefill_smem_bytes(int kvt, int dqk, int dvo);
 // Two-CTA clusters of the bf16 prefill kernel that fit on the device at once.
 int prefill_pair_clusters(int dqk, int dvo);
 // New tokens' bf16 K / V -> the paged cache in its element type (quantise-on-write).
-cudaError_t launch_append_kv(int kvt, const AppendParams& p, cudaStream_t s);
+cudaError_t launch_append_kv(int kvt, const AppendParams& p, int sms, cudaStream_t s);
 
 }  // namespace pa

@@ -207,3 +207,28 @@ def test_append_many_sequences(dt):
     _assert_bytes_equal(cache, ref_cache, "1100 sequences")
     if dt == ac.NVFP4:
         _assert_bytes_equal(sf, ref_sf, "1100 sequences, scales")
+
+
+@pytest.mark.parametrize("per_sm", [72, 144])
+@pytest.mark.parametrize("dt", [ac.BF16, ac.FP8, ac.NVFP4])
+def test_append_several_tokens_per_warp(dt, per_sm):
+    """Appends large enough that each warp writes two (72 new tokens per SM) or four (144)
+    consecutive tokens, over sequences of 0 to 90 new tokens: a warp's tokens cross the
+    ends of sequences, empty ones among them."""
+    import numpy as np
+    import torch
+    ensure_built()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    rng = np.random.default_rng(300 + dt + per_sm)
+    n_new = []
+    while sum(n_new) < per_sm * sms:
+        n_new.append(int(rng.integers(0, 91)) if rng.random() > 0.1 else 0)
+    kv_lens = [n + int(x) for n, x in zip(n_new, rng.integers(0, 50, size=len(n_new)))]
+    case = ac.make(kv_lens=kv_lens, n_new=n_new, Hkv=1, d_qk=256, d_vo=256, page_size=16, kv_dtype=dt,
+                   seed=400 + dt + per_sm, k_scale=0.05, v_scale=0.02)
+    cache, sf, code = _run_gpu(case)
+    ref_cache, ref_sf, skipped = _oracle(case)
+    assert code == 0 and skipped == 0
+    _assert_bytes_equal(cache, ref_cache, f"{sum(n_new)} new tokens")
+    if dt == ac.NVFP4:
+        _assert_bytes_equal(sf, ref_sf, f"{sum(n_new)} new tokens, scales")
